@@ -1,0 +1,217 @@
+"""FP64 CPU oracle for the fine-grained-scaled FP8 GEMM D = C + A @ B.T.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, calls or links this
+package: only the tests, the smoke check and the benchmark's CPU-baseline leg do.
+It shares no code with the CUDA library (``fp8_gemm_nt_gb300``) and imports nothing
+from it; both sides consume the same seeded bytes from ``workloads``.
+
+Sources. Citations name the DeepGEMM README as reproduced on the page "Weight
+gradient kernels for dense and MoE models #95" (gitblind.noratr.app, DeepGEMM pull
+95), by README section, plus the Hindi summary page "DeepGEMM: ... FP8 GEMM kernel"
+(hi.news.hada.io topic 19459) where it restates the same section:
+
+* "Interfaces / Notices": the naming convention D = C + A @ B, the NT layout
+  (fp8_gemm_nt computes D = C + A @ B.T), and the SM100 scale format "packed UE8M0,
+  four UE8M0 in one int", LHS scales "TMA-aligned and transposed".
+* "Grouped GEMMs (contiguous layout)": only M is grouped; N and K are fixed; each
+  expert's token rows are concatenated and every segment is aligned to the M block.
+* "Grouped GEMMs (masked layout)": a mask tensor gives each group's valid rows and
+  only those are computed.
+
+The pages print no formula beyond D = C + A @ B.T, and no scale granularity. This
+oracle therefore writes out the plain definition with the granularity the workload
+names (A: one scale per row per 128-wide K-group; B: one scale per 128x128 block):
+
+    D[m, n] = C[m, n] + sum_g sA[m, g] * sB[n // 128, g] * sum_{k in group g} A[m, k] * B[n, k]
+
+Readings where the pages are silent (each one is listed in the design notes):
+E4M3 is the OCP "E4M3FN" encoding (bias 7, no infinities, S.1111.111 is NaN, max
+448); UE8M0 code e means 2**(e - 127) and 255 is NaN; in a packed word, K-group
+4q + j sits in byte j (least significant first) of word q; scales are stored
+MN-major with the MN extent padded to a multiple of four words; the B scales use
+the same MN-major packing over the N-block index.
+
+Exactness. Every E4M3 value is an integer multiple of 2**-9 below 2**9, so each
+product A*B is a multiple of 2**-18 below 2**18 and a 128-term group sum stays below
+2**25 on the same 2**-18 grid: it is exact in FP64 in any summation order. Scaling
+by powers of two is exact (away from the FP64 range ends), so the only rounding in
+the result is the FP64 sum over K-groups. The group products use numpy's matmul as
+a library step; its blocking cannot change an exact result.
+
+Pins: tests/test_oracle_pins.py checks this module against the OCP code tables,
+torch's own FP8/BF16 decoders, brute-force rational arithmetic on tiny inputs,
+identity/one-hot operands, exact power-of-two scale invariance, the C-only case and
+the grouped-equals-per-expert-dense identity; planted mistakes must fail a pin.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+
+GROUP_K = 128
+BLOCK_N = 128
+
+
+# --------------------------------------------------------------------------------------
+# number formats
+# --------------------------------------------------------------------------------------
+
+def _e4m3_table() -> np.ndarray:
+    """All 256 E4M3FN codes decoded from the format's definition."""
+    t = np.empty(256, np.float64)
+    for code in range(256):
+        s = -1.0 if code & 0x80 else 1.0
+        e = (code >> 3) & 0xF
+        m = code & 0x7
+        if e == 0xF and m == 0x7:
+            t[code] = np.nan                      # the only NaN pattern; no infinities
+        elif e == 0:
+            t[code] = s * (m / 8.0) * 2.0 ** -6   # subnormal
+        else:
+            t[code] = s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return t
+
+
+_E4M3 = _e4m3_table()
+
+
+def decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    """E4M3 bytes -> float64 ("FP8 E4M3" operands, README "Interfaces / Notices")."""
+    return _E4M3[np.asarray(codes, dtype=np.uint8)]
+
+
+def decode_ue8m0(codes: np.ndarray) -> np.ndarray:
+    """UE8M0 scale codes -> float64: 2**(e-127); code 255 is NaN (README "Interfaces / Notices")."""
+    e = np.asarray(codes, dtype=np.int64)
+    out = np.ldexp(1.0, e - 127)
+    return np.where(e == 255, np.nan, out)
+
+
+def decode_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 (a bf16 is the upper half of an IEEE fp32)."""
+    u32 = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return u32.view(np.float32).astype(np.float64)
+
+
+def unpack_sf(words: np.ndarray, mn: int, kgroups: int) -> np.ndarray:
+    """Packed UE8M0 words [ceil(kgroups/4), >=mn] (MN-major) -> codes [mn, kgroups].
+
+    "SM100 requires scaling factors in packed UE8M0 format, which packs 4 UE8M0
+    into a single torch.int" and the LHS factor is "transposed" (README "Interfaces /
+    Notices"). Reading: K-group g is byte g % 4 of word g // 4 of its row.
+    """
+    w = np.asarray(words).view(np.uint32)
+    out = np.empty((mn, kgroups), np.uint8)
+    for g in range(kgroups):
+        out[:, g] = (w[g // 4, :mn] >> np.uint32(8 * (g % 4))) & np.uint32(0xFF)
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# the GEMM forms
+# --------------------------------------------------------------------------------------
+
+def _scaled_gemm(a_codes, sa_codes, b_codes, sb_codes, K: int) -> np.ndarray:
+    """sum_g sA[:, g] * sB[n // 128, g] * (A_g @ B_g.T) in FP64.
+
+    a_codes: E4M3 [R, K]; sa_codes: UE8M0 [R, KG]; b_codes: E4M3 [N, K];
+    sb_codes: UE8M0 [ceil(N/128), KG] (one per 128x128 block of B).
+    """
+    KG = K // GROUP_K
+    N = b_codes.shape[0]
+    A = decode_e4m3(a_codes)                                                # [R, K]
+    B = decode_e4m3(b_codes)                                                # [N, K]
+    sA = decode_ue8m0(sa_codes)                                             # [R, KG]
+    sB = decode_ue8m0(sb_codes)[np.arange(N) // BLOCK_N]                    # [N, KG]
+    D = np.zeros((A.shape[0], N), np.float64)
+    for g in range(KG):
+        ks = slice(g * GROUP_K, (g + 1) * GROUP_K)
+        partial = A[:, ks] @ B[:, ks].T                                     # exact
+        D += sA[:, g:g + 1] * partial * sB[None, :, g]
+    return D
+
+
+def fp8_gemm_nt(a, sfa, b, sfb, c: Optional[np.ndarray], M: int, N: int, K: int,
+                rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """D = C + A @ B.T with fine-grained scales, in FP64 (README "Interfaces / Notices",
+    "Normal dense GEMMs (non-grouped)").
+
+    a: uint8 [M, K]; sfa: int32 [ceil(KG/4), ceil4(M)]; b: uint8 [N, K];
+    sfb: int32 [ceil(KG/4), ceil4(ceil(N/128))]; c: bf16 bits [M, N] or None.
+    rows: optional subset of output rows to compute (default all). Returns [len(rows), N].
+    """
+    assert K % GROUP_K == 0
+    KG = K // GROUP_K
+    rows = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    sa = unpack_sf(sfa, M, KG)[rows]
+    sb = unpack_sf(sfb, -(-N // BLOCK_N), KG)
+    D = _scaled_gemm(np.asarray(a)[rows], sa, np.asarray(b), sb, K)
+    if c is not None:
+        D = decode_bf16(np.asarray(c)[rows]) + D
+    return D
+
+
+def m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, m_indices, M_total: int, N: int, K: int,
+                                     G: int, rows: Optional[Sequence[int]] = None):
+    """Contiguous M-grouped GEMM (README "Grouped GEMMs (contiguous layout)").
+
+    Row r of A belongs to expert m_indices[r] and is multiplied by that expert's B
+    [N, K] and scales; rows with m_indices == -1 are padding and produce nothing.
+    Returns (D [R, N] float64 with NaN on padding rows, valid [R] bool).
+    """
+    KG = K // GROUP_K
+    rows = np.arange(M_total) if rows is None else np.asarray(rows, dtype=np.int64)
+    idx = np.asarray(m_indices)[rows]
+    D = np.full((len(rows), N), np.nan)
+    sa = unpack_sf(sfa, M_total, KG)
+    NB = -(-N // BLOCK_N)
+    for g in range(G):
+        sel = np.nonzero(idx == g)[0]
+        if len(sel) == 0:
+            continue
+        r = rows[sel]
+        D[sel] = _scaled_gemm(np.asarray(a)[r], sa[r], np.asarray(b[g]), unpack_sf(sfb[g], NB, KG), K)
+    return D, idx >= 0
+
+
+def m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, masked_m, G: int, max_m: int, N: int, K: int,
+                                 groups: Optional[Sequence[int]] = None):
+    """Masked M-grouped GEMM (README "Grouped GEMMs (masked layout)").
+
+    For group g only rows r < masked_m[g] of A[g] are computed, against B[g].
+    Returns (D [len(groups), max_m, N] float64 with NaN on masked rows,
+    valid [len(groups), max_m] bool). A count above max_m is clamped to max_m.
+    """
+    KG = K // GROUP_K
+    NB = -(-N // BLOCK_N)
+    groups = list(range(G)) if groups is None else list(groups)
+    D = np.full((len(groups), max_m, N), np.nan)
+    valid = np.zeros((len(groups), max_m), bool)
+    for i, g in enumerate(groups):
+        m = int(min(max(int(masked_m[g]), 0), max_m))
+        valid[i, :m] = True
+        if m:
+            sa = unpack_sf(sfa[g], max_m, KG)[:m]
+            D[i, :m] = _scaled_gemm(np.asarray(a[g])[:m], sa, np.asarray(b[g]),
+                                    unpack_sf(sfb[g], NB, KG), K)
+    return D, valid
+
+
+# --------------------------------------------------------------------------------------
+# comparison (the parity bar)
+# --------------------------------------------------------------------------------------
+
+def parity_report(d: np.ndarray, ref: np.ndarray, rel: float = 1e-2, abs_rms: float = 1e-2):
+    """Per-element bound |d - ref| <= rel*|ref| + abs_rms*rms(ref), and the
+    cosine-style difference 1 - 2*sum(d*ref)/(sum(d^2)+sum(ref^2)). d, ref float64."""
+    d = np.asarray(d, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    err = np.abs(d - ref)
+    bound = rel * np.abs(ref) + abs_rms * rms
+    bad = ~(err <= bound)
+    denom = float((d * d).sum() + (ref * ref).sum())
+    diff = 0.0 if denom == 0.0 else 1.0 - 2.0 * float((d * ref).sum()) / denom
+    return dict(n=int(ref.size), n_bad=int(bad.sum()), max_err=float(err.max()) if ref.size else 0.0,
+                rms=rms, diff=diff, ok=bool(not bad.any() and diff < 1e-3))

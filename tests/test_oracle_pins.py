@@ -1,0 +1,428 @@
+"""Pins for the FP64 oracle: checks against things other than the oracle itself.
+
+Each pin is a function of the oracle module so that the same pins can be run against
+deliberately broken copies (planted on the CPU, below): every planted mistake must
+fail at least one pin. Sources of truth used here:
+  * the OCP E4M3FN and UE8M0 code tables (fixed values) and torch's own decoders;
+  * exact rational arithmetic (fractions.Fraction) over the definition, on tiny inputs;
+  * closed forms: identity and one-hot operands, the C-only case;
+  * exact invariances: power-of-two scale shifts act on exactly one row / one block;
+  * the grouped forms equal the dense form run per expert (README "Grouped GEMMs").
+"""
+from __future__ import annotations
+
+import contextlib
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+
+
+# --------------------------------------------------------------------------------------
+# helpers that do not use the oracle's arithmetic
+# --------------------------------------------------------------------------------------
+
+def torch_e4m3(codes) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def words_from_codes(codes: np.ndarray) -> np.ndarray:
+    """Codes [MN, KG] -> packed words, written with explicit integer arithmetic per word."""
+    MN, KG = codes.shape
+    KP = -(-KG // 4)
+    out = np.zeros((KP, 4 * (-(-MN // 4))), np.int64)
+    for q in range(KP):
+        for i in range(MN):
+            w = 0
+            for j in range(4):
+                g = 4 * q + j
+                if g < KG:
+                    w += int(codes[i, g]) * (256 ** j)
+            out[q, i] = w
+    return out.astype(np.uint32).view(np.int32)
+
+
+def random_codes(rng, shape, nan_free=True):
+    c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    if nan_free:
+        c[(c & 0x7F) == 0x7F] = 0x3F
+    return c
+
+
+def brute_force(a, ea, b, eb_blocks, c_bits=None):
+    """Exact rational D = C + sum_k sA*sB*A*B, with torch decoding the bytes."""
+    M, K = a.shape
+    N = b.shape[0]
+    A = [[Fraction(float(v)) for v in row] for row in torch_e4m3(a)]
+    B = [[Fraction(float(v)) for v in row] for row in torch_e4m3(b)]
+    two = Fraction(2)
+    D = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                g = k // 128
+                acc += A[m][k] * B[n][k] * two ** (int(ea[m, g]) - 127) * two ** (int(eb_blocks[n // 128, g]) - 127)
+            if c_bits is not None:
+                cv = torch.tensor([int(c_bits[m, n])], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+                acc += Fraction(float(cv.to(torch.float64).item()))
+            D[m, n] = float(acc)
+    return D
+
+
+def dense(O_, a, ea, b, eb, c=None):
+    M, K = a.shape
+    N = b.shape[0]
+    return O_.fp8_gemm_nt(a, words_from_codes(ea), b, words_from_codes(eb), c, M, N, K)
+
+
+# --------------------------------------------------------------------------------------
+# pins (each takes the oracle module under test)
+# --------------------------------------------------------------------------------------
+
+def pin_e4m3_table(O_):
+    known = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x3C: 1.5, 0x40: 2.0, 0x7E: 448.0, 0xFE: -448.0, 0x80: -0.0, 0xB8: -1.0, 0x81: -(2.0 ** -9)}
+    for code, v in known.items():
+        assert O_.decode_e4m3(np.array([code], np.uint8))[0] == v, hex(code)
+    assert np.isnan(O_.decode_e4m3(np.array([0x7F, 0xFF], np.uint8))).all()
+    codes = np.arange(256, dtype=np.uint8)
+    ours, ref = O_.decode_e4m3(codes), torch_e4m3(codes)
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert np.array_equal(np.signbit(ours[ok]), np.signbit(ref[ok]))
+
+
+def pin_ue8m0_table(O_):
+    codes = np.array([0, 1, 126, 127, 128, 200, 254], np.uint8)
+    expect = [2.0 ** -127, 2.0 ** -126, 0.5, 1.0, 2.0, 2.0 ** 73, 2.0 ** 127]
+    assert list(O_.decode_ue8m0(codes)) == expect
+    assert np.isnan(O_.decode_ue8m0(np.array([255], np.uint8))[0])
+    if hasattr(torch, "float8_e8m0fnu"):
+        all_codes = np.arange(255, dtype=np.uint8)
+        ref = torch.from_numpy(all_codes).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+        assert np.array_equal(O_.decode_ue8m0(all_codes), ref)
+
+
+def pin_bf16(O_):
+    x = np.array([0.0, 1.0, -2.5, 3.140625, 1e-3, -7e4, 2.0 ** -130], np.float32)
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O_.decode_bf16(bits), ref)
+
+
+def pin_unpack(O_):
+    # word for row i of K-quad q holds groups 4q..4q+3 in bytes 0..3 (LSB first)
+    words = np.array([[0x04030201, 0x08070605, 0, 0], [0x0C0B0A09, 0x100F0E0D, 0, 0]], np.uint32).view(np.int32)
+    codes = O_.unpack_sf(words, 2, 7)
+    assert codes.tolist() == [[1, 2, 3, 4, 9, 10, 11], [5, 6, 7, 8, 13, 14, 15]]
+
+
+def pin_brute_force(O_):
+    rng = np.random.default_rng(7)
+    for (M, N, K, with_c) in [(1, 1, 128, False), (2, 3, 256, True), (3, 130, 256, True), (4, 2, 384, False)]:
+        a = random_codes(rng, (M, K))
+        b = random_codes(rng, (N, K))
+        ea = rng.integers(120, 135, size=(M, K // 128)).astype(np.uint8)
+        eb = rng.integers(120, 135, size=(-(-N // 128), K // 128)).astype(np.uint8)
+        c = rng.integers(0, 2 ** 16, size=(M, N)).astype(np.uint16) if with_c else None
+        if c is not None:
+            c[(c & 0x7F80) == 0x7F80] = 0x3F80     # keep C finite
+        got = dense(O_, a, ea, b, eb, c)
+        ref = brute_force(a, ea, b, eb, c)
+        np.testing.assert_allclose(got, ref, rtol=1e-14, atol=1e-300)
+
+
+def pin_identity(O_):
+    # A = [I | 0] with unit scales gives D[i, n] = B[n, i] * sB(block of n, group 0)
+    rng = np.random.default_rng(11)
+    M, N, K = 4, 256, 256
+    a = np.zeros((M, K), np.uint8)
+    a[np.arange(M), np.arange(M)] = 0x38            # 1.0
+    b = random_codes(rng, (N, K))
+    ea = np.full((M, 2), 127, np.uint8)
+    eb = np.array([[127, 127], [129, 120]], np.uint8)  # block 1 scaled by 4 in group 0
+    got = dense(O_, a, ea, b, eb)
+    Bv = torch_e4m3(b)
+    expect = Bv[:, :M].T * np.where(np.arange(N) >= 128, 4.0, 1.0)[None, :]
+    assert np.array_equal(got, expect)
+
+
+def pin_one_hot(O_):
+    rng = np.random.default_rng(12)
+    M, N, K = 3, 200, 384
+    b = random_codes(rng, (N, K))
+    for (m, k) in [(0, 5), (1, 200), (2, 383)]:
+        a = np.zeros((M, K), np.uint8)
+        a[m, k] = 0x40                              # 2.0
+        ea = np.full((M, 3), 127, np.uint8)
+        ea[m, k // 128] = 125                       # x 1/4
+        eb = np.full((2, 3), 127, np.uint8)
+        eb[1, k // 128] = 130                       # block 1 x 8
+        got = dense(O_, a, ea, b, eb)
+        expect = np.zeros((M, N))
+        expect[m] = 2.0 * 0.25 * torch_e4m3(b[:, k]) * np.where(np.arange(N) >= 128, 8.0, 1.0)
+        assert np.array_equal(got, expect)
+
+
+def pin_pow2_invariance(O_):
+    rng = np.random.default_rng(13)
+    M, N, K = 5, 300, 512
+    a, b = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    ea = rng.integers(124, 131, size=(M, 4)).astype(np.uint8)
+    eb = rng.integers(124, 131, size=(3, 4)).astype(np.uint8)
+    base = dense(O_, a, ea, b, eb)
+    # shift every group of row 2 by +3: row 2 x 8, all other rows unchanged, bit-exactly
+    ea2 = ea.copy(); ea2[2] += 3
+    got = dense(O_, a, ea2, b, eb)
+    expect = base.copy(); expect[2] *= 8.0
+    assert np.array_equal(got, expect)
+    # shift every group of B block 1 by -2: columns 128..255 x 1/4, others unchanged
+    eb2 = eb.copy(); eb2[1] -= 2
+    got = dense(O_, a, ea, b, eb2)
+    expect = base.copy(); expect[:, 128:256] *= 0.25
+    assert np.array_equal(got, expect)
+    # a single group's scale only touches that group's contribution
+    z = a.copy(); z[:, 128:] = 0
+    only_g0 = dense(O_, z, ea, b, eb)
+    ea3 = ea.copy(); ea3[:, 1:] = 127 - 20
+    assert np.array_equal(dense(O_, z, ea3, b, eb), only_g0)
+
+
+def pin_c_only(O_):
+    rng = np.random.default_rng(14)
+    M, N, K = 3, 130, 256
+    c = rng.integers(0, 2 ** 16, size=(M, N)).astype(np.uint16)
+    c[(c & 0x7F80) == 0x7F80] = 0x4000
+    got = dense(O_, np.zeros((M, K), np.uint8), np.full((M, 2), 127, np.uint8),
+                random_codes(rng, (N, K)), np.full((2, 2), 127, np.uint8), c)
+    ref = torch.from_numpy(c.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(got, ref)
+
+
+def pin_dequantised_route(O_):
+    # Same value by another route: dequantise whole operands, one FP64 matmul over all K.
+    p = W.make_dense(17, 260, 640, seed=5, with_c=True)
+    got = O_.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K)
+    KG = p.K // 128
+    ea = np.stack([(p.sfa.view(np.uint32)[g // 4, :p.M] >> (8 * (g % 4))) & 0xFF for g in range(KG)], 1)
+    NB = -(-p.N // 128)
+    eb = np.stack([(p.sfb.view(np.uint32)[g // 4, :NB] >> (8 * (g % 4))) & 0xFF for g in range(KG)], 1)
+    Af = torch_e4m3(p.a) * np.exp2(np.repeat(ea.astype(np.float64) - 127, 128, axis=1))
+    Bf = torch_e4m3(p.b) * np.exp2(np.repeat(np.repeat(eb.astype(np.float64) - 127, 128, axis=0)[:p.N], 128, axis=1))
+    Cf = torch.from_numpy(p.c.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_allclose(got, Cf + Af @ Bf.T, rtol=1e-12, atol=1e-12)
+
+
+def pin_contiguous_equals_dense(O_):
+    p = W.make_contiguous(G=3, tokens=300, N=144, K=256, seed=3, counts=[130, 0, 170])
+    D, valid = O_.m_grouped_fp8_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K, p.G)
+    assert p.M_total == 256 + 256
+    assert np.array_equal(valid, p.m_indices >= 0)
+    assert np.isnan(D[~valid]).all() and not np.isnan(D[valid]).any()
+    KG = p.K // 128
+    ea = np.stack([(p.sfa.view(np.uint32)[g // 4, :p.M_total] >> (8 * (g % 4))) & 0xFF for g in range(KG)], 1)
+    for g in range(p.G):
+        r = np.nonzero(p.m_indices == g)[0]
+        if len(r) == 0:
+            continue
+        NB = -(-p.N // 128)
+        eb = np.stack([(p.sfb[g].view(np.uint32)[q // 4, :NB] >> (8 * (q % 4))) & 0xFF for q in range(KG)], 1)
+        ref = dense(O_, p.a[r], ea[r].astype(np.uint8), p.b[g], eb.astype(np.uint8))
+        assert np.array_equal(D[r], ref)
+        # and against exact rationals on a few rows
+        bf = brute_force(p.a[r[:2]], ea[r[:2]], p.b[g], eb)
+        np.testing.assert_allclose(D[r[:2]], bf, rtol=1e-14)
+
+
+def pin_masked_equals_dense(O_):
+    p = W.make_masked(G=4, max_m=40, N=136, K=256, seed=4, masked_m=[0, 40, 17, 1])
+    D, valid = O_.m_grouped_fp8_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, p.masked_m, p.G, p.max_m, p.N, p.K)
+    assert valid.sum(1).tolist() == [0, 40, 17, 1]
+    assert np.isnan(D[~valid]).all() and not np.isnan(D[valid]).any()
+    KG = p.K // 128
+    NB = -(-p.N // 128)
+    for g in range(p.G):
+        m = int(p.masked_m[g])
+        if m == 0:
+            continue
+        ea = np.stack([(p.sfa[g].view(np.uint32)[q // 4, :m] >> (8 * (q % 4))) & 0xFF for q in range(KG)], 1)
+        eb = np.stack([(p.sfb[g].view(np.uint32)[q // 4, :NB] >> (8 * (q % 4))) & 0xFF for q in range(KG)], 1)
+        bf = brute_force(p.a[g, :min(m, 2)], ea[:2], p.b[g], eb)
+        np.testing.assert_allclose(D[g, :min(m, 2)], bf, rtol=1e-14)
+        ref = dense(O_, p.a[g, :m], ea.astype(np.uint8), p.b[g], eb.astype(np.uint8))
+        assert np.array_equal(D[g, :m], ref)
+
+
+PINS = [pin_e4m3_table, pin_ue8m0_table, pin_bf16, pin_unpack, pin_brute_force, pin_identity,
+        pin_one_hot, pin_pow2_invariance, pin_c_only, pin_dequantised_route,
+        pin_contiguous_equals_dense, pin_masked_equals_dense]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(pin):
+    pin(O)
+
+
+# --------------------------------------------------------------------------------------
+# planted mistakes: each must be caught by at least one pin
+# --------------------------------------------------------------------------------------
+
+def _mut_table(table_fn):
+    @contextlib.contextmanager
+    def ctx():
+        old = O._E4M3.copy()
+        O._E4M3[:] = table_fn(old)
+        try:
+            yield
+        finally:
+            O._E4M3[:] = old
+    return ctx
+
+
+def _mut_attr(name, new):
+    @contextlib.contextmanager
+    def ctx():
+        old = getattr(O, name)
+        setattr(O, name, new(old))
+        try:
+            yield
+        finally:
+            setattr(O, name, old)
+    return ctx
+
+
+def _subnormal_with_implicit_one(t):
+    t = t.copy()
+    for code in range(256):
+        if (code >> 3) & 0xF == 0:
+            s = -1.0 if code & 0x80 else 1.0
+            t[code] = s * (1 + (code & 7) / 8) * 2.0 ** -6
+    return t
+
+
+def _bias_off_by_one(old):
+    return lambda codes: np.ldexp(1.0, np.asarray(codes, np.int64) - 126)
+
+
+def _byte_order_reversed(old):
+    def f(words, mn, kgroups):
+        w = np.asarray(words).view(np.uint32)
+        out = np.empty((mn, kgroups), np.uint8)
+        for g in range(kgroups):
+            out[:, g] = (w[g // 4, :mn] >> np.uint32(8 * (3 - g % 4))) & np.uint32(0xFF)
+        return out
+    return f
+
+
+def _make_scaled(mode):
+    def factory(old):
+        def f(a_codes, sa_codes, b_codes, sb_codes, K):
+            KG = K // 128
+            N = b_codes.shape[0]
+            A = O.decode_e4m3(a_codes)
+            B = O.decode_e4m3(b_codes)
+            if mode == "transposed_b":   # B read as if stored [K, N]
+                B = B.reshape(-1)[: N * K].reshape(K, N).T if N != K else B.T
+            sA = O.decode_ue8m0(sa_codes)
+            blk = (np.arange(N) % 128) if mode == "block_mod" else (np.arange(N) // 128)
+            blk = np.minimum(blk, sb_codes.shape[0] - 1)
+            sB = O.decode_ue8m0(sb_codes)[blk]
+            D = np.zeros((A.shape[0], N))
+            groups = range(KG - 1) if mode == "drop_last_group" else range(KG)
+            for g in groups:
+                ks = slice(g * 128, (g + 1) * 128)
+                ga = 0 if mode == "first_scale_only" else g
+                D += sA[:, ga:ga + 1] * (A[:, ks] @ B[:, ks].T) * sB[None, :, g]
+            return D
+        return f
+    return factory
+
+
+def _c_sign(old):
+    def f(a, sfa, b, sfb, c, M, N, K, rows=None):
+        d = old(a, sfa, b, sfb, None, M, N, K, rows)
+        if c is not None:
+            r = np.arange(M) if rows is None else np.asarray(rows)
+            d = d - O.decode_bf16(np.asarray(c)[r])
+        return d
+    return f
+
+
+def _contig_negative_index(old):
+    def f(a, sfa, b, sfb, m_indices, M_total, N, K, G, rows=None):
+        rows = np.arange(M_total) if rows is None else np.asarray(rows)
+        idx = np.asarray(m_indices)[rows]
+        D = np.full((len(rows), N), np.nan)
+        sa = O.unpack_sf(sfa, M_total, K // 128)
+        for r_i, r in enumerate(rows):
+            g = idx[r_i]          # -1 silently selects the last expert
+            D[r_i] = O._scaled_gemm(a[r:r + 1], sa[r:r + 1], b[g], O.unpack_sf(sfb[g], -(-N // 128), K // 128), K)[0]
+        return D, idx >= 0
+    return f
+
+
+def _masked_off_by_one(old):
+    def f(a, sfa, b, sfb, masked_m, G, max_m, N, K, groups=None):
+        mm = np.minimum(np.asarray(masked_m) + 1, max_m)
+        return old(a, sfa, b, sfb, mm, G, max_m, N, K, groups)
+    return f
+
+
+MUTANTS = {
+    "subnormal_implicit_one": _mut_table(_subnormal_with_implicit_one),
+    "sign_ignored": _mut_table(lambda t: np.abs(t)),
+    "ue8m0_bias_126": _mut_attr("decode_ue8m0", _bias_off_by_one),
+    "sf_byte_order_reversed": _mut_attr("unpack_sf", _byte_order_reversed),
+    "b_transposed": _mut_attr("_scaled_gemm", _make_scaled("transposed_b")),
+    "b_block_index_mod": _mut_attr("_scaled_gemm", _make_scaled("block_mod")),
+    "dropped_last_group": _mut_attr("_scaled_gemm", _make_scaled("drop_last_group")),
+    "a_scale_first_group_only": _mut_attr("_scaled_gemm", _make_scaled("first_scale_only")),
+    "c_subtracted": _mut_attr("fp8_gemm_nt", _c_sign),
+    "contiguous_pad_uses_last_expert": _mut_attr("m_grouped_fp8_gemm_nt_contiguous", _contig_negative_index),
+    "masked_off_by_one": _mut_attr("m_grouped_fp8_gemm_nt_masked", _masked_off_by_one),
+}
+
+
+@pytest.mark.parametrize("name", list(MUTANTS))
+def test_planted_mistake_is_caught(name):
+    caught = []
+    with MUTANTS[name]():
+        for pin in PINS:
+            try:
+                pin(O)
+            except (AssertionError, ValueError, IndexError):
+                caught.append(pin.__name__)
+    assert caught, f"planted mistake {name} passed every pin"
+
+
+# --------------------------------------------------------------------------------------
+# the input generator (not the method): its quantiser keeps values representable
+# --------------------------------------------------------------------------------------
+
+def test_quantiser_roundtrip_and_minimal_exponent():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((64, 512)).astype(np.float32) * 3
+    x[0, :128] = 0.0
+    q, e = W.quantize_rows(x)
+    deq = torch_e4m3(q) * np.exp2(np.repeat(e.astype(np.float64) - 127, 128, axis=1))
+    np.testing.assert_allclose(deq, x, rtol=2 ** -4, atol=2.0 ** -9 * 4)
+    assert e[0, 0] == 127
+    amax = np.abs(x.reshape(64, 4, 128)).max(2)
+    ok = amax > 0
+    assert (amax[ok] / np.exp2(e[ok].astype(np.float64) - 127) <= 448).all()
+    assert (amax[ok] / np.exp2(e[ok].astype(np.float64) - 128) > 448).all()
+
+
+def test_pack_sf_layout():
+    e = np.arange(1, 1 + 6 * 5, dtype=np.uint8).reshape(6, 5)
+    w = W.pack_sf(e)
+    assert w.shape == (2, 8)
+    assert np.array_equal(w, words_from_codes(e))
+    assert np.array_equal(O.unpack_sf(w, 6, 5), e)
