@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of the fine-grained-scaled FP8 GEMM library on one node.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--headline-only]
+
+One step is one call of the GEMM over one batch of the headline workload: the dense
+decode-shaped problem D = C + A @ B.T with M=128, N=7168, K=16384 (E4M3 operands,
+UE8M0 scales per 1x128 / 128x128, BF16 C and D). Inputs are synthetic (seeded) and
+resident in HBM; several rotating copies keep the per-step footprint above the L2
+size, so every step reads its operands from HBM. Under torchrun each rank runs its
+own replica on its own GPU (the problems are independent: weak scaling, no
+collective on the data path); the timed region is bracketed by a barrier and a
+device synchronisation, and the slowest rank's time is used.
+
+Printed (rank 0): one JSON line with the headline throughput (TFLOPS), the roofline of
+the GEMM kernel, an end-to-end figure through the C ABI with host buffers, the CPU
+oracle's throughput on a bounded sample, the SM clocks seen while timing, and the
+other four workloads measured the same way.
+
+--impl reference times the CPU oracle (the only reference implementation of this
+method in the repository) on the same workload and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+HEADLINE = "dense_decode_128x7168x16384_c"
+METRIC = "FP8 GEMM TFLOPS (device-timed) and % of GB300 dense FP8 tensor peak"
+L2_BYTES = 126 * 2 ** 20
+FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate ratio (4.5 / 2.25 PFLOP/s)
+
+
+# --------------------------------------------------------------------------------------
+# peaks
+# --------------------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return dict(hbm_gbs=float(m["hbm_gbs"]), bf16=float(m["bf16_tflops"]),
+                    bf16_sustained=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# --------------------------------------------------------------------------------------
+# problems on the device
+# --------------------------------------------------------------------------------------
+
+def _nbytes(*arrs):
+    return int(sum(a.nbytes for a in arrs if a is not None))
+
+
+def algorithmic(p):
+    """(flops, bytes) the method must do / move: valid rows only, each operand once."""
+    if isinstance(p, W.Dense):
+        by = _nbytes(p.a, p.sfa, p.b, p.sfb) + (p.c.nbytes if p.c is not None else 0) + p.M * p.N * 2
+        return p.flops, by
+    if isinstance(p, W.Contiguous):
+        v = p.valid_rows
+        used = sorted(set(int(g) for g in p.m_indices if g >= 0))
+        by = v * p.K + p.sfa.nbytes + len(used) * (p.N * p.K + p.sfb[0].nbytes) + v * p.N * 2
+        return p.flops, by
+    mm = np.minimum(p.masked_m, p.max_m)
+    used = int((mm > 0).sum())
+    v = int(mm.sum())
+    by = v * p.K + p.sfa.nbytes + used * (p.N * p.K + p.sfb[0].nbytes) + v * p.N * 2
+    return p.flops, by
+
+
+class DeviceProblem:
+    """R rotating device copies of one workload; launch(i) runs the GEMM on copy i % R."""
+
+    def __init__(self, lib, p, torch, max_bytes=6 << 30):
+        self.lib, self.p, self.torch = lib, p, torch
+        foot = sum(x.nbytes for x in self._host_arrays()) + self._out_bytes()
+        self.R = int(min(max(1, math.ceil(2 * L2_BYTES / foot)), 4096, max(1, max_bytes // foot)))
+        self.copies = [self._upload() for _ in range(self.R)]
+
+    def _host_arrays(self):
+        p = self.p
+        if isinstance(p, W.Dense):
+            return [x for x in (p.a, p.sfa, p.b, p.sfb, p.c) if x is not None]
+        if isinstance(p, W.Contiguous):
+            return [p.a, p.sfa, p.b, p.sfb, p.m_indices]
+        return [p.a, p.sfa, p.b, p.sfb, p.masked_m]
+
+    def _out_bytes(self):
+        p = self.p
+        if isinstance(p, W.Dense):
+            return p.M * p.N * 2
+        if isinstance(p, W.Contiguous):
+            return p.M_total * p.N * 2
+        return p.G * p.max_m * p.N * 2
+
+    def _upload(self):
+        t = self.torch
+        p = self.p
+        f = lambda x: t.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+        if isinstance(p, W.Dense):
+            c = t.from_numpy(p.c.view(np.int16)).view(t.bfloat16).cuda() if p.c is not None else None
+            return dict(a=f(p.a), sfa=f(p.sfa), b=f(p.b), sfb=f(p.sfb), c=c,
+                        d=t.empty((p.M, p.N), dtype=t.bfloat16, device="cuda"))
+        if isinstance(p, W.Contiguous):
+            return dict(a=f(p.a), sfa=f(p.sfa), b=f(p.b), sfb=f(p.sfb), idx=f(p.m_indices),
+                        d=t.empty((p.M_total, p.N), dtype=t.bfloat16, device="cuda"))
+        return dict(a=f(p.a), sfa=f(p.sfa), b=f(p.b), sfb=f(p.sfb), mm=f(p.masked_m),
+                    d=t.empty((p.G, p.max_m, p.N), dtype=t.bfloat16, device="cuda"))
+
+    def launch(self, i):
+        c = self.copies[i % self.R]
+        L, p = self.lib, self.p
+        if isinstance(p, W.Dense):
+            L.dg_fp8_gemm_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
+        elif isinstance(p, W.Contiguous):
+            L.dg_m_grouped_fp8_gemm_nt_contiguous(c["a"], c["sfa"], c["b"], c["sfb"], c["d"], c["idx"])
+        else:
+            L.dg_m_grouped_fp8_gemm_nt_masked(c["a"], c["sfa"], c["b"], c["sfb"], c["d"], c["mm"])
+
+
+def time_steps(torch, prob, steps, warmup, barrier=None):
+    """Warm up, then time exactly `steps` launches back to back. Returns (region_ms,
+    per-launch kernel ms list). Events are recorded on the launching stream."""
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        prob.launch(i)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
+        prob.launch(warmup + i)
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    return evs[0].elapsed_time(evs[-1]), per
+
+
+# --------------------------------------------------------------------------------------
+# end to end through the C ABI with host buffers
+# --------------------------------------------------------------------------------------
+
+def e2e_headline(torch, lib, p, steps, warmup):
+    t = torch
+    host = dict(a=t.from_numpy(p.a).pin_memory(), sfa=t.from_numpy(p.sfa).pin_memory(),
+                b=t.from_numpy(p.b).pin_memory(), sfb=t.from_numpy(p.sfb).pin_memory(),
+                c=t.from_numpy(p.c.view(np.int16)).view(t.bfloat16).pin_memory())
+    out_host = t.empty((p.M, p.N), dtype=t.bfloat16).pin_memory()
+    devb = {k: t.empty_like(v, device="cuda") for k, v in host.items()}
+    d = t.empty((p.M, p.N), dtype=t.bfloat16, device="cuda")
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        lib.dg_fp8_gemm_nt(devb["a"], devb["sfa"], devb["b"], devb["sfb"], devb["c"], d)
+        out_host.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s, e = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return dict(value=p.flops / (ms * 1e-3) / 1e12, unit="TFLOPS", h2d_bytes_per_step=int(h2d),
+                d2h_bytes_per_step=int(d2h), ms_per_step=ms)
+
+
+# --------------------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------------------
+
+REASON_FIELDS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), util=float(parts[4]),
+                                 flags=dict(zip(REASON_FIELDS, [x.lower() == "active" for x in parts[6:10]]))))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["util"] >= 50] or rows
+        reasons = sorted({k for r in busy for k, v in r["flags"].items() if v})
+        return dict(sm_mhz=statistics.median(r["sm"] for r in busy), sm_max_mhz=max(r["max"] for r in rows),
+                    reasons=reasons, samples=len(rows), samples_under_load=len([r for r in rows if r["util"] >= 50]),
+                    window="every timed region of this run")
+
+
+# --------------------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample, in a spawned child process
+# --------------------------------------------------------------------------------------
+
+CPU_CHILD = r"""
+import json, os, sys, time
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import workloads as W, oracle as O
+name, budget = sys.argv[2], float(sys.argv[3])
+p = W.make_workload(name)
+rows_per_call = max(1, min(p.M, int(sys.argv[4])))
+done_rows, t0, calls = 0, time.perf_counter(), 0
+while True:
+    rows = np.arange(calls * rows_per_call, (calls + 1) * rows_per_call) % p.M
+    O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K, rows=rows)
+    done_rows += rows_per_call; calls += 1
+    el = time.perf_counter() - t0
+    if el >= budget or calls >= 64:
+        break
+flops = 2.0 * done_rows * p.N * p.K
+print(json.dumps(dict(seconds=el, flops=flops, rows=done_rows, calls=calls, rows_per_call=rows_per_call)))
+"""
+
+
+def cpu_baseline(name, budget_s=10.0, rows_per_call=16):
+    cores = os.cpu_count() or 1
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=str(cores), OMP_NUM_THREADS=str(cores), CUDA_VISIBLE_DEVICES="")
+    try:
+        out = subprocess.run([sys.executable, "-c", CPU_CHILD, ROOT, name, str(budget_s), str(rows_per_call)],
+                             capture_output=True, text=True, env=env, timeout=600)
+        r = json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, never fatal for the GPU line
+        return dict(value=None, unit="TFLOPS", cores=cores, kind="oracle", sample=f"failed: {e}")
+    return dict(value=r["flops"] / r["seconds"] / 1e12, unit="TFLOPS", cores=cores, kind="oracle",
+                sample=(f"{r['calls']} oracle calls x {r['rows_per_call']} output rows (all N={7168} columns, "
+                        f"K=16384) of {name}; {r['seconds']:.1f} s wall, FP64 numpy/OpenBLAS with {cores} threads"),
+                seconds=r["seconds"])
+
+
+# --------------------------------------------------------------------------------------
+# main
+# --------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        barrier = dist.barrier
+
+    import fp8_gemm_nt_gb300 as L
+    L.load_library()
+    peaks = load_peaks()
+    fp8_peak = FP8_OVER_BF16 * peaks["bf16"]
+
+    gpu_index = local_rank
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        gpu_index = vis.split(",")[local_rank]
+    sampler = ClockSampler(gpu_index)
+
+    # ---- headline
+    p = W.make_workload(HEADLINE)
+    prob = DeviceProblem(L, p, torch)
+    region_ms, per = time_steps(torch, prob, args.steps, args.warmup, barrier)
+    if L.dg_get_device_status() != 0:
+        raise RuntimeError("device status reported an error during the benchmark")
+    t_max = region_ms
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([region_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    flops, alg_bytes = algorithmic(p)
+    ms_per_step = t_max / args.steps
+    value = world * flops * args.steps / (t_max * 1e-3) / 1e12
+    kern_ms = statistics.mean(per)
+    achieved_gbs = alg_bytes / (kern_ms * 1e-3) / 1e9
+
+    # ---- other workloads (rank 0 reports; every rank runs them so that replicas stay symmetric)
+    others = {}
+    if not args.headline_only:
+        for name in W.WORKLOAD_ORDER:
+            q = W.make_workload(name)
+            qp = DeviceProblem(L, q, torch)
+            f, b = algorithmic(q)
+            # enough launches for about 0.3 s of work, at least args.steps
+            _, probe = time_steps(torch, qp, 3, 2)
+            n = int(max(args.steps, min(2000, 0.3e3 / max(1e-3, statistics.mean(probe)))))
+            reg, pl = time_steps(torch, qp, n, args.warmup, barrier)
+            km = statistics.mean(pl)
+            others[name] = dict(tflops=f * n / (reg * 1e-3) / 1e12, kernel_ms=km,
+                                kernel_tflops=f / (km * 1e-3) / 1e12,
+                                frac_fp8_peak=f / (km * 1e-3) / 1e12 / fp8_peak,
+                                hbm_gbs=b / (km * 1e-3) / 1e9, frac_hbm=b / (km * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                flops=f, algorithmic_bytes=b, launches=n, rotating_copies=qp.R)
+            del qp
+            torch.cuda.empty_cache()
+        if L.dg_get_device_status() != 0:
+            raise RuntimeError("device status reported an error during the benchmark")
+    clocks = sampler.stop()
+
+    e2e = e2e_headline(torch, L, p, max(3, min(args.steps, 20)), 2)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = cpu_baseline(HEADLINE, args.cpu_budget)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3xe4m3->f32->bf16",
+        "data": "synthetic (seeded PCG64; E4M3 + UE8M0 quantised N(0,1); C ~ N(0,1) bf16)",
+        "config": {"workload": HEADLINE, "M": p.M, "N": p.N, "K": p.K, "with_c": True,
+                   "l2": f"inputs larger than L2: {prob.R} rotating device copies, footprint "
+                         f"{prob.R * (alg_bytes) / 2**20:.0f} MiB > L2",
+                   "parallelism": f"replicas x{world}"},
+        "frac_fp8_peak": value / world / fp8_peak,
+        "fp8_peak_tflops": fp8_peak,
+        "fp8_peak_source": f"{peaks['source']} bf16 burst {peaks['bf16']} TFLOPS x {FP8_OVER_BF16} (nominal FP8/BF16 ratio)",
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "fp8_gemm_kernel (dense, with C)", "kernel_ms": kern_ms,
+                     "algorithmic_bytes_per_launch": alg_bytes, "peak_source": f"{peaks['source']} copy bandwidth"},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "workloads": others,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank):
+    """The CPU oracle timed on the headline workload, each step a bounded sample."""
+    if rank != 0:
+        return
+    import oracle as O
+    cores = os.cpu_count() or 1
+    p = W.make_workload(HEADLINE)
+    rows_per_step = 8
+    flops_step = 2.0 * rows_per_step * p.N * p.K
+    for i in range(args.warmup):
+        O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K, rows=np.arange(rows_per_step))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        rows = (np.arange(rows_per_step) + i * rows_per_step) % p.M
+        O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K, rows=rows)
+    el = time.perf_counter() - t0
+    value = flops_step * args.steps / el / 1e12
+    sample = f"{rows_per_step} output rows x all N={p.N} columns of {HEADLINE} per step, FP64 numpy/OpenBLAS"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded PCG64)", "config": {"workload": HEADLINE, "M": p.M, "N": p.N, "K": p.K},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+"""Python binding of libdg, the GB300 (sm_103a) fine-grained-scaled FP8 GEMM library.
+
+Argument marshalling only: every function below passes device pointers, sizes and the
+current CUDA stream to the C ABI declared in include/dg.h; all arithmetic runs in the
+library's CUDA kernels. There is no fallback: if libdg.so is missing or the call
+fails, an exception is raised.
+
+The GEMM computes D = C + A @ B.T (DeepGEMM README, "Interfaces / Notices", as
+reproduced on the page "Weight gradient kernels for dense and MoE models #95"), with
+A and B in E4M3, UE8M0 scales packed four per int32 (A: per row per 128-K group,
+B: per 128x128 block), FP32 accumulation and a BF16 result.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdg.so")
+
+DG_OK = 0
+STATUS_NAMES = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_MISALIGNED",
+                4: "DG_ERR_CUDA", 5: "DG_ERR_TIMEOUT", 6: "DG_ERR_BAD_INDEX"}
+
+# (name, restype, argtypes) of every entry point in include/dg.h
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = [
+    ("dg_fp8_gemm_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("dg_m_grouped_fp8_gemm_nt_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    ("dg_m_grouped_fp8_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    ("dg_pack_sf_ue8m0", _I, [_P, _P, _I, _I, _P]),
+    ("dg_get_mk_alignment_for_contiguous_layout", _I, []),
+    ("dg_get_tma_aligned_size", _I, [_I, _I]),
+    ("dg_set_num_sms", _I, [_I]),
+    ("dg_get_num_sms", _I, []),
+    ("dg_get_device_status", _I, [_P]),
+    ("dg_status_string", ctypes.c_char_p, [_I]),
+    ("dg_last_cuda_error", _I, []),
+]
+
+
+class DGError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libdg.so (built by fp8_gemm_nt_gb300.build) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m fp8_gemm_nt_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(name: str, status: int) -> None:
+    if status != DG_OK:
+        raise DGError(name, status)
+
+
+def _need(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _fp8(t: torch.Tensor, name: str) -> None:
+    _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _need(t.dtype in (torch.float8_e4m3fn, torch.uint8), f"{name} must be float8_e4m3fn (or its uint8 bytes)")
+
+
+def _i32(t: torch.Tensor, name: str) -> None:
+    _need(t.is_cuda and t.is_contiguous() and t.dtype == torch.int32, f"{name} must be a contiguous CUDA int32 tensor")
+
+
+def _bf16(t: torch.Tensor, name: str) -> None:
+    _need(t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16, f"{name} must be a contiguous CUDA bf16 tensor")
+
+
+def sf_shape(mn: int, k: int, groups: Optional[int] = None):
+    """Shape of a packed scale tensor for an MN extent and K: [(G,) ceil(K/512), ceil4(mn)]."""
+    shape = (-(-(k // 128) // 4), 4 * (-(-mn // 4)))
+    return shape if groups is None else (groups,) + shape
+
+
+def dg_fp8_gemm_nt(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:
+    """D = C + A @ B.T. a [M, K] e4m3, sfa [KP, ceil4(M)] int32, b [N, K] e4m3,
+    sfb [KP, ceil4(ceil(N/128))] int32, c [M, N] bf16 or None, d [M, N] bf16 (written)."""
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d")
+    M, K = a.shape
+    N = b.shape[0]
+    _need(b.shape[1] == K and tuple(d.shape) == (M, N), "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(M, K) and tuple(sfb.shape) == sf_shape(-(-N // 128), K), "scale shape mismatch")
+    if c is not None:
+        _bf16(c, "c")
+        _need(tuple(c.shape) == (M, N), "c shape mismatch")
+    _check("dg_fp8_gemm_nt", lib.dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                                M, N, K, _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, m_indices, stream=None) -> torch.Tensor:
+    """Contiguous M-grouped GEMM. a [M_total, K], sfa [KP, ceil4(M_total)], b [G, N, K],
+    sfb [G, KP, ceil4(ceil(N/128))], d [M_total, N] bf16, m_indices [M_total] int32 (-1 = pad)."""
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d"); _i32(m_indices, "m_indices")
+    M, K = a.shape
+    G, N, Kb = b.shape
+    _need(Kb == K and tuple(d.shape) == (M, N) and tuple(m_indices.shape) == (M,), "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(M, K) and tuple(sfb.shape) == sf_shape(-(-N // 128), K, G),
+          "scale shape mismatch")
+    _check("dg_m_grouped_fp8_gemm_nt_contiguous",
+           lib.dg_m_grouped_fp8_gemm_nt_contiguous(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d),
+                                                   _ptr(m_indices), M, N, K, G, _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, d, masked_m, stream=None) -> torch.Tensor:
+    """Masked M-grouped GEMM. a [G, max_m, K], sfa [G, KP, ceil4(max_m)], b [G, N, K],
+    sfb [G, KP, ceil4(ceil(N/128))], d [G, max_m, N] bf16, masked_m [G] int32 on the device."""
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d"); _i32(masked_m, "masked_m")
+    G, max_m, K = a.shape
+    Gb, N, Kb = b.shape
+    _need(Gb == G and Kb == K and tuple(d.shape) == (G, max_m, N) and tuple(masked_m.shape) == (G,),
+          "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(max_m, K, G) and tuple(sfb.shape) == sf_shape(-(-N // 128), K, G),
+          "scale shape mismatch")
+    _check("dg_m_grouped_fp8_gemm_nt_masked",
+           lib.dg_m_grouped_fp8_gemm_nt_masked(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m),
+                                               G, max_m, N, K, _stream(stream)))
+    return d
+
+
+def dg_pack_sf_ue8m0(sf: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """FP32 scales [mn, kgroups] -> packed UE8M0 int32 [ceil(kgroups/4), ceil4(mn)] (MN-major)."""
+    lib = load_library()
+    _need(sf.is_cuda and sf.is_contiguous() and sf.dtype == torch.float32 and sf.dim() == 2,
+          "sf must be a contiguous 2-D CUDA float32 tensor")
+    mn, kg = sf.shape
+    shape = (-(-kg // 4), 4 * (-(-mn // 4)))
+    if out is None:
+        out = torch.empty(shape, dtype=torch.int32, device=sf.device)
+    _i32(out, "out")
+    _need(tuple(out.shape) == shape, "out shape mismatch")
+    _check("dg_pack_sf_ue8m0", lib.dg_pack_sf_ue8m0(_ptr(sf), _ptr(out), mn, kg, _stream(stream)))
+    return out
+
+
+def dg_get_mk_alignment_for_contiguous_layout() -> int:
+    return load_library().dg_get_mk_alignment_for_contiguous_layout()
+
+
+def dg_get_tma_aligned_size(mn: int, elem_bytes: int) -> int:
+    return load_library().dg_get_tma_aligned_size(mn, elem_bytes)
+
+
+def dg_set_num_sms(n: int) -> None:
+    _check("dg_set_num_sms", load_library().dg_set_num_sms(n))
+
+
+def dg_get_num_sms() -> int:
+    return load_library().dg_get_num_sms()
+
+
+def dg_get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device-side error status code."""
+    return load_library().dg_get_device_status(_stream(stream))
+
+
+def dg_status_string(status: int) -> str:
+    return load_library().dg_status_string(status).decode()
+
+
+def dg_last_cuda_error() -> int:
+    """The last CUDA error code the library saw on this host thread (0 if none)."""
+    return load_library().dg_last_cuda_error()

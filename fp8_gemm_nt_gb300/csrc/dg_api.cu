@@ -1,0 +1,413 @@
+// Host side of libdg: argument validation, TMA descriptor construction, kernel
+// selection and launch, the scale-packing kernel and the device status word.
+// The C ABI is declared (and documented) in include/dg.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "dg.h"
+#include "fp8_gemm.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+std::atomic<int> g_num_sms_cap{0};
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  uint32_t* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mutex;
+
+dg_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return DG_ERR_CUDA;
+}
+
+// Per-device set-up (once): capability check, SM count, the status word.
+dg_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return DG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+    s.supported = (major == 10 && minor == 3);
+    if (s.supported) {
+      if ((e = cudaMalloc(&s.status, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e);
+      if ((e = cudaMemset(s.status, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e);
+    }
+    s.ready = true;
+  }
+  if (!s.supported) return DG_ERR_UNSUPPORTED;
+  *out = &s;
+  return DG_OK;
+}
+
+int sms_to_use(const DeviceState& s) {
+  const int cap = g_num_sms_cap.load();
+  return (cap > 0 && cap < s.num_sms) ? cap : s.num_sms;
+}
+
+// ------------------------------------------------------------------------------------
+// TMA descriptors
+// ------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// dims/box innermost first; strides in bytes for dims 1..rank-1.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  CUresult r = fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, b, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline int ceil4(int x) { return 4 * ceil_div(x, 4); }
+
+// ------------------------------------------------------------------------------------
+// Kernel configurations
+// ------------------------------------------------------------------------------------
+template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC>
+struct Launcher {
+  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs>;
+  static constexpr int kBN = BN;
+
+  static dg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                          const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
+                          cudaStream_t stream) {
+    auto kern = dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC>;
+    static thread_local int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+      if (e != cudaSuccess) return cuda_fail(e);
+      attr_dev = dev;
+    }
+    kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, td, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (std::getenv("DG_PRINT_CONFIGS"))
+      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d BN=%d stages=%d accum=%d epi_warps=%d grid=%d smem=%d\n",
+                   static_cast<int>(kKind), p.M, p.N, p.K, p.G, BN, kStages, kNumAccum, kEpiWarps, grid,
+                   Cfg::SMEM_BYTES);
+    return DG_OK;
+  }
+};
+
+// First configuration: 128 x 128 tiles, double-buffered accumulators, 4 epilogue warps.
+using DenseCfg = Launcher<dg::Kind::Dense, 128, 5, 2, 4, 2, false>;
+using DenseCfgC = Launcher<dg::Kind::Dense, 128, 5, 2, 4, 2, true>;
+using ContigCfg = Launcher<dg::Kind::Contiguous, 128, 5, 2, 4, 2, false>;
+using MaskedCfg = Launcher<dg::Kind::Masked, 128, 5, 2, 4, 2, false>;
+
+// A / B operand maps: E4M3 with 128-byte K boxes and 128-byte swizzle.
+bool map_operand_2d(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(K)};
+  const uint32_t box[2] = {128, static_cast<uint32_t>(box_rows)};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool map_operand_3d(CUtensorMap* m, const void* base, int G, int rows, int K, int box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows), static_cast<uint64_t>(G)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(K) * rows};
+  const uint32_t box[3] = {128, static_cast<uint32_t>(box_rows), 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Packed scale words [(G,) KP, ceil4(mn)] int32, loaded box_x words at a time.
+bool map_sf(CUtensorMap* m, const int32_t* base, int G, int mn, int KP, int box_x) {
+  const uint64_t w = static_cast<uint64_t>(ceil4(mn));
+  if (G <= 0) {
+    const uint64_t dims[2] = {w, static_cast<uint64_t>(KP)};
+    const uint64_t strides[1] = {w * 4};
+    const uint32_t box[2] = {static_cast<uint32_t>(box_x), 1};
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  const uint64_t dims[3] = {w, static_cast<uint64_t>(KP), static_cast<uint64_t>(G)};
+  const uint64_t strides[2] = {w * 4, w * 4 * KP};
+  const uint32_t box[3] = {static_cast<uint32_t>(box_x), 1, 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Output D (BF16), stored 32 rows x 64 columns per TMA store with 128-byte swizzle.
+bool map_out(CUtensorMap* m, void* base, int G, int rows, int N) {
+  if (G <= 0) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t box[2] = {64, 32};
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(rows), static_cast<uint64_t>(G)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(N) * 2 * rows};
+  const uint32_t box[3] = {64, 32, 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+dg_status check_common(int N, int K) {
+  if (K <= 0 || K % 128 != 0) return DG_ERR_INVALID_ARG;
+  if (N <= 0 || N % 16 != 0) return DG_ERR_INVALID_ARG;
+  if (static_cast<long long>(K) / 128 > (1 << 24)) return DG_ERR_INVALID_ARG;
+  return DG_OK;
+}
+
+// ------------------------------------------------------------------------------------
+// scale packing kernel
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ue8m0_ceil(float f, uint32_t* status) {
+  const uint32_t bits = __float_as_uint(f);
+  if (!(f > 0.0f) || !isfinite(f)) {
+    atomicOr(status, dg::kStatusBadIndexBit);
+    return 127u;
+  }
+  const uint32_t e = (bits >> 23) & 0xFFu;
+  const uint32_t mant = bits & 0x7FFFFFu;
+  uint32_t code;
+  if (e == 0) {
+    code = mant <= 0x400000u ? 0u : 1u;   // subnormal: (0, 2^-127] -> 2^-127, else 2^-126
+  } else {
+    code = e + (mant != 0 ? 1u : 0u);
+  }
+  return code > 254u ? 254u : code;
+}
+
+__global__ void pack_sf_kernel(const float* __restrict__ sf, int32_t* __restrict__ out, int mn, int kgroups,
+                               int mn_pad, int kp, uint32_t* status) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(mn_pad) * kp) return;
+  const int q = static_cast<int>(idx / mn_pad);
+  const int i = static_cast<int>(idx % mn_pad);
+  uint32_t w = 0;
+  if (i < mn) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int g = 4 * q + j;
+      if (g < kgroups) w |= ue8m0_ceil(sf[static_cast<long long>(i) * kgroups + g], status) << (8 * j);
+    }
+  }
+  out[idx] = static_cast<int32_t>(w);
+}
+
+}  // namespace
+
+// ======================================================================================
+// C ABI
+// ======================================================================================
+extern "C" {
+
+dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                         void* d, int M, int N, int K, cudaStream_t stream) {
+  if (M < 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (M == 0) return DG_OK;   // nothing to read or write: the pointers may be null
+  if (!a || !sfa || !b || !sfb || !d) return DG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d) || (c && !aligned16(c)))
+    return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+
+  const int KP = ceil_div(K / 128, 4);
+  CUtensorMap ta, tb, tsa, tsb, td;
+  constexpr int BN = DenseCfg::kBN;
+  if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||
+      !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
+      !map_out(&td, d, 0, M, N))
+    return DG_ERR_CUDA;
+  dg::Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.G = 1;
+  p.c = static_cast<const __nv_bfloat16*>(c);
+  p.d = static_cast<__nv_bfloat16*>(d);
+  p.status = ds->status;
+  p.timeout_ns = kWaitTimeoutNs;
+  const long long tiles = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, BN);
+  const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
+  if (c) return DenseCfgC::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+  return DenseCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+}
+
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              void* d, const int32_t* m_indices, int M_total, int N, int K, int G,
+                                              cudaStream_t stream) {
+  if (M_total < 0 || G <= 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (M_total == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d || !m_indices) return DG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d) ||
+      (reinterpret_cast<uintptr_t>(m_indices) & 3u))
+    return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+
+  const int KP = ceil_div(K / 128, 4);
+  CUtensorMap ta, tb, tsa, tsb, td;
+  constexpr int BN = ContigCfg::kBN;
+  if (!map_operand_2d(&ta, a, M_total, K, 128) || !map_operand_3d(&tb, b, G, N, K, BN) ||
+      !map_sf(&tsa, sfa, 0, M_total, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
+      !map_out(&td, d, 0, M_total, N))
+    return DG_ERR_CUDA;
+  dg::Params p{};
+  p.M = M_total;
+  p.N = N;
+  p.K = K;
+  p.G = G;
+  p.m_indices = m_indices;
+  p.d = static_cast<__nv_bfloat16*>(d);
+  p.status = ds->status;
+  p.timeout_ns = kWaitTimeoutNs;
+  const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
+  const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
+  return ContigCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+}
+
+dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                          void* d, const int32_t* masked_m, int G, int max_m, int N, int K,
+                                          cudaStream_t stream) {
+  if (G <= 0 || max_m < 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (max_m == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d || !masked_m) return DG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d) ||
+      (reinterpret_cast<uintptr_t>(masked_m) & 3u))
+    return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+
+  const int KP = ceil_div(K / 128, 4);
+  CUtensorMap ta, tb, tsa, tsb, td;
+  constexpr int BN = MaskedCfg::kBN;
+  if (!map_operand_3d(&ta, a, G, max_m, K, 128) || !map_operand_3d(&tb, b, G, N, K, BN) ||
+      !map_sf(&tsa, sfa, G, max_m, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
+      !map_out(&td, d, G, max_m, N))
+    return DG_ERR_CUDA;
+  dg::Params p{};
+  p.M = max_m;
+  p.N = N;
+  p.K = K;
+  p.G = G;
+  p.masked_m = masked_m;
+  p.d = static_cast<__nv_bfloat16*>(d);
+  p.status = ds->status;
+  p.timeout_ns = kWaitTimeoutNs;
+  const long long tiles = static_cast<long long>(G) * ceil_div(max_m, 128) * ceil_div(N, BN);
+  const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
+  return MaskedCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+}
+
+dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgroups, cudaStream_t stream) {
+  if (!sf_fp32 || !out || mn < 0 || kgroups <= 0) return DG_ERR_INVALID_ARG;
+  if (!aligned16(out) || (reinterpret_cast<uintptr_t>(sf_fp32) & 3u)) return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  const int mn_pad = ceil4(mn);
+  const int kp = ceil_div(kgroups, 4);
+  const long long n = static_cast<long long>(mn_pad) * kp;
+  if (n == 0) return DG_OK;
+  const int threads = 256;
+  const long long blocks = (n + threads - 1) / threads;
+  if (blocks > 0x7FFFFFFFll) return DG_ERR_INVALID_ARG;
+  pack_sf_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(sf_fp32, out, mn, kgroups, mn_pad, kp,
+                                                                        ds->status);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DG_OK : cuda_fail(e);
+}
+
+int dg_get_mk_alignment_for_contiguous_layout(void) { return dg::BLOCK_M; }
+
+int dg_get_tma_aligned_size(int mn, int elem_bytes) {
+  if (mn < 0 || (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)) return -1;
+  const int per16 = 16 / elem_bytes;
+  return ceil_div(mn, per16) * per16;
+}
+
+dg_status dg_set_num_sms(int n) {
+  if (n <= 0) {
+    g_num_sms_cap.store(0);
+    return DG_OK;
+  }
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  if (n > ds->num_sms) return DG_ERR_INVALID_ARG;
+  g_num_sms_cap.store(n);
+  return DG_OK;
+}
+
+int dg_get_num_sms(void) {
+  DeviceState* ds = nullptr;
+  if (device_state(&ds) != DG_OK) return g_num_sms_cap.load();
+  return sms_to_use(*ds);
+}
+
+dg_status dg_get_device_status(cudaStream_t stream) {
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  uint32_t v = 0;
+  if ((e = cudaMemcpy(&v, ds->status, sizeof(v), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+  if (v == 0) return DG_OK;
+  if ((e = cudaMemset(ds->status, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e);
+  if (v & dg::kStatusTimeoutBit) return DG_ERR_TIMEOUT;
+  return DG_ERR_BAD_INDEX;
+}
+
+const char* dg_status_string(dg_status s) {
+  switch (s) {
+    case DG_OK: return "DG_OK";
+    case DG_ERR_INVALID_ARG: return "DG_ERR_INVALID_ARG";
+    case DG_ERR_UNSUPPORTED: return "DG_ERR_UNSUPPORTED";
+    case DG_ERR_MISALIGNED: return "DG_ERR_MISALIGNED";
+    case DG_ERR_CUDA: return "DG_ERR_CUDA";
+    case DG_ERR_TIMEOUT: return "DG_ERR_TIMEOUT";
+    case DG_ERR_BAD_INDEX: return "DG_ERR_BAD_INDEX";
+  }
+  return "DG_ERR_UNKNOWN";
+}
+
+int dg_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

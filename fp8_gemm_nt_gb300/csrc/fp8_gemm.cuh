@@ -1,0 +1,514 @@
+// Persistent, warp-specialised fine-grained-scaled FP8 GEMM for sm_103a.
+//
+//   D = C + A @ B.T, A: E4M3 [rows, K] (one UE8M0 scale per row per 128-K group),
+//   B: E4M3 [N, K] (one UE8M0 scale per 128x128 block), FP32 accumulation in TMEM,
+//   BF16 output. Operation and scale format: DeepGEMM README ("Interfaces / Notices",
+//   "Normal dense GEMMs", "Grouped GEMMs (contiguous layout)", "Grouped GEMMs (masked
+//   layout)") as reproduced on the page "Weight gradient kernels for dense and MoE
+//   models #95".
+//
+// One CTA per SM loops over output tiles of 128 x BN. Roles:
+//   warp 0       TMA producer: A tile (128 x 128 B), B tile (BN x 128 B) and, once per
+//                four K-groups, the packed scale words, into a kStages-deep ring.
+//   warp 1       MMA warp: rearranges the scale words into the tcgen05.cp source layout,
+//                copies them into TMEM, and one elected thread issues
+//                tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 per instruction, four per
+//                K-group, all four reading the group's scale byte via the scale-factor id).
+//   warps 2..    epilogue: TMEM -> registers (+C) -> BF16 -> swizzled smem -> TMA store,
+//                or predicated row stores for tiles that hold padding / masked rows.
+// The accumulator is double-buffered in TMEM (kNumAccum = 2) so the epilogue of one tile
+// overlaps the main loop of the next.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace dg {
+
+enum class Kind : int { Dense = 0, Contiguous = 1, Masked = 2 };
+
+// Device status bits: bit (1 << s) for dg_status s.
+enum : uint32_t { kStatusTimeoutBit = 1u << 5, kStatusBadIndexBit = 1u << 6 };
+
+constexpr int BLOCK_M = 128;
+constexpr int BLOCK_K = 128;   // one scale group per pipeline stage
+constexpr int SF_BLOCK_N = 128;
+
+struct Params {
+  int M;   // dense: M; contiguous: M_total; masked: max_m (rows per group)
+  int N;
+  int K;
+  int G;
+  const int32_t* m_indices;       // contiguous: expert of each row, -1 = padding
+  const int32_t* masked_m;        // masked: valid rows per group (device)
+  const __nv_bfloat16* c;         // dense: optional addend [M, N]
+  __nv_bfloat16* d;               // output (used by the predicated store path)
+  uint32_t* status;               // device status word
+  unsigned long long timeout_ns;  // bound on every pipeline wait
+};
+
+__host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) / b; }
+
+template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs>
+struct Config {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
+  static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue uses 4 or 8 warps");
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kColsPerEpiWarp = BN / (kEpiWarps / 4);
+  static_assert(kColsPerEpiWarp % 64 == 0, "each epilogue warp stores whole 64-column chunks");
+
+  // shared memory (offsets from a 1024-byte-aligned base)
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K;
+  static constexpr int B_BYTES = BN * BLOCK_K;
+  static constexpr int SFB_CHUNKS = ceil_div_c(BN, 128);        // 128-row chunks of B scale rows
+  static constexpr int SF_RAW_A = 0;                            // 128 words as loaded (row-major)
+  static constexpr int SF_RAW_B = 512;                          // 8 block words as loaded
+  static constexpr int SF_UT_A = 1024;                          // 32 rows x 16 B tcgen05.cp source
+  static constexpr int SF_UT_B = 1536;                          // SFB_CHUNKS x (32 rows x 16 B)
+  static constexpr int SF_BYTES = SF_UT_B + SFB_CHUNKS * 512;
+  static constexpr int SF_TX_BYTES = BLOCK_M * 4 + 8 * 4;       // SFA box {128,1} + SFB box {8,1}
+  static constexpr int EPI_BUF_BYTES = 32 * 128;                // 32 rows x 64 BF16 columns
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + kStages * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + kStages * B_BYTES;
+  static constexpr int OFF_EPI = ((OFF_SF + kStages * SF_BYTES + 1023) / 1024) * 1024;
+  static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * kEpiBufs * EPI_BUF_BYTES;
+  static constexpr int NUM_BARS = 2 * kStages + 2 * kNumAccum + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;       // + slack for manual alignment
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
+
+  // tensor memory columns
+  static constexpr int ACC_COLS = kNumAccum * BN;
+  static constexpr int SFA_COL = ACC_COLS;                      // 2 buffers x 4 columns
+  static constexpr int SFB_COL = SFA_COL + 8;                   // 2 buffers x 4*SFB_CHUNKS columns
+  static constexpr int TMEM_USED = SFB_COL + 2 * 4 * SFB_CHUNKS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
+                                 : TMEM_USED <= 256 ? 256 : 512;
+  static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
+};
+
+// ------------------------------------------------------------------------------------
+// Tile scheduler: every role walks the same sequence t = blockIdx.x, += gridDim.x.
+// ------------------------------------------------------------------------------------
+struct Tile {
+  int g;        // expert (grouped forms), 0 for dense
+  int m_blk;    // 128-row block (within the group for the masked form)
+  int n_blk;
+  int valid_m;  // masked: rows of the group that are valid (clamped count)
+};
+
+template <Kind kKind, int BN>
+struct Scheduler {
+  int num_n, num_m, total;
+  int g_cur, g_start, g_tiles;
+
+  __device__ __forceinline__ int clamped_mask(const Params& p, int g) const {
+    int m = __ldg(p.masked_m + g);
+    return m < 0 ? 0 : (m > p.M ? p.M : m);
+  }
+
+  __device__ __forceinline__ explicit Scheduler(const Params& p) {
+    num_n = ceil_div_c(p.N, BN);
+    num_m = ceil_div_c(p.M, BLOCK_M);
+    g_cur = 0;
+    g_start = 0;
+    g_tiles = 0;
+    if constexpr (kKind == Kind::Masked) {
+      total = 0;
+      for (int g = 0; g < p.G; ++g) total += ceil_div_c(clamped_mask(p, g), BLOCK_M) * num_n;
+      if (blockIdx.x == 0 && threadIdx.x == 0) {
+        for (int g = 0; g < p.G; ++g) {
+          const int m = __ldg(p.masked_m + g);
+          if (m < 0 || m > p.M) atomicOr(p.status, kStatusBadIndexBit);
+        }
+      }
+      g_tiles = p.G > 0 ? ceil_div_c(clamped_mask(p, 0), BLOCK_M) * num_n : 0;
+    } else {
+      total = num_m * num_n;
+    }
+  }
+
+  // Returns false for a tile that has nothing to compute (contiguous padding block).
+  __device__ __forceinline__ bool get(const Params& p, int t, Tile& ti) {
+    if constexpr (kKind == Kind::Masked) {
+      while (t >= g_start + g_tiles && g_cur + 1 < p.G) {
+        g_start += g_tiles;
+        ++g_cur;
+        g_tiles = ceil_div_c(clamped_mask(p, g_cur), BLOCK_M) * num_n;
+      }
+      const int local = t - g_start;
+      ti.g = g_cur;
+      ti.m_blk = local / num_n;
+      ti.n_blk = local % num_n;
+      ti.valid_m = clamped_mask(p, g_cur);
+      return true;
+    } else {
+      ti.m_blk = t / num_n;
+      ti.n_blk = t % num_n;
+      ti.valid_m = p.M;
+      ti.g = 0;
+      if constexpr (kKind == Kind::Contiguous) {
+        const int g = __ldg(p.m_indices + ti.m_blk * BLOCK_M);
+        if (g < 0 || g >= p.G) return false;
+        ti.g = g;
+      }
+      return true;
+    }
+  }
+};
+
+// Warp-uniform bounded wait: every lane polls, and the warp proceeds only if all lanes
+// saw the phase complete and no other role has aborted.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                          volatile uint32_t* abort_flag) {
+  const bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC>
+__global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs>::kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
+                    const __grid_constant__ CUtensorMap tm_d, const Params p) {
+  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + kStages;
+  uint64_t* tfull_bar = bars + 2 * kStages;
+  uint64_t* tempty_bar = bars + 2 * kStages + kNumAccum;
+  uint64_t* drain_bar = bars + 2 * kStages + 2 * kNumAccum;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x / 32;
+  const uint32_t lane = threadIdx.x % 32;
+  const int num_kb = p.K / BLOCK_K;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < kNumAccum; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_sfa);
+    tma_prefetch_desc(&tm_sfb);
+    tma_prefetch_desc(&tm_d);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto on_timeout = [&]() {
+    atomicOr(p.status, kStatusTimeoutBit);
+    *abort_flag = 1;
+  };
+
+  Scheduler<kKind, BN> sched(p);
+
+  if (warp == 0) {
+    // ================================ TMA producer ================================
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, issued = 0;
+      for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
+        Tile ti;
+        if (!sched.get(p, t, ti)) continue;
+        const int row0 = ti.m_blk * BLOCK_M;
+        const int n0 = ti.n_blk * BN;
+        const int sfb_x = (n0 / SF_BLOCK_N) & ~3;   // 16-byte aligned start of the block-scale window
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (*abort_flag || !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns)) {
+            on_timeout();
+            goto producer_done;
+          }
+          const bool with_sf = (kb % 4) == 0;
+          uint64_t* fb = &full_bar[stage];
+          mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + (with_sf ? C::SF_TX_BYTES : 0));
+          uint8_t* sa = smem + C::OFF_A + stage * C::A_BYTES;
+          uint8_t* sb = smem + C::OFF_B + stage * C::B_BYTES;
+          uint8_t* ssf = smem + C::OFF_SF + stage * C::SF_BYTES;
+          if constexpr (kKind == Kind::Masked) {
+            tma_load_3d(sa, &tm_a, fb, kb * BLOCK_K, row0, ti.g);
+          } else {
+            tma_load_2d(sa, &tm_a, fb, kb * BLOCK_K, row0);
+          }
+          if constexpr (kKind == Kind::Dense) {
+            tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, n0);
+          } else {
+            tma_load_3d(sb, &tm_b, fb, kb * BLOCK_K, n0, ti.g);
+          }
+          if (with_sf) {
+            if constexpr (kKind == Kind::Masked) {
+              tma_load_3d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, kb / 4, ti.g);
+            } else {
+              tma_load_2d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, kb / 4);
+            }
+            if constexpr (kKind == Kind::Dense) {
+              tma_load_2d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, kb / 4);
+            } else {
+              tma_load_3d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, kb / 4, ti.g);
+            }
+          }
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    producer_done:
+      // No TMA write may still be landing in this CTA's shared memory at exit: wait for
+      // the last use of every stage (already consumed on the normal path).
+      for (uint32_t s = 0; s < kStages && s < issued; ++s) {
+        const uint32_t last_use = (issued - 1 - s) / kStages;
+        mbar_wait(&full_bar[s], last_use & 1, 50000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================ MMA issuer ==================================
+    constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(BLOCK_M, BN);
+    uint32_t stage = 0, phase = 0, tile_iter = 0, sf_iter = 0;
+    for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
+      Tile ti;
+      if (!sched.get(p, t, ti)) continue;
+      const uint32_t acc = tile_iter % kNumAccum;
+      const uint32_t acc_phase = (tile_iter / kNumAccum) & 1;
+      if (!warp_wait(&tempty_bar[acc], acc_phase ^ 1, p.timeout_ns, abort_flag)) {
+        if (lane == 0) on_timeout();
+        goto mma_done;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      const int n0 = ti.n_blk * BN;
+      const int sfb_x = (n0 / SF_BLOCK_N) & ~3;
+      uint32_t sfa_tmem = 0, sfb_tmem = 0;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!warp_wait(&full_bar[stage], phase, p.timeout_ns, abort_flag)) {
+          if (lane == 0) on_timeout();
+          goto mma_done;
+        }
+        tc_fence_after();
+        const uint32_t sf_base = smem_addr(smem + C::OFF_SF + stage * C::SF_BYTES);
+        if (kb % 4 == 0) {
+          // Scale words -> tcgen05.cp source layout: row r (= TMEM lane r of every
+          // sub-partition) holds, in word c, the scale word of tile row 32c + r.
+          const uint32_t a0 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * lane);
+          const uint32_t a1 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 32));
+          const uint32_t a2 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 64));
+          const uint32_t a3 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 96));
+          st_shared_v4(sf_base + C::SF_UT_A + 16 * lane, a0, a1, a2, a3);
+#pragma unroll
+          for (int ch = 0; ch < C::SFB_CHUNKS; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int n = n0 + 128 * ch + static_cast<int>(lane) + 32 * j;
+              w[j] = ld_shared_u32(sf_base + C::SF_RAW_B + 4 * (n / SF_BLOCK_N - sfb_x));
+            }
+            st_shared_v4(sf_base + C::SF_UT_B + 512 * ch + 16 * lane, w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          const uint32_t buf = sf_iter & 1;
+          ++sf_iter;
+          sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
+          sfb_tmem = tmem_base + C::SFB_COL + 4 * C::SFB_CHUNKS * buf;
+          if (lane == 0) {
+            tmem_copy_32x128b_warpx4(sfa_tmem, make_smem_desc(sf_base + C::SF_UT_A, 0, 128, kLayoutNone));
+#pragma unroll
+            for (int ch = 0; ch < C::SFB_CHUNKS; ++ch)
+              tmem_copy_32x128b_warpx4(sfb_tmem + 4 * ch,
+                                       make_smem_desc(sf_base + C::SF_UT_B + 512 * ch, 0, 128, kLayoutNone));
+          }
+        }
+        if (lane == 0) {
+          const uint32_t a_base = smem_addr(smem + C::OFF_A + stage * C::A_BYTES);
+          const uint32_t b_base = smem_addr(smem + C::OFF_B + stage * C::B_BYTES);
+          const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
+#pragma unroll
+          for (int k = 0; k < BLOCK_K / 32; ++k) {
+            const uint64_t adesc = make_smem_desc(a_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
+            const uint64_t bdesc = make_smem_desc(b_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
+            mma_mxf8_block_scale(d_tmem, adesc, bdesc, idesc, sfa_tmem, sfb_tmem, (kb | k) != 0);
+          }
+          tc_commit(&empty_bar[stage]);
+        }
+        __syncwarp();
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (lane == 0) tc_commit(&tfull_bar[acc]);
+      __syncwarp();
+      ++tile_iter;
+    }
+  mma_done:
+    // Every MMA / copy issued above must have finished before TMEM is released.
+    if (lane == 0) {
+      tc_commit(drain_bar);
+      mbar_wait(drain_bar, 0, 50000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ================================ epilogue ====================================
+    const int ew = warp - 2;
+    const int quad = warp % 4;                      // TMEM sub-partition this warp may access
+    const int col_part = ew / 4;
+    uint8_t* stage_base = smem + C::OFF_EPI + ew * kEpiBufs * C::EPI_BUF_BYTES;
+    uint32_t tile_iter = 0, buf_iter = 0;
+    for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
+      Tile ti;
+      if (!sched.get(p, t, ti)) {
+        if constexpr (kKind == Kind::Contiguous) {
+          const int g = __ldg(p.m_indices + (t / sched.num_n) * BLOCK_M);
+          if (lane == 0 && quad == 0 && col_part == 0 && (g < -1 || g >= p.G) && (t % sched.num_n) == 0)
+            atomicOr(p.status, kStatusBadIndexBit);
+        }
+        continue;
+      }
+      const uint32_t acc = tile_iter % kNumAccum;
+      const uint32_t acc_phase = (tile_iter / kNumAccum) & 1;
+      if (!warp_wait(&tfull_bar[acc], acc_phase, p.timeout_ns, abort_flag)) {
+        if (lane == 0) on_timeout();
+        break;
+      }
+      tc_fence_after();
+
+      const int row_in_tile = quad * 32 + static_cast<int>(lane);
+      const int row = ti.m_blk * BLOCK_M + row_in_tile;   // row index within A / D (or within group)
+      bool row_ok;
+      long long d_row;                                     // linear row of D
+      if constexpr (kKind == Kind::Dense) {
+        row_ok = row < p.M;
+        d_row = row;
+      } else if constexpr (kKind == Kind::Contiguous) {
+        const int gi = row < p.M ? __ldg(p.m_indices + row) : -1;
+        row_ok = gi == ti.g;
+        if (gi != ti.g && gi != -1 && ti.n_blk == 0 && col_part == 0) atomicOr(p.status, kStatusBadIndexBit);
+        d_row = row;
+      } else {
+        row_ok = row < ti.valid_m;
+        d_row = static_cast<long long>(ti.g) * p.M + row;
+      }
+      const uint32_t ok_mask = __ballot_sync(0xffffffffu, row_ok);
+      const int n0 = ti.n_blk * BN;
+
+      constexpr int kChunks = C::kColsPerEpiWarp / 64;
+#pragma unroll 1
+      for (int ch = 0; ch < kChunks; ++ch) {
+        const int col = col_part * C::kColsPerEpiWarp + ch * 64;   // column within the tile
+        uint32_t v0[32], v1[32];
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + col;
+        tmem_load_32x32b_x32(taddr, v0);
+        tmem_load_32x32b_x32(taddr + 32, v1);
+        tmem_load_wait();
+        if (ch == kChunks - 1) {
+          // this warp has read its whole share of the accumulator: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+        }
+        float f[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          f[i] = __uint_as_float(v0[i]);
+          f[32 + i] = __uint_as_float(v1[i]);
+        }
+        if constexpr (kHasC) {
+          if (row_ok) {
+            const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (n0 + col + 8 * q < p.N) {
+                const uint4 cv = ld_global_nc_v4(crow + 8 * q);
+                const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162*>(&cw[e]);
+                  const float2 cf = __bfloat1622float2(c2);
+                  f[8 * q + 2 * e] = cf.x + f[8 * q + 2 * e];
+                  f[8 * q + 2 * e + 1] = cf.y + f[8 * q + 2 * e + 1];
+                }
+              }
+            }
+          }
+        }
+        // stage the 32 x 64 BF16 chunk (128-byte rows, 16-byte units XOR-swizzled by row % 8)
+        uint8_t* sbuf = stage_base + (buf_iter % kEpiBufs) * C::EPI_BUF_BYTES;
+        ++buf_iter;
+        if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
+        __syncwarp();
+        const uint32_t srow = smem_addr(sbuf) + lane * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * u + 2 * e], f[8 * u + 2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          st_shared_v4(srow + ((u ^ (lane & 7)) * 16), w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (kKind == Kind::Dense || ok_mask == 0xffffffffu) {
+          if (lane == 0) {
+            if constexpr (kKind == Kind::Masked) {
+              tma_store_3d(&tm_d, sbuf, n0 + col, ti.m_blk * BLOCK_M + quad * 32, ti.g);
+            } else {
+              tma_store_2d(&tm_d, sbuf, n0 + col, ti.m_blk * BLOCK_M + quad * 32);
+            }
+            bulk_commit_group();
+          }
+        } else if (ok_mask != 0) {
+          // Rows of this warp are partly padding / masked: copy only the valid rows, one
+          // 128-byte row per warp instruction (lane = two columns).
+          const int gcol = n0 + col + 2 * static_cast<int>(lane);
+#pragma unroll 1
+          for (int r = 0; r < 32; ++r) {
+            const long long drow = __shfl_sync(0xffffffffu, d_row, r);
+            if (((ok_mask >> r) & 1u) && gcol < p.N) {
+              const uint32_t unit = (lane / 4) ^ (r & 7);
+              const uint32_t val = ld_shared_u32(smem_addr(sbuf) + r * 128 + unit * 16 + (lane % 4) * 4);
+              *reinterpret_cast<uint32_t*>(p.d + drow * p.N + gcol) = val;
+            }
+          }
+        }
+      }
+      ++tile_iter;
+    }
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace dg

@@ -1,0 +1,155 @@
+/*
+ * dg.h -- C ABI of the GB300 (sm_103a) fine-grained-scaled FP8 GEMM library (libdg.so).
+ *
+ * Operation (DeepGEMM README, as reproduced on the page "Weight gradient kernels for
+ * dense and MoE models #95", section "Interfaces / Notices"): the library follows the
+ * naming convention D = C + A @ B with the NT layout, so fp8_gemm_nt computes
+ *
+ *     D[m, n] = C[m, n] + sum_g sA[m, g] * sB[n / 128, g] * sum_{k = 128 g}^{128 g + 127} A[m, k] * B[n, k]
+ *
+ * with A and B in FP8 E4M3 (OCP "E4M3FN"), FP32 accumulation and a BF16 result.
+ * Scale granularity: A has one scale per row per 128-wide K-group ("1x128"), B one
+ * scale per 128x128 block. Scales are UE8M0 (code e means 2^(e-127)), packed four per
+ * int32 ("SM100 requires scaling factors in packed UE8M0 format, which packs 4 UE8M0
+ * into a single torch.int", same section): K-group 4q+j is byte j (least significant
+ * first) of word q. The LHS scales are "TMA-aligned and transposed": MN-major, with
+ * the MN extent padded to a multiple of 4 words (16 bytes).
+ *
+ * Notation used below: KG = K / 128, KP = ceil(KG / 4), NB = ceil(N / 128),
+ * ceil4(x) = 4 * ceil(x / 4).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument of the GEMM calls is caller-owned DEVICE memory on the
+ *     current device; the library never frees or retains it. Row-major means the
+ *     last index is contiguous. All base pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream). The returned
+ *     status covers host-side validation and the launch only; errors detected on the
+ *     device (bad expert index, masked count above max_m, a pipeline wait that timed
+ *     out) are recorded in a library-owned device status word and reported by
+ *     dg_get_device_status().
+ *   - On a non-OK synchronous status nothing is launched and no memory is written.
+ *   - Shape limits: K > 0 and K % 128 == 0; N > 0 and N % 16 == 0; M >= 0. An empty
+ *     problem (M, M_total or max_m == 0) launches nothing, and its pointers may be NULL.
+ *     Rows past M are never read or written.
+ *   - Not thread-safe against concurrent dg_set_num_sms(); GEMM calls themselves may
+ *     be issued from several host threads.
+ */
+#ifndef DG_H_
+#define DG_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, K % 128 != 0, N % 16 != 0, G <= 0 */
+  DG_ERR_UNSUPPORTED = 2,   /* device is not sm_103 / not supported by this build */
+  DG_ERR_MISALIGNED = 3,    /* a base pointer is not 16-byte aligned */
+  DG_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (see dg_last_cuda_error) */
+  DG_ERR_TIMEOUT = 5,       /* device: a pipeline wait exceeded its time limit; the kernel exited */
+  DG_ERR_BAD_INDEX = 6      /* device: m_indices[r] >= G or < -1, or masked_m[g] outside [0, max_m] */
+} dg_status;
+
+/*
+ * Dense GEMM: D = C + A @ B.T ("Normal dense GEMMs (non-grouped)": fp8_gemm_nt).
+ *   a   : E4M3 [M, K] row-major (K-major).
+ *   sfa : int32 [KP, ceil4(M)]; word (q, m) packs the UE8M0 scales of row m for
+ *         K-groups 4q..4q+3.
+ *   b   : E4M3 [N, K] row-major (K-major), i.e. B.T is column-major.
+ *   sfb : int32 [KP, ceil4(NB)]; word (q, j) packs the scales of the 128x128 block
+ *         (rows 128j..128j+127 of b) for K-groups 4q..4q+3.
+ *   c   : BF16 [M, N] row-major addend, or NULL for C = 0. May alias d exactly.
+ *   d   : BF16 [M, N] row-major output; fully overwritten for rows < M.
+ */
+dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa,
+                         const void* b, const int32_t* sfb,
+                         const void* c, void* d,
+                         int M, int N, int K, cudaStream_t stream);
+
+/*
+ * M-grouped GEMM, contiguous layout ("Grouped GEMMs (contiguous layout)":
+ * m_grouped_fp8_gemm_nt_contiguous). Only M is grouped; N and K are shared by the G
+ * experts. Each expert's token rows are concatenated along M, and each expert segment
+ * starts on a multiple of dg_get_mk_alignment_for_contiguous_layout() rows; padding
+ * rows are marked -1 in m_indices and form a suffix of their segment.
+ *   a         : E4M3 [M_total, K] row-major.
+ *   sfa       : int32 [KP, ceil4(M_total)] (as for dense A).
+ *   b         : E4M3 [G, N, K] row-major (expert g's weights at b + g*N*K).
+ *   sfb       : int32 [G, KP, ceil4(NB)] (expert g's block scales).
+ *   d         : BF16 [M_total, N] row-major. Rows with m_indices == -1 are NOT written.
+ *   m_indices : int32 [M_total] device array: expert of each row, -1 for padding.
+ *               The expert of a 128-row block is read from its first row; a block whose
+ *               first row is -1 is skipped entirely.
+ */
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
+                                              const void* b, const int32_t* sfb,
+                                              void* d, const int32_t* m_indices,
+                                              int M_total, int N, int K, int G,
+                                              cudaStream_t stream);
+
+/*
+ * M-grouped GEMM, masked layout ("Grouped GEMMs (masked layout)":
+ * m_grouped_fp8_gemm_nt_masked). For expert g only rows r < masked_m[g] are
+ * computed; the counts are read on the device, so the call can be captured in a CUDA
+ * graph while the host does not know them.
+ *   a        : E4M3 [G, max_m, K] row-major.
+ *   sfa      : int32 [G, KP, ceil4(max_m)].
+ *   b        : E4M3 [G, N, K] row-major.
+ *   sfb      : int32 [G, KP, ceil4(NB)].
+ *   d        : BF16 [G, max_m, N] row-major. Rows r >= masked_m[g] are NOT written.
+ *   masked_m : int32 [G] device array. A count above max_m is clamped to max_m and a
+ *              negative one is treated as 0; both set DG_ERR_BAD_INDEX on the device.
+ */
+dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa,
+                                          const void* b, const int32_t* sfb,
+                                          void* d, const int32_t* masked_m,
+                                          int G, int max_m, int N, int K,
+                                          cudaStream_t stream);
+
+/*
+ * Scale-factor packing ("Utilities": get_mn_major_tma_aligned_packed_ue8m0_tensor /
+ * transform_sf_into_required_layout). Converts FP32 scales into the packed, MN-major,
+ * TMA-aligned UE8M0 words the GEMMs consume.
+ *   sf_fp32 : FP32 [mn, kgroups] row-major device array (one scale per row/block and
+ *             K-group). Each value must be a positive finite number; it is rounded UP to
+ *             the next power of two (exact powers of two are kept), then clamped to the
+ *             UE8M0 range [2^-127, 2^127]. Non-positive or non-finite values encode 127
+ *             (scale 1.0) and set DG_ERR_BAD_INDEX on the device.
+ *   out     : int32 [ceil(kgroups/4), ceil4(mn)] device array, fully written (padding
+ *             bytes and padding rows are 0).
+ */
+dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgroups,
+                           cudaStream_t stream);
+
+/* Row alignment of each expert segment in the contiguous layout (the M block): 128. */
+int dg_get_mk_alignment_for_contiguous_layout(void);
+
+/* Smallest MN extent >= mn whose size in bytes is a multiple of 16 ("get_tma_aligned_size").
+ * elem_bytes must be 1, 2, 4 or 8; returns -1 on a bad argument. */
+int dg_get_tma_aligned_size(int mn, int elem_bytes);
+
+/* Cap on the number of SMs the persistent kernels use ("set_num_sms / get_num_sms").
+ * n <= 0 restores the default (all SMs of the device). Returns DG_ERR_INVALID_ARG if n
+ * exceeds the device's SM count. */
+dg_status dg_set_num_sms(int n);
+int dg_get_num_sms(void);
+
+/* Synchronises `stream`, then returns (and clears) the first error recorded on the
+ * current device by any earlier call: DG_ERR_TIMEOUT, DG_ERR_BAD_INDEX, or DG_OK. */
+dg_status dg_get_device_status(cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* dg_status_string(dg_status s);
+
+/* The last CUDA error code seen by the library on this host thread (0 if none). */
+int dg_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H_ */

@@ -1,0 +1,63 @@
+"""Helpers shared by the GPU tests: move seeded workloads to the device, run the
+library through its binding, and compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+import workloads as W
+
+SENTINEL = W.sentinel_bits()
+
+
+def dev(x: np.ndarray, dtype=None) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.cuda()
+
+
+def sentinel_like(shape) -> torch.Tensor:
+    return torch.full(shape, SENTINEL, dtype=torch.int16).view(torch.bfloat16).cuda()
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_dense(lib, p: W.Dense, c_alias: bool = False) -> torch.Tensor:
+    a, b = dev(p.a), dev(p.b)
+    sfa, sfb = dev(p.sfa), dev(p.sfb)
+    c = dev(p.c.view(np.int16), torch.bfloat16) if p.c is not None else None
+    if c_alias and c is not None:
+        d = c
+    else:
+        d = sentinel_like((p.M, p.N))
+    lib.dg_fp8_gemm_nt(a, sfa, b, sfb, c, d)
+    torch.cuda.synchronize()
+    return d
+
+
+def run_contiguous(lib, p: W.Contiguous) -> torch.Tensor:
+    d = sentinel_like((p.M_total, p.N))
+    lib.dg_m_grouped_fp8_gemm_nt_contiguous(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d, dev(p.m_indices))
+    torch.cuda.synchronize()
+    return d
+
+
+def run_masked(lib, p: W.Masked) -> torch.Tensor:
+    d = sentinel_like((p.G, p.max_m, p.N))
+    lib.dg_m_grouped_fp8_gemm_nt_masked(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d, dev(p.masked_m))
+    torch.cuda.synchronize()
+    return d
+
+
+def assert_parity(d_f64: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
+    rep = O.parity_report(d_f64, ref)
+    assert rep["ok"], f"parity failed {what}: {rep}"
+    return rep

@@ -1,0 +1,82 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads, exports
+every entry point declared in include/dg.h, and rejects bad arguments before it
+touches the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"\b(dg_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_gemm_nt_gb300 import build
+    build.build()
+    import fp8_gemm_nt_gb300 as L
+    return L.load_library()
+
+
+def test_header_declares_the_three_gemms():
+    names = declared_symbols()
+    for n in ("dg_fp8_gemm_nt", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_masked"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    import fp8_gemm_nt_gb300 as L
+    bound = {name for name, _, _ in L.SIGNATURES}
+    assert set(declared_symbols()) == bound
+    for name in declared_symbols():
+        assert callable(getattr(L, name)), name
+
+
+def test_host_helpers(lib):
+    assert lib.dg_get_mk_alignment_for_contiguous_layout() == 128
+    assert lib.dg_get_tma_aligned_size(5, 4) == 8
+    assert lib.dg_get_tma_aligned_size(16, 4) == 16
+    assert lib.dg_get_tma_aligned_size(17, 1) == 32
+    assert lib.dg_get_tma_aligned_size(3, 2) == 8
+    assert lib.dg_get_tma_aligned_size(3, 3) == -1
+    assert lib.dg_status_string(6) == b"DG_ERR_BAD_INDEX"
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    P = ctypes.c_void_p
+    x = P(0x10000)           # never dereferenced: validation fails first
+    INVALID, MISALIGNED = 1, 3
+    # null pointers
+    assert lib.dg_fp8_gemm_nt(None, x, x, x, None, x, 128, 128, 128, None) == INVALID
+    assert lib.dg_fp8_gemm_nt(x, x, x, x, None, None, 128, 128, 128, None) == INVALID
+    # K not a multiple of 128, N not a multiple of 16, negative M
+    assert lib.dg_fp8_gemm_nt(x, x, x, x, None, x, 128, 128, 100, None) == INVALID
+    assert lib.dg_fp8_gemm_nt(x, x, x, x, None, x, 128, 120, 128, None) == INVALID
+    assert lib.dg_fp8_gemm_nt(x, x, x, x, None, x, -1, 128, 128, None) == INVALID
+    assert lib.dg_fp8_gemm_nt(x, x, x, x, None, x, 128, 128, 0, None) == INVALID
+    # misaligned base pointer
+    assert lib.dg_fp8_gemm_nt(P(0x10008), x, x, x, None, x, 128, 128, 128, None) == MISALIGNED
+    # grouped forms: G <= 0
+    assert lib.dg_m_grouped_fp8_gemm_nt_contiguous(x, x, x, x, x, x, 128, 128, 128, 0, None) == INVALID
+    assert lib.dg_m_grouped_fp8_gemm_nt_masked(x, x, x, x, x, x, 0, 128, 128, 128, None) == INVALID
+    assert lib.dg_m_grouped_fp8_gemm_nt_masked(x, x, x, x, x, x, 4, -1, 128, 128, None) == INVALID
+    assert lib.dg_m_grouped_fp8_gemm_nt_contiguous(x, x, x, x, x, P(0x10002), 128, 128, 128, 2, None) == MISALIGNED
+    assert lib.dg_pack_sf_ue8m0(None, x, 4, 4, None) == INVALID

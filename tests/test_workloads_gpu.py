@@ -1,0 +1,78 @@
+"""Parity at the five workload sizes, in the launch configuration the benchmark times.
+
+The oracle computes sampled rows (all N columns) of each full-size problem; the
+integer decisions (padding rows of the contiguous layout, masked rows) are checked
+bit-exactly over the whole output.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from gpu_util import SENTINEL, assert_parity, bf16_bits, bf16_f64, run_contiguous, run_dense, run_masked
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp8_gemm_nt_gb300 as L
+    L.load_library()
+    return L
+
+
+def _rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    r = set(rng.choice(n, size=min(k, n), replace=False).tolist())
+    r.update({0, n - 1, min(127, n - 1), min(128, n - 1)})
+    return np.array(sorted(r))
+
+
+@pytest.mark.parametrize("name", [n for n in W.WORKLOAD_ORDER if W.WORKLOADS[n]["kind"] == "dense"])
+def test_dense_workload(lib, name):
+    p = W.make_workload(name)
+    d = run_dense(lib, p)
+    rows = np.arange(p.M) if p.M <= 128 else _rows(p.M, 96, 1)
+    ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K, rows=rows)
+    assert_parity(bf16_f64(d)[rows], ref, name)
+    assert lib.dg_get_device_status() == 0
+
+
+def test_contiguous_workload(lib):
+    name = "contiguous_g8_t32768_n4096_k7168"
+    p = W.make_workload(name)
+    d = run_contiguous(lib, p)
+    bits = bf16_bits(d)
+    pad = p.m_indices < 0
+    assert (bits[pad] == SENTINEL).all()
+    assert not (bits[~pad] == SENTINEL).all(axis=1).any()
+    # sampled rows, including each expert's first and last valid row
+    starts = [int(np.nonzero(p.m_indices == g)[0][0]) for g in range(p.G) if (p.m_indices == g).any()]
+    ends = [int(np.nonzero(p.m_indices == g)[0][-1]) for g in range(p.G) if (p.m_indices == g).any()]
+    rows = np.unique(np.concatenate([_rows(p.M_total, 96, 2), starts, ends]))
+    rows = rows[p.m_indices[rows] >= 0]
+    ref, valid = O.m_grouped_fp8_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K,
+                                                    p.G, rows=rows)
+    assert valid.all()
+    assert_parity(bf16_f64(d)[rows], ref, name)
+    assert lib.dg_get_device_status() == 0
+
+
+def test_masked_workload(lib):
+    name = "masked_g32_m256_n7168_k2048"
+    p = W.make_workload(name)
+    d = run_masked(lib, p)
+    bits = bf16_bits(d)
+    valid = np.arange(p.max_m)[None, :] < p.masked_m[:, None]
+    assert (bits[~valid] == SENTINEL).all()
+    groups = sorted(set([0, p.G - 1] + np.random.default_rng(3).choice(p.G, 6, replace=False).tolist()))
+    ref, v = O.m_grouped_fp8_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, p.masked_m, p.G, p.max_m, p.N, p.K,
+                                            groups=groups)
+    got = bf16_f64(d)[groups]
+    assert_parity(got[v], ref[v], name)
+    assert lib.dg_get_device_status() == 0
