@@ -40,6 +40,7 @@ SIGNATURES = [
     ("dg_get_device_status", _I, [_P]),
     ("dg_status_string", ctypes.c_char_p, [_I]),
     ("dg_last_cuda_error", _I, []),
+    ("dg_set_debug", _I, [_I, ctypes.c_ulonglong]),
 ]
 
 
@@ -199,3 +200,9 @@ def dg_status_string(status: int) -> str:
 def dg_last_cuda_error() -> int:
     """The last CUDA error code the library saw on this host thread (0 if none)."""
     return load_library().dg_last_cuda_error()
+
+
+def dg_set_debug(fault_mode: int, wait_timeout_ns: int = 0) -> None:
+    """Failure-detection test hook: fault_mode 1 makes later launches time out on purpose
+    (their producer issues nothing); wait_timeout_ns bounds every pipeline wait (0 = 2 s)."""
+    _check("dg_set_debug", load_library().dg_set_debug(fault_mode, wait_timeout_ns))

@@ -5,11 +5,13 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "dg.h"
 #include "fp8_gemm.cuh"
@@ -18,15 +20,26 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_num_sms_cap{0};
+std::atomic<int> g_fault{0};
+std::atomic<unsigned long long> g_timeout_ns{0};
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
+constexpr int kMinKGroupsPerCta = 4;                            // stream-K: smallest share per CTA
+
+// Stream-K workspace owned by the library: one per (device, stream), grown on demand.
+struct Workspace {
+  cudaStream_t stream = nullptr;
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
 
 struct DeviceState {
   bool ready = false;
   bool supported = false;
   int num_sms = 0;
   uint32_t* status = nullptr;
+  std::vector<Workspace> workspaces;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mutex;
@@ -66,6 +79,41 @@ int sms_to_use(const DeviceState& s) {
   return (cap > 0 && cap < s.num_sms) ? cap : s.num_sms;
 }
 
+unsigned long long wait_timeout_ns() {
+  const unsigned long long t = g_timeout_ns.load();
+  return t ? t : kWaitTimeoutNs;
+}
+
+// Workspace of at least `bytes` for `stream`, first `zero_bytes` zeroed when (re)allocated.
+// The stream-K counters are left at zero by every completed launch, so they are cleared
+// only when the buffer is created.
+dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, size_t zero_bytes, void** out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  Workspace* w = nullptr;
+  for (auto& x : ds.workspaces)
+    if (x.stream == stream) w = &x;
+  if (!w) {
+    ds.workspaces.push_back(Workspace{stream, nullptr, 0});
+    w = &ds.workspaces.back();
+  }
+  if (w->bytes < bytes) {
+    cudaError_t e;
+    if (w->ptr) {
+      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e);
+      if ((e = cudaFree(w->ptr)) != cudaSuccess) return cuda_fail(e);
+      w->ptr = nullptr;
+      w->bytes = 0;
+    }
+    const size_t alloc = bytes + bytes / 2;
+    if ((e = cudaMalloc(&w->ptr, alloc)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemsetAsync(w->ptr, 0, alloc, stream)) != cudaSuccess) return cuda_fail(e);
+    w->bytes = alloc;
+  }
+  (void)zero_bytes;
+  *out = w->ptr;
+  return DG_OK;
+}
+
 // ------------------------------------------------------------------------------------
 // TMA descriptors
 // ------------------------------------------------------------------------------------
@@ -82,9 +130,48 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// A small per-thread cache of encoded descriptors: repeated calls on the same buffers
+// (the common case: weights, activations and outputs reused every step) skip the encode.
+struct MapKey {
+  const void* base;
+  uint64_t dims[3];
+  uint64_t strides[2];
+  uint32_t box[3];
+  int dt, rank, swz;
+};
+
+struct MapCacheEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+
+constexpr int kMapCacheSize = 32;
+thread_local MapCacheEntry g_map_cache[kMapCacheSize];
+thread_local int g_map_cache_next = 0;
+
+bool same_key(const MapKey& a, const MapKey& b) { return std::memcmp(&a, &b, sizeof(MapKey)) == 0; }
+
 // dims/box innermost first; strides in bytes for dims 1..rank-1.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
               const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swz) {
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.base = base;
+  key.dt = static_cast<int>(dt);
+  key.rank = rank;
+  key.swz = static_cast<int>(swz);
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) key.strides[i] = strides[i];
+  for (int i = 0; i < kMapCacheSize; ++i) {
+    if (g_map_cache[i].used && same_key(g_map_cache[i].key, key)) {
+      *m = g_map_cache[i].map;
+      return true;
+    }
+  }
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
@@ -98,7 +185,13 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
   CUresult r = fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, b, elem_strides,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  MapCacheEntry& e = g_map_cache[g_map_cache_next];
+  g_map_cache_next = (g_map_cache_next + 1) % kMapCacheSize;
+  e.key = key;
+  e.map = *m;
+  e.used = true;
+  return true;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -108,8 +201,9 @@ inline int ceil4(int x) { return 4 * ceil_div(x, 4); }
 // ------------------------------------------------------------------------------------
 // Kernel configurations
 // ------------------------------------------------------------------------------------
-template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC>
+template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps_, int kEpiBufs, bool kHasC>
 struct Launcher {
+  static constexpr int kEpiWarps = kEpiWarps_;
   using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs>;
   static constexpr int kBN = BN;
 
@@ -129,9 +223,9 @@ struct Launcher {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
-      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d BN=%d stages=%d accum=%d epi_warps=%d grid=%d smem=%d\n",
+      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d BN=%d stages=%d accum=%d epi_warps=%d grid=%d smem=%d stream_k=%d\n",
                    static_cast<int>(kKind), p.M, p.N, p.K, p.G, BN, kStages, kNumAccum, kEpiWarps, grid,
-                   Cfg::SMEM_BYTES);
+                   Cfg::SMEM_BYTES, p.sk_ctas);
     return DG_OK;
   }
 };
@@ -263,9 +357,33 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   p.c = static_cast<const __nv_bfloat16*>(c);
   p.d = static_cast<__nv_bfloat16*>(d);
   p.status = ds->status;
-  p.timeout_ns = kWaitTimeoutNs;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, BN);
-  const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
+  const int sms = sms_to_use(*ds);
+  int grid = static_cast<int>(tiles < sms ? tiles : sms);
+  // Fewer tiles than SMs: share the K-groups of all tiles among all SMs (stream-K) so that
+  // every SM streams operands; each CTA gets at least kMinKGroupsPerCta K-groups.
+  const long long kgroups = tiles * (K / 128);
+  const long long sk = std::min<long long>(sms, kgroups / kMinKGroupsPerCta);
+  if (tiles < sms && sk > tiles) {
+    const int num_kb = K / 128;
+    int slots = 1;
+    for (long long t = 0; t < tiles; ++t) {
+      auto owner = [&](long long v) { return ((v + 1) * sk - 1) / kgroups; };
+      const int n = static_cast<int>(owner(t * num_kb + num_kb - 1) - owner(t * num_kb) + 1);
+      slots = std::max(slots, n);
+    }
+    const size_t ws_floats = static_cast<size_t>(tiles) * slots * 128 * BN;
+    const size_t counters = static_cast<size_t>(tiles) * DenseCfg::kEpiWarps;
+    void* ws = nullptr;
+    if (dg_status s = stream_workspace(*ds, stream, ws_floats * 4 + counters * 4, 0, &ws); s != DG_OK) return s;
+    p.sk_ctas = static_cast<int>(sk);
+    p.sk_slots = slots;
+    p.sk_ws = static_cast<float*>(ws);
+    p.sk_counters = reinterpret_cast<int*>(static_cast<float*>(ws) + ws_floats);
+    grid = static_cast<int>(sk);
+  }
   if (c) return DenseCfgC::launch(ta, tb, tsa, tsb, td, p, grid, stream);
   return DenseCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
 }
@@ -298,7 +416,8 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   p.m_indices = m_indices;
   p.d = static_cast<__nv_bfloat16*>(d);
   p.status = ds->status;
-  p.timeout_ns = kWaitTimeoutNs;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
   return ContigCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
@@ -332,7 +451,8 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   p.masked_m = masked_m;
   p.d = static_cast<__nv_bfloat16*>(d);
   p.status = ds->status;
-  p.timeout_ns = kWaitTimeoutNs;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(G) * ceil_div(max_m, 128) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
   return MaskedCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
@@ -391,7 +511,13 @@ dg_status dg_get_device_status(cudaStream_t stream) {
   if ((e = cudaMemcpy(&v, ds->status, sizeof(v), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
   if (v == 0) return DG_OK;
   if ((e = cudaMemset(ds->status, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e);
-  if (v & dg::kStatusTimeoutBit) return DG_ERR_TIMEOUT;
+  if (v & dg::kStatusTimeoutBit) {
+    // an aborted stream-K launch may leave its arrival counters non-zero: clear them
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (auto& w : ds->workspaces)
+      if (w.ptr && (e = cudaMemset(w.ptr, 0, w.bytes)) != cudaSuccess) return cuda_fail(e);
+    return DG_ERR_TIMEOUT;
+  }
   return DG_ERR_BAD_INDEX;
 }
 
@@ -409,5 +535,12 @@ const char* dg_status_string(dg_status s) {
 }
 
 int dg_last_cuda_error(void) { return g_last_cuda_error; }
+
+dg_status dg_set_debug(int fault_mode, unsigned long long wait_timeout_ns) {
+  if (fault_mode < 0 || fault_mode > dg::kFaultProducerSilent) return DG_ERR_INVALID_ARG;
+  g_fault.store(fault_mode);
+  g_timeout_ns.store(wait_timeout_ns);
+  return DG_OK;
+}
 
 }  // extern "C"

@@ -7,17 +7,27 @@
 //   layout)") as reproduced on the page "Weight gradient kernels for dense and MoE
 //   models #95".
 //
-// One CTA per SM loops over output tiles of 128 x BN. Roles:
-//   warp 0       TMA producer: A tile (128 x 128 B), B tile (BN x 128 B) and, once per
-//                four K-groups, the packed scale words, into a kStages-deep ring.
+// One CTA per SM walks a sequence of *segments*: a segment is one 128 x BN output tile
+// and a range of its K-groups. In tile mode every segment is a whole tile (K-groups
+// 0..KG-1), tiles dealt round-robin to the CTAs. In stream-K mode (dense form, used
+// when there are fewer tiles than SMs) the flattened (tile, K-group) space is cut into
+// one equal contiguous range per CTA; a tile covered by several CTAs is finished by
+// the last of them to arrive, which sums the FP32 partials of all contributors in a
+// fixed order (so the result does not depend on arrival order) from a workspace.
+//
+// Roles:
+//   warp 0       TMA producer: A tile (128 x 128 B), B tile (BN x 128 B) and, at the
+//                first K-group of a segment and every fourth K-group, the packed scale
+//                words, into a kStages-deep ring.
 //   warp 1       MMA warp: rearranges the scale words into the tcgen05.cp source layout,
 //                copies them into TMEM, and one elected thread issues
 //                tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 per instruction, four per
 //                K-group, all four reading the group's scale byte via the scale-factor id).
 //   warps 2..    epilogue: TMEM -> registers (+C) -> BF16 -> swizzled smem -> TMA store,
-//                or predicated row stores for tiles that hold padding / masked rows.
-// The accumulator is double-buffered in TMEM (kNumAccum = 2) so the epilogue of one tile
-// overlaps the main loop of the next.
+//                or predicated row stores for tiles that hold padding / masked rows, or
+//                (stream-K) FP32 partials to the workspace and the last-arriver reduction.
+// The accumulator is double-buffered in TMEM (kNumAccum = 2) so the epilogue of one
+// segment overlaps the main loop of the next.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -31,6 +41,9 @@ enum class Kind : int { Dense = 0, Contiguous = 1, Masked = 2 };
 
 // Device status bits: bit (1 << s) for dg_status s.
 enum : uint32_t { kStatusTimeoutBit = 1u << 5, kStatusBadIndexBit = 1u << 6 };
+
+// Fault injection for the failure-detection tests (host-side switch, default off).
+enum : int { kFaultNone = 0, kFaultProducerSilent = 1 };
 
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_K = 128;   // one scale group per pipeline stage
@@ -47,6 +60,12 @@ struct Params {
   __nv_bfloat16* d;               // output (used by the predicated store path)
   uint32_t* status;               // device status word
   unsigned long long timeout_ns;  // bound on every pipeline wait
+  // stream-K (dense only); sk_ctas == 0 selects tile mode
+  int sk_ctas;                    // number of CTAs sharing the K-group space (== gridDim.x)
+  int sk_slots;                   // partial slots per tile in the workspace
+  float* sk_ws;                   // [tiles][sk_slots][128 * BN] FP32 partials
+  int* sk_counters;               // [tiles][epilogue warps], zero between launches
+  int fault;                      // kFault*
 };
 
 __host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) / b; }
@@ -88,22 +107,35 @@ struct Config {
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                  : TMEM_USED <= 256 ? 256 : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
+
+  // stream-K partial layout: per epilogue warp a 32-row x kColsPerEpiWarp block of float4,
+  // float4 (c4, lane) at index c4 * 32 + lane (a warp's 32 lanes write 512 contiguous bytes)
+  static constexpr int SK_TILE_FLOATS = BLOCK_M * BN;
+  static constexpr int SK_WARP_FLOATS = 32 * kColsPerEpiWarp;
 };
 
 // ------------------------------------------------------------------------------------
-// Tile scheduler: every role walks the same sequence t = blockIdx.x, += gridDim.x.
+// Segment scheduler: every role of a CTA walks the same sequence of segments.
 // ------------------------------------------------------------------------------------
-struct Tile {
-  int g;        // expert (grouped forms), 0 for dense
-  int m_blk;    // 128-row block (within the group for the masked form)
+struct Segment {
+  int g;          // expert (grouped forms), 0 for dense
+  int m_blk;      // 128-row block (within the group for the masked form)
   int n_blk;
-  int valid_m;  // masked: rows of the group that are valid (clamped count)
+  int valid_m;    // masked: rows of the group that are valid (clamped count)
+  int tile;       // linear tile index (stream-K workspace / counters)
+  int kb_begin;   // K-groups [kb_begin, kb_end) of the tile
+  int kb_end;
+  int n_contrib;  // CTAs contributing to this tile (1 = this segment is the whole tile)
+  int slot;       // this CTA's position among them
 };
 
 template <Kind kKind, int BN>
 struct Scheduler {
-  int num_n, num_m, total;
-  int g_cur, g_start, g_tiles;
+  int num_n, num_m, total, num_kb;
+  int g_cur, g_start, g_tiles;   // masked: incremental walk over groups
+  int t;                         // tile mode: next tile index
+  long long u, u_end, U;         // stream-K: this CTA's K-group range, total K-groups
+  bool stream_k;
 
   __device__ __forceinline__ int clamped_mask(const Params& p, int g) const {
     int m = __ldg(p.masked_m + g);
@@ -113,50 +145,100 @@ struct Scheduler {
   __device__ __forceinline__ explicit Scheduler(const Params& p) {
     num_n = ceil_div_c(p.N, BN);
     num_m = ceil_div_c(p.M, BLOCK_M);
+    num_kb = p.K / BLOCK_K;
     g_cur = 0;
     g_start = 0;
     g_tiles = 0;
+    t = blockIdx.x;
+    stream_k = false;
+    u = u_end = U = 0;
     if constexpr (kKind == Kind::Masked) {
       total = 0;
       for (int g = 0; g < p.G; ++g) total += ceil_div_c(clamped_mask(p, g), BLOCK_M) * num_n;
+      g_tiles = p.G > 0 ? ceil_div_c(clamped_mask(p, 0), BLOCK_M) * num_n : 0;
       if (blockIdx.x == 0 && threadIdx.x == 0) {
         for (int g = 0; g < p.G; ++g) {
           const int m = __ldg(p.masked_m + g);
           if (m < 0 || m > p.M) atomicOr(p.status, kStatusBadIndexBit);
         }
       }
-      g_tiles = p.G > 0 ? ceil_div_c(clamped_mask(p, 0), BLOCK_M) * num_n : 0;
     } else {
       total = num_m * num_n;
+      if constexpr (kKind == Kind::Dense) {
+        if (p.sk_ctas > 0) {
+          stream_k = true;
+          U = static_cast<long long>(total) * num_kb;
+          u = static_cast<long long>(blockIdx.x) * U / p.sk_ctas;
+          u_end = static_cast<long long>(blockIdx.x + 1) * U / p.sk_ctas;
+        }
+      }
     }
   }
 
-  // Returns false for a tile that has nothing to compute (contiguous padding block).
-  __device__ __forceinline__ bool get(const Params& p, int t, Tile& ti) {
-    if constexpr (kKind == Kind::Masked) {
-      while (t >= g_start + g_tiles && g_cur + 1 < p.G) {
-        g_start += g_tiles;
-        ++g_cur;
-        g_tiles = ceil_div_c(clamped_mask(p, g_cur), BLOCK_M) * num_n;
-      }
-      const int local = t - g_start;
-      ti.g = g_cur;
-      ti.m_blk = local / num_n;
-      ti.n_blk = local % num_n;
-      ti.valid_m = clamped_mask(p, g_cur);
-      return true;
-    } else {
-      ti.m_blk = t / num_n;
-      ti.n_blk = t % num_n;
-      ti.valid_m = p.M;
-      ti.g = 0;
-      if constexpr (kKind == Kind::Contiguous) {
-        const int g = __ldg(p.m_indices + ti.m_blk * BLOCK_M);
-        if (g < 0 || g >= p.G) return false;
-        ti.g = g;
-      }
+  // CTA whose K-group range contains flattened K-group index v.
+  __device__ __forceinline__ int sk_owner(const Params& p, long long v) const {
+    return static_cast<int>(((v + 1) * p.sk_ctas - 1) / U);
+  }
+
+  // Next segment of this CTA; false when there is none left. Contiguous padding blocks
+  // are skipped here (every role skips the same ones).
+  __device__ __forceinline__ bool next(const Params& p, Segment& s) {
+    if (stream_k) {
+      if (u >= u_end) return false;
+      const int tile = static_cast<int>(u / num_kb);
+      s.tile = tile;
+      s.m_blk = tile / num_n;
+      s.n_blk = tile % num_n;
+      s.g = 0;
+      s.valid_m = p.M;
+      s.kb_begin = static_cast<int>(u - static_cast<long long>(tile) * num_kb);
+      const long long left = u_end - u;
+      s.kb_end = static_cast<int>(left < num_kb - s.kb_begin ? s.kb_begin + left : num_kb);
+      const int first = sk_owner(p, static_cast<long long>(tile) * num_kb);
+      const int last = sk_owner(p, static_cast<long long>(tile) * num_kb + num_kb - 1);
+      s.n_contrib = last - first + 1;
+      s.slot = static_cast<int>(blockIdx.x) - first;
+      u += s.kb_end - s.kb_begin;
       return true;
     }
+    while (t < total) {
+      const int cur = t;
+      t += gridDim.x;
+      s.tile = cur;
+      s.kb_begin = 0;
+      s.kb_end = num_kb;
+      s.n_contrib = 1;
+      s.slot = 0;
+      if constexpr (kKind == Kind::Masked) {
+        while (cur >= g_start + g_tiles && g_cur + 1 < p.G) {
+          g_start += g_tiles;
+          ++g_cur;
+          g_tiles = ceil_div_c(clamped_mask(p, g_cur), BLOCK_M) * num_n;
+        }
+        const int local = cur - g_start;
+        s.g = g_cur;
+        s.m_blk = local / num_n;
+        s.n_blk = local % num_n;
+        s.valid_m = clamped_mask(p, g_cur);
+        return true;
+      } else {
+        s.m_blk = cur / num_n;
+        s.n_blk = cur % num_n;
+        s.valid_m = p.M;
+        s.g = 0;
+        if constexpr (kKind == Kind::Contiguous) {
+          const int g = __ldg(p.m_indices + s.m_blk * BLOCK_M);
+          if (g < 0 || g >= p.G) {
+            // a block led by an out-of-range index is reported once (by its n = 0 tile)
+            if ((g < -1 || g >= p.G) && s.n_blk == 0 && threadIdx.x == 64) atomicOr(p.status, kStatusBadIndexBit);
+            continue;
+          }
+          s.g = g;
+        }
+        return true;
+      }
+    }
+    return false;
   }
 };
 
@@ -166,6 +248,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
                                           volatile uint32_t* abort_flag) {
   const bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, timeout_ns);
   return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void st_global_v4f(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_global_cg_v4f(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
 }
 
 template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC>
@@ -188,7 +283,6 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
 
   const int warp = threadIdx.x / 32;
   const uint32_t lane = threadIdx.x % 32;
-  const int num_kb = p.K / BLOCK_K;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -226,48 +320,47 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
   };
 
   Scheduler<kKind, BN> sched(p);
+  Segment seg;
 
   if (warp == 0) {
     // ================================ TMA producer ================================
-    if (lane == 0) {
+    if (lane == 0 && p.fault != kFaultProducerSilent) {
       uint32_t stage = 0, phase = 0, issued = 0;
-      for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
-        Tile ti;
-        if (!sched.get(p, t, ti)) continue;
-        const int row0 = ti.m_blk * BLOCK_M;
-        const int n0 = ti.n_blk * BN;
+      while (sched.next(p, seg)) {
+        const int row0 = seg.m_blk * BLOCK_M;
+        const int n0 = seg.n_blk * BN;
         const int sfb_x = (n0 / SF_BLOCK_N) & ~3;   // 16-byte aligned start of the block-scale window
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
           if (*abort_flag || !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns)) {
             on_timeout();
             goto producer_done;
           }
-          const bool with_sf = (kb % 4) == 0;
+          const bool with_sf = kb == seg.kb_begin || (kb % 4) == 0;
           uint64_t* fb = &full_bar[stage];
           mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + (with_sf ? C::SF_TX_BYTES : 0));
           uint8_t* sa = smem + C::OFF_A + stage * C::A_BYTES;
           uint8_t* sb = smem + C::OFF_B + stage * C::B_BYTES;
           uint8_t* ssf = smem + C::OFF_SF + stage * C::SF_BYTES;
           if constexpr (kKind == Kind::Masked) {
-            tma_load_3d(sa, &tm_a, fb, kb * BLOCK_K, row0, ti.g);
+            tma_load_3d(sa, &tm_a, fb, kb * BLOCK_K, row0, seg.g);
           } else {
             tma_load_2d(sa, &tm_a, fb, kb * BLOCK_K, row0);
           }
           if constexpr (kKind == Kind::Dense) {
             tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, n0);
           } else {
-            tma_load_3d(sb, &tm_b, fb, kb * BLOCK_K, n0, ti.g);
+            tma_load_3d(sb, &tm_b, fb, kb * BLOCK_K, n0, seg.g);
           }
           if (with_sf) {
             if constexpr (kKind == Kind::Masked) {
-              tma_load_3d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, kb / 4, ti.g);
+              tma_load_3d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, kb / 4, seg.g);
             } else {
               tma_load_2d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, kb / 4);
             }
             if constexpr (kKind == Kind::Dense) {
               tma_load_2d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, kb / 4);
             } else {
-              tma_load_3d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, kb / 4, ti.g);
+              tma_load_3d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, kb / 4, seg.g);
             }
           }
           ++issued;
@@ -288,81 +381,82 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
   } else if (warp == 1) {
     // ================================ MMA issuer ==================================
     constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(BLOCK_M, BN);
-    uint32_t stage = 0, phase = 0, tile_iter = 0, sf_iter = 0;
-    for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
-      Tile ti;
-      if (!sched.get(p, t, ti)) continue;
-      const uint32_t acc = tile_iter % kNumAccum;
-      const uint32_t acc_phase = (tile_iter / kNumAccum) & 1;
+    uint32_t stage = 0, phase = 0, seg_iter = 0, sf_iter = 0;
+    while (sched.next(p, seg)) {
+      const uint32_t acc = seg_iter % kNumAccum;
+      const uint32_t acc_phase = (seg_iter / kNumAccum) & 1;
       if (!warp_wait(&tempty_bar[acc], acc_phase ^ 1, p.timeout_ns, abort_flag)) {
         if (lane == 0) on_timeout();
         goto mma_done;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      const int n0 = ti.n_blk * BN;
-      const int sfb_x = (n0 / SF_BLOCK_N) & ~3;
-      uint32_t sfa_tmem = 0, sfb_tmem = 0;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        if (!warp_wait(&full_bar[stage], phase, p.timeout_ns, abort_flag)) {
-          if (lane == 0) on_timeout();
-          goto mma_done;
-        }
-        tc_fence_after();
-        const uint32_t sf_base = smem_addr(smem + C::OFF_SF + stage * C::SF_BYTES);
-        if (kb % 4 == 0) {
-          // Scale words -> tcgen05.cp source layout: row r (= TMEM lane r of every
-          // sub-partition) holds, in word c, the scale word of tile row 32c + r.
-          const uint32_t a0 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * lane);
-          const uint32_t a1 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 32));
-          const uint32_t a2 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 64));
-          const uint32_t a3 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 96));
-          st_shared_v4(sf_base + C::SF_UT_A + 16 * lane, a0, a1, a2, a3);
+      {
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        const int n0 = seg.n_blk * BN;
+        const int sfb_x = (n0 / SF_BLOCK_N) & ~3;
+        uint32_t sfa_tmem = 0, sfb_tmem = 0;
+        for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
+          if (!warp_wait(&full_bar[stage], phase, p.timeout_ns, abort_flag)) {
+            if (lane == 0) on_timeout();
+            goto mma_done;
+          }
+          tc_fence_after();
+          const uint32_t sf_base = smem_addr(smem + C::OFF_SF + stage * C::SF_BYTES);
+          if (kb == seg.kb_begin || kb % 4 == 0) {
+            // Scale words -> tcgen05.cp source layout: row r (= TMEM lane r of every
+            // sub-partition) holds, in word c, the scale word of tile row 32c + r.
+            const uint32_t a0 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * lane);
+            const uint32_t a1 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 32));
+            const uint32_t a2 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 64));
+            const uint32_t a3 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 96));
+            st_shared_v4(sf_base + C::SF_UT_A + 16 * lane, a0, a1, a2, a3);
 #pragma unroll
-          for (int ch = 0; ch < C::SFB_CHUNKS; ++ch) {
-            uint32_t w[4];
+            for (int ch = 0; ch < C::SFB_CHUNKS; ++ch) {
+              uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int n = n0 + 128 * ch + static_cast<int>(lane) + 32 * j;
-              w[j] = ld_shared_u32(sf_base + C::SF_RAW_B + 4 * (n / SF_BLOCK_N - sfb_x));
+              for (int j = 0; j < 4; ++j) {
+                const int n = n0 + 128 * ch + static_cast<int>(lane) + 32 * j;
+                w[j] = ld_shared_u32(sf_base + C::SF_RAW_B + 4 * (n / SF_BLOCK_N - sfb_x));
+              }
+              st_shared_v4(sf_base + C::SF_UT_B + 512 * ch + 16 * lane, w[0], w[1], w[2], w[3]);
             }
-            st_shared_v4(sf_base + C::SF_UT_B + 512 * ch + 16 * lane, w[0], w[1], w[2], w[3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            const uint32_t buf = sf_iter & 1;
+            ++sf_iter;
+            sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
+            sfb_tmem = tmem_base + C::SFB_COL + 4 * C::SFB_CHUNKS * buf;
+            if (lane == 0) {
+              tmem_copy_32x128b_warpx4(sfa_tmem, make_smem_desc(sf_base + C::SF_UT_A, 0, 128, kLayoutNone));
+#pragma unroll
+              for (int ch = 0; ch < C::SFB_CHUNKS; ++ch)
+                tmem_copy_32x128b_warpx4(sfb_tmem + 4 * ch,
+                                         make_smem_desc(sf_base + C::SF_UT_B + 512 * ch, 0, 128, kLayoutNone));
+            }
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          const uint32_t buf = sf_iter & 1;
-          ++sf_iter;
-          sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
-          sfb_tmem = tmem_base + C::SFB_COL + 4 * C::SFB_CHUNKS * buf;
           if (lane == 0) {
-            tmem_copy_32x128b_warpx4(sfa_tmem, make_smem_desc(sf_base + C::SF_UT_A, 0, 128, kLayoutNone));
+            const uint32_t a_base = smem_addr(smem + C::OFF_A + stage * C::A_BYTES);
+            const uint32_t b_base = smem_addr(smem + C::OFF_B + stage * C::B_BYTES);
+            const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
 #pragma unroll
-            for (int ch = 0; ch < C::SFB_CHUNKS; ++ch)
-              tmem_copy_32x128b_warpx4(sfb_tmem + 4 * ch,
-                                       make_smem_desc(sf_base + C::SF_UT_B + 512 * ch, 0, 128, kLayoutNone));
+            for (int k = 0; k < BLOCK_K / 32; ++k) {
+              const uint64_t adesc = make_smem_desc(a_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
+              const uint64_t bdesc = make_smem_desc(b_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
+              mma_mxf8_block_scale(d_tmem, adesc, bdesc, idesc, sfa_tmem, sfb_tmem,
+                                   (kb != seg.kb_begin || k != 0) ? 1u : 0u);
+            }
+            tc_commit(&empty_bar[stage]);
           }
-        }
-        if (lane == 0) {
-          const uint32_t a_base = smem_addr(smem + C::OFF_A + stage * C::A_BYTES);
-          const uint32_t b_base = smem_addr(smem + C::OFF_B + stage * C::B_BYTES);
-          const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
-#pragma unroll
-          for (int k = 0; k < BLOCK_K / 32; ++k) {
-            const uint64_t adesc = make_smem_desc(a_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
-            const uint64_t bdesc = make_smem_desc(b_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
-            mma_mxf8_block_scale(d_tmem, adesc, bdesc, idesc, sfa_tmem, sfb_tmem, (kb | k) != 0);
+          __syncwarp();
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
           }
-          tc_commit(&empty_bar[stage]);
-        }
-        __syncwarp();
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1;
         }
       }
       if (lane == 0) tc_commit(&tfull_bar[acc]);
       __syncwarp();
-      ++tile_iter;
+      ++seg_iter;
     }
   mma_done:
     // Every MMA / copy issued above must have finished before TMEM is released.
@@ -377,19 +471,13 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     const int quad = warp % 4;                      // TMEM sub-partition this warp may access
     const int col_part = ew / 4;
     uint8_t* stage_base = smem + C::OFF_EPI + ew * kEpiBufs * C::EPI_BUF_BYTES;
-    uint32_t tile_iter = 0, buf_iter = 0;
-    for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
-      Tile ti;
-      if (!sched.get(p, t, ti)) {
-        if constexpr (kKind == Kind::Contiguous) {
-          const int g = __ldg(p.m_indices + (t / sched.num_n) * BLOCK_M);
-          if (lane == 0 && quad == 0 && col_part == 0 && (g < -1 || g >= p.G) && (t % sched.num_n) == 0)
-            atomicOr(p.status, kStatusBadIndexBit);
-        }
-        continue;
-      }
-      const uint32_t acc = tile_iter % kNumAccum;
-      const uint32_t acc_phase = (tile_iter / kNumAccum) & 1;
+    uint32_t seg_iter = 0, buf_iter = 0;
+    constexpr int kChunks = C::kColsPerEpiWarp / 64;
+
+    while (sched.next(p, seg)) {
+      const uint32_t acc = seg_iter % kNumAccum;
+      const uint32_t acc_phase = (seg_iter / kNumAccum) & 1;
+      ++seg_iter;
       if (!warp_wait(&tfull_bar[acc], acc_phase, p.timeout_ns, abort_flag)) {
         if (lane == 0) on_timeout();
         break;
@@ -397,7 +485,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
       tc_fence_after();
 
       const int row_in_tile = quad * 32 + static_cast<int>(lane);
-      const int row = ti.m_blk * BLOCK_M + row_in_tile;   // row index within A / D (or within group)
+      const int row = seg.m_blk * BLOCK_M + row_in_tile;   // row index within A / D (or within group)
       bool row_ok;
       long long d_row;                                     // linear row of D
       if constexpr (kKind == Kind::Dense) {
@@ -405,37 +493,19 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
         d_row = row;
       } else if constexpr (kKind == Kind::Contiguous) {
         const int gi = row < p.M ? __ldg(p.m_indices + row) : -1;
-        row_ok = gi == ti.g;
-        if (gi != ti.g && gi != -1 && ti.n_blk == 0 && col_part == 0) atomicOr(p.status, kStatusBadIndexBit);
+        row_ok = gi == seg.g;
+        if (gi != seg.g && gi != -1 && seg.n_blk == 0 && col_part == 0) atomicOr(p.status, kStatusBadIndexBit);
         d_row = row;
       } else {
-        row_ok = row < ti.valid_m;
-        d_row = static_cast<long long>(ti.g) * p.M + row;
+        row_ok = row < seg.valid_m;
+        d_row = static_cast<long long>(seg.g) * p.M + row;
       }
       const uint32_t ok_mask = __ballot_sync(0xffffffffu, row_ok);
-      const int n0 = ti.n_blk * BN;
+      const int n0 = seg.n_blk * BN;
+      const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
 
-      constexpr int kChunks = C::kColsPerEpiWarp / 64;
-#pragma unroll 1
-      for (int ch = 0; ch < kChunks; ++ch) {
-        const int col = col_part * C::kColsPerEpiWarp + ch * 64;   // column within the tile
-        uint32_t v0[32], v1[32];
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + col;
-        tmem_load_32x32b_x32(taddr, v0);
-        tmem_load_32x32b_x32(taddr + 32, v1);
-        tmem_load_wait();
-        if (ch == kChunks - 1) {
-          // this warp has read its whole share of the accumulator: hand it back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty_bar[acc]);
-        }
-        float f[64];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          f[i] = __uint_as_float(v0[i]);
-          f[32 + i] = __uint_as_float(v1[i]);
-        }
+      // (+C) -> BF16 -> swizzled smem -> TMA store / predicated rows, for one 64-column chunk
+      auto store_chunk = [&](float (&f)[64], int col) {
         if constexpr (kHasC) {
           if (row_ok) {
             const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
@@ -455,7 +525,6 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
             }
           }
         }
-        // stage the 32 x 64 BF16 chunk (128-byte rows, 16-byte units XOR-swizzled by row % 8)
         uint8_t* sbuf = stage_base + (buf_iter % kEpiBufs) * C::EPI_BUF_BYTES;
         ++buf_iter;
         if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
@@ -476,9 +545,9 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
         if (kKind == Kind::Dense || ok_mask == 0xffffffffu) {
           if (lane == 0) {
             if constexpr (kKind == Kind::Masked) {
-              tma_store_3d(&tm_d, sbuf, n0 + col, ti.m_blk * BLOCK_M + quad * 32, ti.g);
+              tma_store_3d(&tm_d, sbuf, n0 + col, seg.m_blk * BLOCK_M + quad * 32, seg.g);
             } else {
-              tma_store_2d(&tm_d, sbuf, n0 + col, ti.m_blk * BLOCK_M + quad * 32);
+              tma_store_2d(&tm_d, sbuf, n0 + col, seg.m_blk * BLOCK_M + quad * 32);
             }
             bulk_commit_group();
           }
@@ -496,8 +565,92 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
             }
           }
         }
+      };
+
+      if (seg.n_contrib == 1) {
+#pragma unroll 1
+        for (int ch = 0; ch < kChunks; ++ch) {
+          const int col = col_part * C::kColsPerEpiWarp + ch * 64;   // column within the tile
+          uint32_t v0[32], v1[32];
+          const uint32_t taddr = tmem_base + t_lane + acc * BN + col;
+          tmem_load_32x32b_x32(taddr, v0);
+          tmem_load_32x32b_x32(taddr + 32, v1);
+          tmem_load_wait();
+          if (ch == kChunks - 1) {
+            // this warp has read its whole share of the accumulator: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+          }
+          float f[64];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            f[i] = __uint_as_float(v0[i]);
+            f[32 + i] = __uint_as_float(v1[i]);
+          }
+          store_chunk(f, col);
+        }
+      } else {
+        // stream-K: publish this CTA's FP32 partial of the warp's block, then let the last
+        // contributor to arrive sum all partials (in slot order) and store the tile.
+        float* my_ws = p.sk_ws + (static_cast<long long>(seg.tile) * p.sk_slots + seg.slot) * C::SK_TILE_FLOATS +
+                       ew * C::SK_WARP_FLOATS;
+#pragma unroll 1
+        for (int ch = 0; ch < kChunks; ++ch) {
+          const int col = col_part * C::kColsPerEpiWarp + ch * 64;
+          uint32_t v0[32], v1[32];
+          const uint32_t taddr = tmem_base + t_lane + acc * BN + col;
+          tmem_load_32x32b_x32(taddr, v0);
+          tmem_load_32x32b_x32(taddr + 32, v1);
+          tmem_load_wait();
+          if (ch == kChunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* src = q < 4 ? &v0[8 * q] : &v1[8 * (q - 4)];
+            const int c4 = ch * 16 + 2 * q;   // float4 column group within the warp's columns
+            st_global_v4f(my_ws + (c4 * 32 + lane) * 4, __uint_as_float(src[0]), __uint_as_float(src[1]),
+                          __uint_as_float(src[2]), __uint_as_float(src[3]));
+            st_global_v4f(my_ws + ((c4 + 1) * 32 + lane) * 4, __uint_as_float(src[4]), __uint_as_float(src[5]),
+                          __uint_as_float(src[6]), __uint_as_float(src[7]));
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        int arrived = 0;
+        int* counter = p.sk_counters + seg.tile * kEpiWarps + ew;
+        if (lane == 0) arrived = atomicAdd(counter, 1);
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        if (arrived == seg.n_contrib - 1) {
+          __threadfence();
+          const float* tile_ws = p.sk_ws + static_cast<long long>(seg.tile) * p.sk_slots * C::SK_TILE_FLOATS +
+                                 ew * C::SK_WARP_FLOATS;
+#pragma unroll 1
+          for (int ch = 0; ch < kChunks; ++ch) {
+            const int col = col_part * C::kColsPerEpiWarp + ch * 64;
+            float f[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+#pragma unroll 1
+            for (int s = 0; s < seg.n_contrib; ++s) {
+              const float* src = tile_ws + static_cast<long long>(s) * C::SK_TILE_FLOATS;
+#pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                const float4 v = ld_global_cg_v4f(src + ((ch * 16 + q) * 32 + lane) * 4);
+                f[4 * q + 0] += v.x;
+                f[4 * q + 1] += v.y;
+                f[4 * q + 2] += v.z;
+                f[4 * q + 3] += v.w;
+              }
+            }
+            store_chunk(f, col);
+          }
+          if (lane == 0) *counter = 0;   // ready for the next launch
+        }
       }
-      ++tile_iter;
     }
     if (lane == 0) bulk_wait_group_all();
     __syncwarp();

@@ -148,6 +148,17 @@ const char* dg_status_string(dg_status s);
 /* The last CUDA error code seen by the library on this host thread (0 if none). */
 int dg_last_cuda_error(void);
 
+/*
+ * Test hook for the failure-detection path (no counterpart on the pages).
+ *   fault_mode      : 0 = none (default); 1 = the TMA producer of every later GEMM launch
+ *                     issues no loads, so the MMA and epilogue waits run out and the
+ *                     kernel exits with DG_ERR_TIMEOUT recorded in the status word.
+ *   wait_timeout_ns : limit of every pipeline wait in later launches; 0 = default (2 s).
+ * Process-wide; affects launches made after the call. Returns DG_ERR_INVALID_ARG for an
+ * unknown fault_mode.
+ */
+dg_status dg_set_debug(int fault_mode, unsigned long long wait_timeout_ns);
+
 #ifdef __cplusplus
 }
 #endif
