@@ -26,6 +26,7 @@ std::atomic<unsigned long long> g_timeout_ns{0};
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
 constexpr int kMinKGroupsPerCta = 4;                            // stream-K: smallest share per CTA
+constexpr size_t kSkCounterInts = 4096;                         // stream-K arrival counters per workspace
 
 // Stream-K workspace owned by the library: one per (device, stream), grown on demand.
 struct Workspace {
@@ -84,10 +85,9 @@ unsigned long long wait_timeout_ns() {
   return t ? t : kWaitTimeoutNs;
 }
 
-// Workspace of at least `bytes` for `stream`, first `zero_bytes` zeroed when (re)allocated.
-// The stream-K counters are left at zero by every completed launch, so they are cleared
-// only when the buffer is created.
-dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, size_t zero_bytes, void** out) {
+// Workspace of at least `bytes` for `stream`, zeroed when (re)allocated. The stream-K
+// arrival counters at its start are left at zero by every completed launch.
+dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, void** out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   Workspace* w = nullptr;
   for (auto& x : ds.workspaces)
@@ -109,7 +109,6 @@ dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, s
     if ((e = cudaMemsetAsync(w->ptr, 0, alloc, stream)) != cudaSuccess) return cuda_fail(e);
     w->bytes = alloc;
   }
-  (void)zero_bytes;
   *out = w->ptr;
   return DG_OK;
 }
@@ -230,11 +229,34 @@ struct Launcher {
   }
 };
 
-// First configuration: 128 x 128 tiles, double-buffered accumulators, 4 epilogue warps.
-using DenseCfg = Launcher<dg::Kind::Dense, 128, 5, 2, 4, 2, false>;
-using DenseCfgC = Launcher<dg::Kind::Dense, 128, 5, 2, 4, 2, true>;
-using ContigCfg = Launcher<dg::Kind::Contiguous, 128, 5, 2, 4, 2, false>;
-using MaskedCfg = Launcher<dg::Kind::Masked, 128, 5, 2, 4, 2, false>;
+// Tile configurations (BN = tile width). All use 128-row tiles and 4 epilogue warps.
+//   128: 5-stage ring, double-buffered accumulators (TMEM 2 x 128 columns)
+//   192: 4-stage ring, double-buffered accumulators (TMEM 2 x 192 columns)
+//   256: 4-stage ring, single accumulator (TMEM 256 columns; 2 x 256 + scales exceeds 512)
+template <dg::Kind kKind, bool kHasC>
+dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                    const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
+                    cudaStream_t stream) {
+  switch (bn) {
+    case 128: return Launcher<kKind, 128, 5, 2, 4, 2, kHasC>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 192: return Launcher<kKind, 192, 4, 2, 4, 2, kHasC>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 256: return Launcher<kKind, 256, 4, 1, 4, 1, kHasC>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+  }
+  return DG_ERR_INVALID_ARG;
+}
+constexpr int kEpilogueWarps = 4;
+
+// Tile width for a problem: DG_FORCE_BN (128, 192 or 256) overrides the heuristic.
+int pick_bn(int tiles128, int N, int sms) {
+  if (const char* f = std::getenv("DG_FORCE_BN")) {
+    const int v = std::atoi(f);
+    if (v == 128 || v == 192 || v == 256) return v;
+  }
+  (void)tiles128;
+  (void)N;
+  (void)sms;
+  return 128;
+}
 
 // A / B operand maps: E4M3 with 128-byte K boxes and 128-byte swizzle.
 bool map_operand_2d(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
@@ -344,7 +366,10 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
 
   const int KP = ceil_div(K / 128, 4);
   CUtensorMap ta, tb, tsa, tsb, td;
-  constexpr int BN = DenseCfg::kBN;
+  const int sms = sms_to_use(*ds);
+  const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
+  // fewer tiles than SMs: 128-wide tiles shared over K (stream-K); otherwise the heuristic
+  const int BN = tiles128 < sms ? 128 : pick_bn(static_cast<int>(std::min<long long>(tiles128, 1 << 30)), N, sms);
   if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||
       !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, 0, M, N))
@@ -360,7 +385,6 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   p.timeout_ns = wait_timeout_ns();
   p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, BN);
-  const int sms = sms_to_use(*ds);
   int grid = static_cast<int>(tiles < sms ? tiles : sms);
   // Fewer tiles than SMs: share the K-groups of all tiles among all SMs (stream-K) so that
   // every SM streams operands; each CTA gets at least kMinKGroupsPerCta K-groups.
@@ -374,18 +398,20 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
       const int n = static_cast<int>(owner(t * num_kb + num_kb - 1) - owner(t * num_kb) + 1);
       slots = std::max(slots, n);
     }
+    // Layout: a fixed-size counter region first (its position must not depend on the
+    // problem shape: completed launches leave it all-zero for the next one), then partials.
     const size_t ws_floats = static_cast<size_t>(tiles) * slots * 128 * BN;
-    const size_t counters = static_cast<size_t>(tiles) * DenseCfg::kEpiWarps;
+    if (static_cast<size_t>(tiles) * kEpilogueWarps > kSkCounterInts) return DG_ERR_UNSUPPORTED;
     void* ws = nullptr;
-    if (dg_status s = stream_workspace(*ds, stream, ws_floats * 4 + counters * 4, 0, &ws); s != DG_OK) return s;
+    if (dg_status s = stream_workspace(*ds, stream, kSkCounterInts * 4 + ws_floats * 4, &ws); s != DG_OK) return s;
     p.sk_ctas = static_cast<int>(sk);
     p.sk_slots = slots;
-    p.sk_ws = static_cast<float*>(ws);
-    p.sk_counters = reinterpret_cast<int*>(static_cast<float*>(ws) + ws_floats);
+    p.sk_counters = static_cast<int*>(ws);
+    p.sk_ws = reinterpret_cast<float*>(static_cast<int*>(ws) + kSkCounterInts);
     grid = static_cast<int>(sk);
   }
-  if (c) return DenseCfgC::launch(ta, tb, tsa, tsb, td, p, grid, stream);
-  return DenseCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+  if (c) return launch_bn<dg::Kind::Dense, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+  return launch_bn<dg::Kind::Dense, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
@@ -403,7 +429,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
 
   const int KP = ceil_div(K / 128, 4);
   CUtensorMap ta, tb, tsa, tsb, td;
-  constexpr int BN = ContigCfg::kBN;
+  const int BN = pick_bn(ceil_div(M_total, 128) * ceil_div(N, 128), N, sms_to_use(*ds));
   if (!map_operand_2d(&ta, a, M_total, K, 128) || !map_operand_3d(&tb, b, G, N, K, BN) ||
       !map_sf(&tsa, sfa, 0, M_total, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, 0, M_total, N))
@@ -420,7 +446,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
-  return ContigCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+  return launch_bn<dg::Kind::Contiguous, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
@@ -438,7 +464,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
 
   const int KP = ceil_div(K / 128, 4);
   CUtensorMap ta, tb, tsa, tsb, td;
-  constexpr int BN = MaskedCfg::kBN;
+  const int BN = pick_bn(G * ceil_div(max_m, 128) * ceil_div(N, 128), N, sms_to_use(*ds));
   if (!map_operand_3d(&ta, a, G, max_m, K, 128) || !map_operand_3d(&tb, b, G, N, K, BN) ||
       !map_sf(&tsa, sfa, G, max_m, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, G, max_m, N))
@@ -455,7 +481,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(G) * ceil_div(max_m, 128) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
-  return MaskedCfg::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+  return launch_bn<dg::Kind::Masked, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
 }
 
 dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgroups, cudaStream_t stream) {
