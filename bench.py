@@ -318,7 +318,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--profile-case", default=None,
+                    help="run --launches untimed launches of one workload and exit (for profilers)")
+    ap.add_argument("--launches", type=int, default=2)
     args = ap.parse_args()
+    if args.profile_case:
+        return profile_case(args.profile_case, args.launches)
     args.warmup = max(3, args.warmup)
 
     rank = int(os.environ.get("RANK", "0"))
@@ -435,6 +440,22 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def profile_case(name, launches):
+    """Launch one workload `launches` times on cuda:0 with no timing, for ncu captures."""
+    import torch
+    import fp8_gemm_nt_gb300 as L
+    L.load_library()
+    prob = DeviceProblem(L, W.make_workload(name), torch, max_bytes=0)
+    torch.cuda.synchronize()
+    for i in range(launches):
+        prob.launch(i)
+    torch.cuda.synchronize()
+    status = L.dg_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    print(f"profile-case {name}: {launches} launches ok")
 
 
 def run_reference(args, rank):

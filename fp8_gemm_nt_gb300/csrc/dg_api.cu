@@ -247,15 +247,27 @@ dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const 
 constexpr int kEpilogueWarps = 4;
 
 // Tile width for a problem: DG_FORCE_BN (128, 192 or 256) overrides the heuristic.
-int pick_bn(int tiles128, int N, int sms) {
+// Measured on GB300 (tile mode): wider tiles cut the L2->SM bytes per FLOP, which is what
+// limits the 128-wide configuration, so the widest tile that wastes no more columns than
+// the narrower ones wins; the masked form (short K, HBM-bound) prefers 192 with its
+// double-buffered accumulators.
+int pick_bn(dg::Kind kind, int N) {
   if (const char* f = std::getenv("DG_FORCE_BN")) {
     const int v = std::atoi(f);
     if (v == 128 || v == 192 || v == 256) return v;
   }
-  (void)tiles128;
-  (void)N;
-  (void)sms;
-  return 128;
+  if (kind == dg::Kind::Masked) return N > 128 ? 192 : 128;
+  const int cands[3] = {256, 192, 128};
+  int best = 256;
+  long long best_cols = -1;
+  for (int bn : cands) {
+    const long long cols = static_cast<long long>(ceil_div(N, bn)) * bn;
+    if (best_cols < 0 || cols < best_cols) {
+      best = bn;
+      best_cols = cols;
+    }
+  }
+  return best;
 }
 
 // A / B operand maps: E4M3 with 128-byte K boxes and 128-byte swizzle.
@@ -369,7 +381,14 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   const int sms = sms_to_use(*ds);
   const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
   // fewer tiles than SMs: 128-wide tiles shared over K (stream-K); otherwise the heuristic
-  const int BN = tiles128 < sms ? 128 : pick_bn(static_cast<int>(std::min<long long>(tiles128, 1 << 30)), N, sms);
+  // Fewer 128 x 128 tiles than SMs: stream-K (see below) with DG_SK_BN-wide tiles (default
+  // 128); otherwise the tile-mode heuristic.
+  int sk_bn = 128;
+  if (const char* f = std::getenv("DG_SK_BN")) {
+    const int v = std::atoi(f);
+    if (v == 128 || v == 192 || v == 256) sk_bn = v;
+  }
+  const int BN = tiles128 < sms ? sk_bn : pick_bn(dg::Kind::Dense, N);
   if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||
       !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, 0, M, N))
@@ -429,7 +448,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
 
   const int KP = ceil_div(K / 128, 4);
   CUtensorMap ta, tb, tsa, tsb, td;
-  const int BN = pick_bn(ceil_div(M_total, 128) * ceil_div(N, 128), N, sms_to_use(*ds));
+  const int BN = pick_bn(dg::Kind::Contiguous, N);
   if (!map_operand_2d(&ta, a, M_total, K, 128) || !map_operand_3d(&tb, b, G, N, K, BN) ||
       !map_sf(&tsa, sfa, 0, M_total, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, 0, M_total, N))
@@ -464,7 +483,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
 
   const int KP = ceil_div(K / 128, 4);
   CUtensorMap ta, tb, tsa, tsb, td;
-  const int BN = pick_bn(G * ceil_div(max_m, 128) * ceil_div(N, 128), N, sms_to_use(*ds));
+  const int BN = pick_bn(dg::Kind::Masked, N);
   if (!map_operand_3d(&ta, a, G, max_m, K, 128) || !map_operand_3d(&tb, b, G, N, K, BN) ||
       !map_sf(&tsa, sfa, G, max_m, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, G, max_m, N))

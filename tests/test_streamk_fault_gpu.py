@@ -80,3 +80,14 @@ def test_timeout_is_reported_and_context_survives(lib, shape):
     ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, None, M, N, K)
     assert_parity(bf16_f64(d), ref, "after timeout")
     assert lib.dg_get_device_status() == 0
+
+
+@pytest.mark.parametrize("sk_bn", [128, 192, 256])
+@pytest.mark.parametrize("M,N,K", [(128, 2048, 8192), (96, 7168, 4096)])
+def test_stream_k_tile_widths(lib, sk_bn, M, N, K, monkeypatch):
+    monkeypatch.setenv("DG_SK_BN", str(sk_bn))
+    p = W.make_dense(M, N, K, seed=700 + sk_bn + M, with_c=True)
+    d = run_dense(lib, p)
+    ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, M, N, K)
+    assert_parity(bf16_f64(d), ref, f"stream-K bn={sk_bn}")
+    assert lib.dg_get_device_status() == 0
