@@ -15,6 +15,7 @@
 
 #include "dg.h"
 #include "fp8_gemm.cuh"
+#include "fp8_gemm_pair.cuh"
 
 namespace {
 
@@ -246,6 +247,75 @@ dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const 
 }
 constexpr int kEpilogueWarps = 4;
 
+// CTA-pair configuration: 256 x 256 tiles over two SMs, 5-stage ring per CTA.
+constexpr int kPairStages = 5;
+
+template <dg::Kind kKind, bool kHasC>
+struct PairLauncher {
+  using Cfg = dg::PairConfig<kPairStages>;
+  static constexpr auto kernel() { return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kHasC>; }
+
+  // Largest number of co-resident CTA pairs (0 if the device cannot run the kernel).
+  static int max_clusters() {
+    static thread_local int dev_cached = -1, value = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev == dev_cached) return value;
+    auto kern = kernel();
+    value = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) == cudaSuccess &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2, 1, 1);
+      cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess) value = n;
+    }
+    cudaGetLastError();
+    dev_cached = dev;
+    return value;
+  }
+
+  static dg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                          const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int clusters,
+                          cudaStream_t stream) {
+    auto kern = kernel();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, p);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (std::getenv("DG_PRINT_CONFIGS"))
+      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d pair 256x256 stages=%d clusters=%d smem=%d\n",
+                   static_cast<int>(kKind), p.M, p.N, p.K, p.G, kPairStages, clusters, Cfg::SMEM_BYTES);
+    return DG_OK;
+  }
+};
+
+bool pair_enabled() {
+  const char* f = std::getenv("DG_PAIR");
+  return !(f && f[0] == '0');
+}
+
+
+
 // Tile width for a problem: DG_FORCE_BN (128, 192 or 256) overrides the heuristic.
 // Measured on GB300 (tile mode): wider tiles cut the L2->SM bytes per FLOP, which is what
 // limits the 128-wide configuration, so the widest tile that wastes no more columns than
@@ -312,6 +382,50 @@ bool map_out(CUtensorMap* m, void* base, int G, int rows, int N) {
   const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(N) * 2 * rows};
   const uint32_t box[3] = {64, 32, 1};
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Dense / contiguous GEMM on CTA pairs: converts the scale words into tcgen05.cp chunks in
+// the stream workspace (two small kernels), then launches the pair kernel.
+template <dg::Kind kKind, bool kHasC>
+dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d,
+                   dg::Params p, int clusters, cudaStream_t stream) {
+  const int KP = ceil_div(p.K / 128, 4);
+  const int num_mb = ceil_div(p.M, 128);
+  const int NB = ceil_div(p.N, 128);
+  const int G = kKind == dg::Kind::Dense ? 1 : p.G;
+  const size_t sfa_words = static_cast<size_t>(KP) * num_mb * 128;
+  const size_t sfb_words = static_cast<size_t>(G) * KP * NB * 128;
+  if (static_cast<size_t>(KP) * num_mb > (1u << 30) || static_cast<size_t>(G) * KP * NB > (1u << 30))
+    return DG_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  if (dg_status s = stream_workspace(ds, stream, kSkCounterInts * 4 + (sfa_words + sfb_words) * 4, &ws); s != DG_OK)
+    return s;
+  int32_t* sfa_t = static_cast<int32_t*>(ws) + kSkCounterInts;
+  int32_t* sfb_t = sfa_t + sfa_words;
+  auto blocks_for = [](size_t n) { return static_cast<unsigned>(std::min<size_t>((n + 255) / 256, 2048)); };
+  dg::sf_to_utccp_kernel<<<blocks_for(sfa_words), 256, 0, stream>>>(sfa, sfa_t, 1, KP, p.M, ceil4(p.M), num_mb, 0);
+  dg::sf_to_utccp_kernel<<<blocks_for(sfb_words), 256, 0, stream>>>(sfb, sfb_t, G, KP, NB, ceil4(NB), NB, 1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  CUtensorMap ta, tb, tsa, tsb, td;
+  bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) && map_out(&td, d, 0, p.M, p.N);
+  if (kKind == dg::Kind::Dense)
+    ok = ok && map_operand_2d(&tb, b, p.N, p.K, 128);
+  else
+    ok = ok && map_operand_3d(&tb, b, G, p.N, p.K, 128);
+  {
+    const uint64_t dims_a[2] = {128, static_cast<uint64_t>(KP) * num_mb};
+    const uint64_t dims_b[2] = {128, static_cast<uint64_t>(G) * KP * NB};
+    const uint64_t strides[1] = {512};
+    const uint32_t box_a[2] = {128, 1}, box_b[2] = {128, 2};
+    ok = ok && make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa_t, dims_a, strides, box_a, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && make_map(&tsb, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfb_t, dims_b, strides, box_b, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!ok) return DG_ERR_CUDA;
+  p.sf_num_mb = num_mb;
+  p.sf_nb = NB;
+  return PairLauncher<kKind, kHasC>::launch(ta, tb, tsa, tsb, td, p, clusters, stream);
 }
 
 dg_status check_common(int N, int K) {
@@ -389,6 +503,26 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
     if (v == 128 || v == 192 || v == 256) sk_bn = v;
   }
   const int BN = tiles128 < sms ? sk_bn : pick_bn(dg::Kind::Dense, N);
+  if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
+    const int max_cl = c ? PairLauncher<dg::Kind::Dense, true>::max_clusters()
+                         : PairLauncher<dg::Kind::Dense, false>::max_clusters();
+    if (max_cl > 0) {
+      dg::Params pp{};
+      pp.M = M;
+      pp.N = N;
+      pp.K = K;
+      pp.G = 1;
+      pp.c = static_cast<const __nv_bfloat16*>(c);
+      pp.d = static_cast<__nv_bfloat16*>(d);
+      pp.status = ds->status;
+      pp.timeout_ns = wait_timeout_ns();
+      pp.fault = g_fault.load();
+      const long long pair_tiles = static_cast<long long>(ceil_div(M, 256)) * ceil_div(N, 256);
+      const int clusters = static_cast<int>(std::min<long long>(std::min(max_cl, sms / 2), pair_tiles));
+      if (c) return run_pair<dg::Kind::Dense, true>(*ds, a, sfa, b, sfb, d, pp, clusters, stream);
+      return run_pair<dg::Kind::Dense, false>(*ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    }
+  }
   if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||
       !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, 0, M, N))
@@ -446,6 +580,26 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   DeviceState* ds = nullptr;
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
 
+  if (pair_enabled() && !std::getenv("DG_FORCE_BN")) {
+    const int max_cl = PairLauncher<dg::Kind::Contiguous, false>::max_clusters();
+    if (max_cl > 0) {
+      dg::Params pp{};
+      pp.M = M_total;
+      pp.N = N;
+      pp.K = K;
+      pp.G = G;
+      pp.m_indices = m_indices;
+      pp.d = static_cast<__nv_bfloat16*>(d);
+      pp.status = ds->status;
+      pp.timeout_ns = wait_timeout_ns();
+      pp.fault = g_fault.load();
+      // the number of pair rows depends on m_indices (device): bound it by the block count
+      const long long pair_tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, 256);
+      const int clusters =
+          static_cast<int>(std::min<long long>(std::min(max_cl, sms_to_use(*ds) / 2), pair_tiles));
+      return run_pair<dg::Kind::Contiguous, false>(*ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    }
+  }
   const int KP = ceil_div(K / 128, 4);
   CUtensorMap ta, tb, tsa, tsb, td;
   const int BN = pick_bn(dg::Kind::Contiguous, N);

@@ -66,6 +66,9 @@ struct Params {
   float* sk_ws;                   // [tiles][sk_slots][128 * BN] FP32 partials
   int* sk_counters;               // [tiles][epilogue warps], zero between launches
   int fault;                      // kFault*
+  // CTA-pair kernel: row counts of the tcgen05.cp-layout scale chunk tensors
+  int sf_num_mb;                  // 128-row blocks of A per K-quad
+  int sf_nb;                      // 128-row blocks of B per (group, K-quad)
 };
 
 __host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) / b; }

@@ -1,0 +1,92 @@
+"""The CTA-pair kernel (two SMs share one 256 x 256 tcgen05 MMA) against the oracle.
+
+Dense problems reach it in tile mode (at least as many 128 x 128 tiles as SMs used);
+the SM cap is lowered so that small problems qualify. Contiguous problems always use it
+(unless DG_PAIR=0)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from gpu_util import SENTINEL, assert_parity, bf16_bits, bf16_f64, run_contiguous, run_dense
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp8_gemm_nt_gb300 as L
+    L.load_library()
+    return L
+
+
+@pytest.fixture
+def few_sms(lib):
+    lib.dg_set_num_sms(8)
+    yield
+    lib.dg_set_num_sms(0)
+
+
+@pytest.mark.parametrize("M,N,K,with_c", [
+    (256, 256, 128, False),
+    (384, 512, 640, True),       # odd number of 128-row blocks: the last pair's second half is empty
+    (300, 400, 1152, True),      # ragged M and N, K-groups not a multiple of 4
+    (1024, 768, 2048, False),    # several pair tiles per CTA pair
+])
+def test_pair_dense(lib, few_sms, M, N, K, with_c):
+    p = W.make_dense(M, N, K, seed=900 + M + N + K, with_c=with_c)
+    d = run_dense(lib, p)
+    ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, M, N, K)
+    assert_parity(bf16_f64(d), ref, f"pair dense {M}x{N}x{K}")
+    assert lib.dg_get_device_status() == 0
+
+
+def test_pair_distinct_block_scales_exact(lib, few_sms):
+    # B blocks of the two CTA halves carry different power-of-two scales, A rows of the two
+    # halves too: a scale placed in the wrong TMEM columns or lanes changes results by a
+    # power of two, so the shifted run must equal the base run times the shift exactly.
+    p = W.make_dense(256, 256, 512, seed=4)
+    base = bf16_f64(run_dense(lib, p))
+    ea = O.unpack_sf(p.sfa, 256, 4).copy()
+    eb = O.unpack_sf(p.sfb, 2, 4).copy()
+    ea[130:140] += 1
+    eb[1] -= 2
+    q = W.Dense(p.a, W.pack_sf(ea), p.b, W.pack_sf(eb), None, 256, 256, 512)
+    got = bf16_f64(run_dense(lib, q))
+    expect = base.copy()
+    expect[130:140] *= 2.0
+    expect[:, 128:] *= 0.25
+    assert np.array_equal(got, expect)
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([300, 100, 300], 512, 512),        # 3, 1 and 3 blocks per expert
+    ([128, 0, 129, 255], 256, 384),
+    ([1, 1, 1, 1, 1], 272, 256),
+])
+def test_pair_contiguous(lib, counts, N, K):
+    p = W.make_contiguous(G=len(counts), tokens=sum(counts), N=N, K=K, seed=950 + N + K, counts=counts)
+    d = run_contiguous(lib, p)
+    ref, valid = O.m_grouped_fp8_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K, p.G)
+    assert (bf16_bits(d)[~valid] == SENTINEL).all()
+    assert_parity(bf16_f64(d)[valid], ref[valid], f"pair contiguous {counts}")
+    assert lib.dg_get_device_status() == 0
+
+
+def test_pair_timeout_path(lib, few_sms):
+    p = W.make_dense(512, 512, 512, seed=5)
+    lib.dg_get_device_status()
+    lib.dg_set_debug(1, 20_000_000)
+    try:
+        run_dense(lib, p)
+        assert lib.dg_get_device_status() == 5
+    finally:
+        lib.dg_set_debug(0, 0)
+    ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, None, p.M, p.N, p.K)
+    assert_parity(bf16_f64(run_dense(lib, p)), ref, "after pair timeout")
+    assert lib.dg_get_device_status() == 0
