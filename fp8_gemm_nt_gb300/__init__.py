@@ -41,6 +41,7 @@ SIGNATURES = [
     ("dg_status_string", ctypes.c_char_p, [_I]),
     ("dg_last_cuda_error", _I, []),
     ("dg_set_debug", _I, [_I, ctypes.c_ulonglong]),
+    ("dg_fp8_gemm_nt_no_alloc", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
 ]
 
 
@@ -206,3 +207,26 @@ def dg_set_debug(fault_mode: int, wait_timeout_ns: int = 0) -> None:
     """Failure-detection test hook: fault_mode 1 makes later launches time out on purpose
     (their producer issues nothing); wait_timeout_ns bounds every pipeline wait (0 = 2 s)."""
     _check("dg_set_debug", load_library().dg_set_debug(fault_mode, wait_timeout_ns))
+
+
+def dg_fp8_gemm_nt_no_alloc(a, sfa, b, sfb, c, d, status, stream=None) -> torch.Tensor:
+    """D = C + A @ B.T without any device allocation by the library, for callers that
+    cannot allocate at call time (graph capture, fixed-footprint servers, custom
+    allocators). Same tensors as dg_fp8_gemm_nt plus `status`, a CUDA uint32/int32 tensor
+    of one element that receives device-side error bits. The library's fixed 16 MiB
+    scratch bounds the problem size (DG_ERR_INVALID_ARG beyond it); calls that overlap on
+    the GPU race on that scratch."""
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d")
+    _need(status.is_cuda and status.numel() == 1 and status.element_size() == 4, "status must be one 4-byte CUDA word")
+    M, K = a.shape
+    N = b.shape[0]
+    _need(b.shape[1] == K and tuple(d.shape) == (M, N), "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(M, K) and tuple(sfb.shape) == sf_shape(-(-N // 128), K), "scale shape mismatch")
+    if c is not None:
+        _bf16(c, "c")
+        _need(tuple(c.shape) == (M, N), "c shape mismatch")
+    _check("dg_fp8_gemm_nt_no_alloc",
+           lib.dg_fp8_gemm_nt_no_alloc(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d), _ptr(status),
+                                       M, N, K, _stream(stream)))
+    return d

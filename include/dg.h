@@ -125,6 +125,39 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa,
 dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgroups,
                            cudaStream_t stream);
 
+/*
+ * Dense GEMM that allocates no device memory (the pages have no counterpart: this is an
+ * extra entry point of this library).
+ *
+ * For callers that cannot allocate when they run the GEMM: code being captured into a
+ * CUDA graph, servers that fix their device-memory footprint at start-up, or a custom
+ * allocator that owns all device memory. dg_fp8_gemm_nt allocates on first use (a status
+ * word, and a per-stream workspace for problems with fewer 128x128 tiles than SMs); this
+ * entry point uses instead a fixed 16 MiB scratch array that the library holds in device
+ * memory from the first call on each GPU until the process exits.
+ *
+ * Computes the same D = C + A @ B.T as dg_fp8_gemm_nt, with the same argument meanings and
+ * layouts, through the same kernel in its stream-K mode (the K-groups of all 128x128 tiles
+ * shared among the SMs), so results match dg_fp8_gemm_nt within the parity tolerance.
+ *   status : caller-owned DEVICE uint32 word (4-byte aligned); device-side errors are OR-ed
+ *            into it as bit (1 << DG_ERR_TIMEOUT). It is not cleared by the call.
+ * Limits: the problem must fit the scratch: 16 KiB of counters (at most 1024 tiles of
+ * 128x128) plus tiles x contributors-per-tile x 64 KiB of FP32 partials (the 128x7168
+ * decode shape uses about 14.7 MiB). Larger problems return DG_ERR_INVALID_ARG with nothing
+ * launched; use dg_fp8_gemm_nt for them.
+ * The first call on a device looks up the scratch array's device address (once per device,
+ * with that device current); make that first call before any stream capture. Every call
+ * shares the one array and it keeps the previous call's contents: each call clears the
+ * counters it needs (an asynchronous memset on `stream`) before its kernel. Calls whose work
+ * overlaps on the GPU (different streams, or several host threads) race on the array: keep
+ * them ordered on one stream.
+ * Calls no cudaMalloc / cudaFree and no allocating library routine.
+ */
+dg_status dg_fp8_gemm_nt_no_alloc(const void* a, const int32_t* sfa,
+                                  const void* b, const int32_t* sfb,
+                                  const void* c, void* d, uint32_t* status,
+                                  int M, int N, int K, cudaStream_t stream);
+
 /* Row alignment of each expert segment in the contiguous layout (the M block): 128. */
 int dg_get_mk_alignment_for_contiguous_layout(void);
 
