@@ -77,7 +77,8 @@ template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs>
 struct Config {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
   static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue uses 4 or 8 warps");
-  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kSfWarp = 2 + kEpiWarps;                 // rearranges the scale words
+  static constexpr int kThreads = (3 + kEpiWarps) * 32;
   static constexpr int kColsPerEpiWarp = BN / (kEpiWarps / 4);
   static_assert(kColsPerEpiWarp % 64 == 0, "each epilogue warp stores whole 64-column chunks");
 
@@ -97,7 +98,7 @@ struct Config {
   static constexpr int OFF_SF = OFF_B + kStages * B_BYTES;
   static constexpr int OFF_EPI = ((OFF_SF + kStages * SF_BYTES + 1023) / 1024) * 1024;
   static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * kEpiBufs * EPI_BUF_BYTES;
-  static constexpr int NUM_BARS = 2 * kStages + 2 * kNumAccum + 1;
+  static constexpr int NUM_BARS = 3 * kStages + 2 * kNumAccum + 1;   // + scale-ready per stage
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;       // + slack for manual alignment
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
@@ -281,6 +282,8 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
   uint64_t* tfull_bar = bars + 2 * kStages;
   uint64_t* tempty_bar = bars + 2 * kStages + kNumAccum;
   uint64_t* drain_bar = bars + 2 * kStages + 2 * kNumAccum;
+  // scale words of a stage rearranged by the scale warp (used on scale stages only)
+  uint64_t* sf_ready_bar = bars + 2 * kStages + 2 * kNumAccum + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -290,13 +293,14 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], 2);   // the MMA commit and the scale warp
     }
     for (int a = 0; a < kNumAccum; ++a) {
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&sf_ready_bar[s], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -383,92 +387,123 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     }
   } else if (warp == 1) {
     // ================================ MMA issuer ==================================
-    constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(BLOCK_M, BN);
-    uint32_t stage = 0, phase = 0, seg_iter = 0, sf_iter = 0;
-    while (sched.next(p, seg)) {
-      const uint32_t acc = seg_iter % kNumAccum;
-      const uint32_t acc_phase = (seg_iter / kNumAccum) & 1;
-      if (!warp_wait(&tempty_bar[acc], acc_phase ^ 1, p.timeout_ns, abort_flag)) {
-        if (lane == 0) on_timeout();
-        goto mma_done;
-      }
-      tc_fence_after();
-      {
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        const int n0 = seg.n_blk * BN;
-        const int sfb_x = (n0 / SF_BLOCK_N) & ~3;
-        uint32_t sfa_tmem = 0, sfb_tmem = 0;
-        for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
-          if (!warp_wait(&full_bar[stage], phase, p.timeout_ns, abort_flag)) {
-            if (lane == 0) on_timeout();
-            goto mma_done;
-          }
-          tc_fence_after();
-          const uint32_t sf_base = smem_addr(smem + C::OFF_SF + stage * C::SF_BYTES);
-          if (kb == seg.kb_begin || kb % 4 == 0) {
-            // Scale words -> tcgen05.cp source layout: row r (= TMEM lane r of every
-            // sub-partition) holds, in word c, the scale word of tile row 32c + r.
-            const uint32_t a0 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * lane);
-            const uint32_t a1 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 32));
-            const uint32_t a2 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 64));
-            const uint32_t a3 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 96));
-            st_shared_v4(sf_base + C::SF_UT_A + 16 * lane, a0, a1, a2, a3);
-#pragma unroll
-            for (int ch = 0; ch < C::SFB_CHUNKS; ++ch) {
-              uint32_t w[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int n = n0 + 128 * ch + static_cast<int>(lane) + 32 * j;
-                w[j] = ld_shared_u32(sf_base + C::SF_RAW_B + 4 * (n / SF_BLOCK_N - sfb_x));
-              }
-              st_shared_v4(sf_base + C::SF_UT_B + 512 * ch + 16 * lane, w[0], w[1], w[2], w[3]);
+    // A single thread runs the whole loop: waits, scale copies into TMEM, four MMAs per
+    // K-group and the commits, with no warp-wide synchronisation per K-group (measured on
+    // GB300: each tcgen05.mma issue costs ~75 cycles and a warp-wide wait path ~400, so the
+    // loop, not the tensor pipe, set the pace).
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(BLOCK_M, BN);
+      const uint64_t a_desc0 = make_smem_desc(smem_addr(smem + C::OFF_A), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t b_desc0 = make_smem_desc(smem_addr(smem + C::OFF_B), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t sf_desc0 = make_smem_desc(smem_addr(smem + C::OFF_SF), 0, 128, kLayoutNone);
+      uint32_t stage = 0, phase = 0, seg_iter = 0, sf_iter = 0, sf_parity = 0;
+      while (sched.next(p, seg)) {
+        const uint32_t acc = seg_iter % kNumAccum;
+        const uint32_t acc_phase = (seg_iter / kNumAccum) & 1;
+        if (*abort_flag || !mbar_wait(&tempty_bar[acc], acc_phase ^ 1, p.timeout_ns)) {
+          on_timeout();
+          goto mma_done;
+        }
+        tc_fence_after();
+        {
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          uint32_t sfa_tmem = 0, sfb_tmem = 0;
+          for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
+            if (!mbar_wait(&full_bar[stage], phase, p.timeout_ns)) {
+              on_timeout();
+              goto mma_done;
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            const uint32_t buf = sf_iter & 1;
-            ++sf_iter;
-            sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
-            sfb_tmem = tmem_base + C::SFB_COL + 4 * C::SFB_CHUNKS * buf;
-            if (lane == 0) {
-              tmem_copy_32x128b_warpx4(sfa_tmem, make_smem_desc(sf_base + C::SF_UT_A, 0, 128, kLayoutNone));
+            if (kb == seg.kb_begin || kb % 4 == 0) {
+              // the scale warp has rearranged this stage's scale words for tcgen05.cp
+              if (!mbar_wait(&sf_ready_bar[stage], (sf_parity >> stage) & 1u, p.timeout_ns)) {
+                on_timeout();
+                goto mma_done;
+              }
+              sf_parity ^= 1u << stage;
+              tc_fence_after();
+              const uint32_t buf = sf_iter & 1;
+              ++sf_iter;
+              sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
+              sfb_tmem = tmem_base + C::SFB_COL + 4 * C::SFB_CHUNKS * buf;
+              const uint64_t sf_desc = sf_desc0 + ((stage * C::SF_BYTES) >> 4);
+              tmem_copy_32x128b_warpx4(sfa_tmem, sf_desc + (C::SF_UT_A >> 4));
 #pragma unroll
               for (int ch = 0; ch < C::SFB_CHUNKS; ++ch)
-                tmem_copy_32x128b_warpx4(sfb_tmem + 4 * ch,
-                                         make_smem_desc(sf_base + C::SF_UT_B + 512 * ch, 0, 128, kLayoutNone));
+                tmem_copy_32x128b_warpx4(sfb_tmem + 4 * ch, sf_desc + ((C::SF_UT_B + 512 * ch) >> 4));
+            } else {
+              tc_fence_after();
             }
-          }
-          if (lane == 0) {
-            const uint32_t a_base = smem_addr(smem + C::OFF_A + stage * C::A_BYTES);
-            const uint32_t b_base = smem_addr(smem + C::OFF_B + stage * C::B_BYTES);
+            // descriptor address field is (address >> 4): stage and 32-byte K steps add to it
+            const uint64_t adesc = a_desc0 + ((stage * C::A_BYTES) >> 4);
+            const uint64_t bdesc = b_desc0 + ((stage * C::B_BYTES) >> 4);
             const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
 #pragma unroll
-            for (int k = 0; k < BLOCK_K / 32; ++k) {
-              const uint64_t adesc = make_smem_desc(a_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
-              const uint64_t bdesc = make_smem_desc(b_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
-              mma_mxf8_block_scale(d_tmem, adesc, bdesc, idesc, sfa_tmem, sfb_tmem,
+            for (int k = 0; k < BLOCK_K / 32; ++k)
+              mma_mxf8_block_scale(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
                                    (kb != seg.kb_begin || k != 0) ? 1u : 0u);
-            }
             tc_commit(&empty_bar[stage]);
-          }
-          __syncwarp();
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
+        tc_commit(&tfull_bar[acc]);
+        ++seg_iter;
       }
-      if (lane == 0) tc_commit(&tfull_bar[acc]);
-      __syncwarp();
-      ++seg_iter;
-    }
-  mma_done:
-    // Every MMA / copy issued above must have finished before TMEM is released.
-    if (lane == 0) {
+    mma_done:
+      // Every MMA / copy issued above must have finished before TMEM is released.
       tc_commit(drain_bar);
       mbar_wait(drain_bar, 0, 50000000ull);
     }
     __syncwarp();
-  } else {
+  } else if (warp == C::kSfWarp) {
+    // ================================ scale warp ==================================
+    // Walks every stage in order. On a stage that carries scale words it rearranges them
+    // into the tcgen05.cp source layout (row r holds, in word c, the word of tile row
+    // 32c + r; B's per-block words replicated per row) and signals the MMA thread. It is the
+    // second arrival on every stage's empty barrier, so the producer cannot refill a stage
+    // this warp has not seen: its parity waits can never alias a later phase.
+    uint32_t stage = 0, phase = 0;
+    while (sched.next(p, seg)) {
+      const int n0 = seg.n_blk * BN;
+      const int sfb_x = (n0 / SF_BLOCK_N) & ~3;
+      for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
+        if (!warp_wait(&full_bar[stage], phase, p.timeout_ns, abort_flag)) {
+          if (lane == 0) on_timeout();
+          goto sf_done;
+        }
+        if (kb == seg.kb_begin || kb % 4 == 0) {
+          const uint32_t sf_base = smem_addr(smem + C::OFF_SF + stage * C::SF_BYTES);
+          const uint32_t a0 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * lane);
+          const uint32_t a1 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 32));
+          const uint32_t a2 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 64));
+          const uint32_t a3 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 96));
+          st_shared_v4(sf_base + C::SF_UT_A + 16 * lane, a0, a1, a2, a3);
+#pragma unroll
+          for (int ch = 0; ch < C::SFB_CHUNKS; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int n = n0 + 128 * ch + static_cast<int>(lane) + 32 * j;
+              w[j] = ld_shared_u32(sf_base + C::SF_RAW_B + 4 * (n / SF_BLOCK_N - sfb_x));
+            }
+            st_shared_v4(sf_base + C::SF_UT_B + 512 * ch + 16 * lane, w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sf_ready_bar[stage]);
+        }
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  sf_done:
+    __syncwarp();
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // ================================ epilogue ====================================
     const int ew = warp - 2;
     const int quad = warp % 4;                      // TMEM sub-partition this warp may access

@@ -251,64 +251,59 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ================================ MMA issuer (leader) ===========================
-    if (leader) {
+    // One thread of the leader runs the whole loop (no warp-wide synchronisation per K-group).
+    if (leader && lane == 0) {
       constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(2 * BLOCK_M, C::BN);
+      const uint64_t a_desc0 = make_smem_desc(smem_addr(smem + C::OFF_A), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t b_desc0 = make_smem_desc(smem_addr(smem + C::OFF_B), 16, 1024, kLayoutSwizzle128B);
+      const uint64_t sf_desc0 = make_smem_desc(smem_addr(smem + C::OFF_SF), 0, 128, kLayoutNone);
       uint32_t stage = 0, phase = 0, tile_iter = 0, sf_iter = 0;
       while (sched.next(p, seg)) {
-        if (!warp_wait(tempty_bar, (tile_iter & 1) ^ 1, p.timeout_ns, abort_flag)) {
-          if (lane == 0) on_timeout();
+        if (*abort_flag || !mbar_wait(tempty_bar, (tile_iter & 1) ^ 1, p.timeout_ns)) {
+          on_timeout();
           goto mma_done;
         }
         tc_fence_after();
         {
           uint32_t sfa_tmem = 0, sfb_tmem = 0;
           for (int kb = 0; kb < num_kb; ++kb) {
-            if (!warp_wait(&full_bar[stage], phase, p.timeout_ns, abort_flag)) {
-              if (lane == 0) on_timeout();
+            if (!mbar_wait(&full_bar[stage], phase, p.timeout_ns)) {
+              on_timeout();
               goto mma_done;
             }
             tc_fence_after();
-            if (lane == 0) {
-              const uint32_t sf_base = smem_addr(smem + C::OFF_SF + stage * C::SF_STRIDE);
-              if (kb % 4 == 0) {
-                const uint32_t buf = sf_iter & 1;
-                ++sf_iter;
-                sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
-                sfb_tmem = tmem_base + C::SFB_COL + 8 * buf;
-                tmem_copy_32x128b_warpx4_pair(sfa_tmem, make_smem_desc(sf_base, 0, 128, kLayoutNone));
-                tmem_copy_32x128b_warpx4_pair(sfb_tmem, make_smem_desc(sf_base + C::SFA_BYTES, 0, 128, kLayoutNone));
-                tmem_copy_32x128b_warpx4_pair(sfb_tmem + 4,
-                                              make_smem_desc(sf_base + C::SFA_BYTES + 512, 0, 128, kLayoutNone));
-              }
-              const uint32_t a_base = smem_addr(smem + C::OFF_A + stage * C::A_BYTES);
-              const uint32_t b_base = smem_addr(smem + C::OFF_B + stage * C::B_BYTES);
-              const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
-#pragma unroll
-              for (int k = 0; k < BLOCK_K / 32; ++k) {
-                const uint64_t adesc = make_smem_desc(a_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
-                const uint64_t bdesc = make_smem_desc(b_base + 32 * k, 16, 1024, kLayoutSwizzle128B);
-                mma_mxf8_block_scale_pair(tmem_base, adesc, bdesc, idesc, sfa_tmem, sfb_tmem, (kb | k) != 0);
-              }
-              tc_commit_pair(&empty_bar[stage]);
+            if (kb % 4 == 0) {
+              const uint32_t buf = sf_iter & 1;
+              ++sf_iter;
+              sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
+              sfb_tmem = tmem_base + C::SFB_COL + 8 * buf;
+              const uint64_t sf_desc = sf_desc0 + ((stage * C::SF_STRIDE) >> 4);
+              tmem_copy_32x128b_warpx4_pair(sfa_tmem, sf_desc);
+              tmem_copy_32x128b_warpx4_pair(sfb_tmem, sf_desc + (C::SFA_BYTES >> 4));
+              tmem_copy_32x128b_warpx4_pair(sfb_tmem + 4, sf_desc + ((C::SFA_BYTES + 512) >> 4));
             }
-            __syncwarp();
+            const uint64_t adesc = a_desc0 + ((stage * C::A_BYTES) >> 4);
+            const uint64_t bdesc = b_desc0 + ((stage * C::B_BYTES) >> 4);
+            const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
+#pragma unroll
+            for (int k = 0; k < BLOCK_K / 32; ++k)
+              mma_mxf8_block_scale_pair(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
+                                        (kb | k) != 0);
+            tc_commit_pair(&empty_bar[stage]);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
             }
           }
         }
-        if (lane == 0) tc_commit_pair(tfull_bar);
-        __syncwarp();
+        tc_commit_pair(tfull_bar);
         ++tile_iter;
       }
     mma_done:
-      if (lane == 0) {
-        tc_commit_pair(drain_bar);
-        mbar_wait(drain_bar, 0, 50000000ull);
-      }
-      __syncwarp();
+      tc_commit_pair(drain_bar);
+      mbar_wait(drain_bar, 0, 50000000ull);
     }
+    __syncwarp();
   } else {
     // ================================ epilogue (both CTAs) ==========================
     const int ew = warp - 2;
