@@ -117,6 +117,14 @@ dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, v
 // ------------------------------------------------------------------------------------
 // TMA descriptors
 // ------------------------------------------------------------------------------------
+// Programmatic dependent launch (DG_PDL=0 disables): a GEMM may start its prologue while the
+// previous kernel in the stream finishes; the kernels wait for that grid before touching
+// global memory.
+bool pdl_enabled() {
+  const char* f = std::getenv("DG_PDL");
+  return !(f && f[0] == '0');
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -201,16 +209,17 @@ inline int ceil4(int x) { return 4 * ceil_div(x, 4); }
 // ------------------------------------------------------------------------------------
 // Kernel configurations
 // ------------------------------------------------------------------------------------
-template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps_, int kEpiBufs, bool kHasC>
+template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps_, int kEpiBufs, bool kHasC,
+          int kKG = 1>
 struct Launcher {
   static constexpr int kEpiWarps = kEpiWarps_;
-  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs>;
+  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG>;
   static constexpr int kBN = BN;
 
   static dg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                           const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
                           cudaStream_t stream) {
-    auto kern = dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC>;
+    auto kern = dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG>;
     static thread_local int attr_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -219,8 +228,17 @@ struct Launcher {
       if (e != cudaSuccess) return cuda_fail(e);
       attr_dev = dev;
     }
-    kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, td, p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, p);
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
       std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d BN=%d stages=%d accum=%d epi_warps=%d grid=%d smem=%d stream_k=%d\n",
@@ -234,10 +252,15 @@ struct Launcher {
 //   128: 5-stage ring, double-buffered accumulators (TMEM 2 x 128 columns)
 //   192: 4-stage ring, double-buffered accumulators (TMEM 2 x 192 columns)
 //   256: 4-stage ring, single accumulator (TMEM 256 columns; 2 x 256 + scales exceeds 512)
+//   128 x 2: two K-groups per stage (64 KB stages, 3 of them), for HBM-bound stream-K shapes
 template <dg::Kind kKind, bool kHasC>
 dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                     const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, int kgroups_per_stage = 1) {
+  if constexpr (kKind == dg::Kind::Dense) {
+    if (kgroups_per_stage == 2 && bn == 128)
+      return Launcher<kKind, 128, 3, 2, 4, 1, kHasC, 2>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+  }
   switch (bn) {
     case 128: return Launcher<kKind, 128, 5, 2, 4, 2, kHasC>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
     case 192: return Launcher<kKind, 192, 4, 2, 4, 2, kHasC>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
@@ -289,17 +312,19 @@ struct PairLauncher {
                           cudaStream_t stream) {
     auto kern = kernel();
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, p);
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
@@ -540,15 +565,22 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   const long long tiles = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, BN);
   int grid = static_cast<int>(tiles < sms ? tiles : sms);
   // Fewer tiles than SMs: share the K-groups of all tiles among all SMs (stream-K) so that
-  // every SM streams operands; each CTA gets at least kMinKGroupsPerCta K-groups.
-  const long long kgroups = tiles * (K / 128);
-  const long long sk = std::min<long long>(sms, kgroups / kMinKGroupsPerCta);
+  // every SM streams operands; each CTA gets at least kMinKGroupsPerCta K-groups. The
+  // stream-K unit is one pipeline stage: two K-groups for 128-wide tiles (DG_KG=1 selects
+  // one K-group per stage), one otherwise.
+  int kg = 1;
+  if (BN == 128) {
+    const char* f = std::getenv("DG_KG");
+    kg = (f && f[0] == '1') ? 1 : 2;
+  }
+  const int num_kc = ceil_div(K / 128, kg);                 // stream-K units per tile
+  const long long units = tiles * num_kc;
+  const long long sk = std::min<long long>(sms, units * kg / kMinKGroupsPerCta);
   if (tiles < sms && sk > tiles) {
-    const int num_kb = K / 128;
     int slots = 1;
     for (long long t = 0; t < tiles; ++t) {
-      auto owner = [&](long long v) { return ((v + 1) * sk - 1) / kgroups; };
-      const int n = static_cast<int>(owner(t * num_kb + num_kb - 1) - owner(t * num_kb) + 1);
+      auto owner = [&](long long v) { return ((v + 1) * sk - 1) / units; };
+      const int n = static_cast<int>(owner(t * num_kc + num_kc - 1) - owner(t * num_kc) + 1);
       slots = std::max(slots, n);
     }
     // Layout: a fixed-size counter region first (its position must not depend on the
@@ -562,9 +594,11 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
     p.sk_counters = static_cast<int*>(ws);
     p.sk_ws = reinterpret_cast<float*>(static_cast<int*>(ws) + kSkCounterInts);
     grid = static_cast<int>(sk);
+  } else {
+    kg = 1;   // tile mode: whole tiles, one K-group per stage
   }
-  if (c) return launch_bn<dg::Kind::Dense, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
-  return launch_bn<dg::Kind::Dense, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+  if (c) return launch_bn<dg::Kind::Dense, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
+  return launch_bn<dg::Kind::Dense, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
@@ -580,7 +614,11 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   DeviceState* ds = nullptr;
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
 
-  if (pair_enabled() && !std::getenv("DG_FORCE_BN")) {
+  // The contiguous form runs on single-CTA 128x256 tiles by default (measured faster on
+  // GB300 than the CTA-pair kernel for the G=8 workload: 2856 vs 2730 TFLOPS); DG_PAIR=1
+  // selects the pair kernel.
+  const char* pair_env = std::getenv("DG_PAIR");
+  if (pair_env && pair_env[0] == '1' && !std::getenv("DG_FORCE_BN")) {
     const int max_cl = PairLauncher<dg::Kind::Contiguous, false>::max_clusters();
     if (max_cl > 0) {
       dg::Params pp{};

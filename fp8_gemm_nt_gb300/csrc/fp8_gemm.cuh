@@ -73,8 +73,13 @@ struct Params {
 
 __host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) / b; }
 
-template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs>
+// kKG = K-groups per pipeline stage (1 or 2). Two K-groups per stage double the bytes
+// each TMA round trip moves; on GB300 a single producer thread streams markedly more from
+// HBM with 64 KB stages than with 32 KB ones (measured 5.2 vs 4.1 TB/s in a TMA-only
+// probe with the decode shape's A and B boxes), which is what the HBM-bound shapes need.
+template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, int kKG = 1>
 struct Config {
+  static_assert(kKG == 1 || kKG == 2, "one or two K-groups per stage");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
   static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue uses 4 or 8 warps");
   static constexpr int kSfWarp = 2 + kEpiWarps;                 // rearranges the scale words
@@ -83,8 +88,10 @@ struct Config {
   static_assert(kColsPerEpiWarp % 64 == 0, "each epilogue warp stores whole 64-column chunks");
 
   // shared memory (offsets from a 1024-byte-aligned base)
-  static constexpr int A_BYTES = BLOCK_M * BLOCK_K;
-  static constexpr int B_BYTES = BN * BLOCK_K;
+  static constexpr int A_SUB = BLOCK_M * BLOCK_K;               // one K-group of A
+  static constexpr int B_SUB = BN * BLOCK_K;                    // one K-group of B
+  static constexpr int A_BYTES = kKG * A_SUB;                   // per stage
+  static constexpr int B_BYTES = kKG * B_SUB;
   static constexpr int SFB_CHUNKS = ceil_div_c(BN, 128);        // 128-row chunks of B scale rows
   static constexpr int SF_RAW_A = 0;                            // 128 words as loaded (row-major)
   static constexpr int SF_RAW_B = 512;                          // 8 block words as loaded
@@ -131,11 +138,12 @@ struct Segment {
   int kb_end;
   int n_contrib;  // CTAs contributing to this tile (1 = this segment is the whole tile)
   int slot;       // this CTA's position among them
+  bool cta_last;  // stream-K: no further segment for this CTA (its ring smem is free afterwards)
 };
 
-template <Kind kKind, int BN>
+template <Kind kKind, int BN, int kKG = 1>
 struct Scheduler {
-  int num_n, num_m, total, num_kb;
+  int num_n, num_m, total, num_kb, num_kc;   // num_kc: stream-K units (kKG K-groups) per tile
   int g_cur, g_start, g_tiles;   // masked: incremental walk over groups
   int t;                         // tile mode: next tile index
   long long u, u_end, U;         // stream-K: this CTA's K-group range, total K-groups
@@ -150,6 +158,7 @@ struct Scheduler {
     num_n = ceil_div_c(p.N, BN);
     num_m = ceil_div_c(p.M, BLOCK_M);
     num_kb = p.K / BLOCK_K;
+    num_kc = ceil_div_c(num_kb, kKG);
     g_cur = 0;
     g_start = 0;
     g_tiles = 0;
@@ -171,7 +180,7 @@ struct Scheduler {
       if constexpr (kKind == Kind::Dense) {
         if (p.sk_ctas > 0) {
           stream_k = true;
-          U = static_cast<long long>(total) * num_kb;
+          U = static_cast<long long>(total) * num_kc;
           u = static_cast<long long>(blockIdx.x) * U / p.sk_ctas;
           u_end = static_cast<long long>(blockIdx.x + 1) * U / p.sk_ctas;
         }
@@ -179,7 +188,7 @@ struct Scheduler {
     }
   }
 
-  // CTA whose K-group range contains flattened K-group index v.
+  // CTA whose unit range contains flattened unit index v (a unit is kKG K-groups).
   __device__ __forceinline__ int sk_owner(const Params& p, long long v) const {
     return static_cast<int>(((v + 1) * p.sk_ctas - 1) / U);
   }
@@ -189,20 +198,23 @@ struct Scheduler {
   __device__ __forceinline__ bool next(const Params& p, Segment& s) {
     if (stream_k) {
       if (u >= u_end) return false;
-      const int tile = static_cast<int>(u / num_kb);
+      const int tile = static_cast<int>(u / num_kc);
       s.tile = tile;
       s.m_blk = tile / num_n;
       s.n_blk = tile % num_n;
       s.g = 0;
       s.valid_m = p.M;
-      s.kb_begin = static_cast<int>(u - static_cast<long long>(tile) * num_kb);
+      const int kc_begin = static_cast<int>(u - static_cast<long long>(tile) * num_kc);
       const long long left = u_end - u;
-      s.kb_end = static_cast<int>(left < num_kb - s.kb_begin ? s.kb_begin + left : num_kb);
-      const int first = sk_owner(p, static_cast<long long>(tile) * num_kb);
-      const int last = sk_owner(p, static_cast<long long>(tile) * num_kb + num_kb - 1);
+      const int kc_end = static_cast<int>(left < num_kc - kc_begin ? kc_begin + left : num_kc);
+      s.kb_begin = kc_begin * kKG;
+      s.kb_end = kc_end * kKG < num_kb ? kc_end * kKG : num_kb;
+      const int first = sk_owner(p, static_cast<long long>(tile) * num_kc);
+      const int last = sk_owner(p, static_cast<long long>(tile) * num_kc + num_kc - 1);
       s.n_contrib = last - first + 1;
       s.slot = static_cast<int>(blockIdx.x) - first;
-      u += s.kb_end - s.kb_begin;
+      u += kc_end - kc_begin;
+      s.cta_last = u >= u_end;
       return true;
     }
     while (t < total) {
@@ -213,6 +225,7 @@ struct Scheduler {
       s.kb_end = num_kb;
       s.n_contrib = 1;
       s.slot = 0;
+      s.cta_last = false;
       if constexpr (kKind == Kind::Masked) {
         while (cur >= g_start + g_tiles && g_cur + 1 < p.G) {
           g_start += g_tiles;
@@ -267,12 +280,12 @@ __device__ __forceinline__ float4 ld_global_cg_v4f(const float* p) {
   return v;
 }
 
-template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC>
-__global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs>::kThreads, 1)
+template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC, int kKG = 1>
+__global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_d, const Params p) {
-  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs>;
+  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -320,13 +333,17 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // With programmatic dependent launch this kernel may start while the previous one in the
+  // stream is finishing: everything above overlapped it; nothing below may read or write
+  // global memory before that grid has completed.
+  grid_dependency_wait();
 
   auto on_timeout = [&]() {
     atomicOr(p.status, kStatusTimeoutBit);
     *abort_flag = 1;
   };
 
-  Scheduler<kKind, BN> sched(p);
+  Scheduler<kKind, BN, kKG> sched(p);
   Segment seg;
 
   if (warp == 0) {
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
         const int row0 = seg.m_blk * BLOCK_M;
         const int n0 = seg.n_blk * BN;
         const int sfb_x = (n0 / SF_BLOCK_N) & ~3;   // 16-byte aligned start of the block-scale window
-        for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
+        for (int kb = seg.kb_begin; kb < seg.kb_end; kb += kKG) {
           if (*abort_flag || !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns)) {
             on_timeout();
             goto producer_done;
@@ -348,15 +365,19 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
           uint8_t* sa = smem + C::OFF_A + stage * C::A_BYTES;
           uint8_t* sb = smem + C::OFF_B + stage * C::B_BYTES;
           uint8_t* ssf = smem + C::OFF_SF + stage * C::SF_BYTES;
-          if constexpr (kKind == Kind::Masked) {
-            tma_load_3d(sa, &tm_a, fb, kb * BLOCK_K, row0, seg.g);
-          } else {
-            tma_load_2d(sa, &tm_a, fb, kb * BLOCK_K, row0);
-          }
-          if constexpr (kKind == Kind::Dense) {
-            tma_load_2d(sb, &tm_b, fb, kb * BLOCK_K, n0);
-          } else {
-            tma_load_3d(sb, &tm_b, fb, kb * BLOCK_K, n0, seg.g);
+          // (with two K-groups per stage, a second K-group past K reads zeros)
+#pragma unroll
+          for (int j = 0; j < kKG; ++j) {
+            if constexpr (kKind == Kind::Masked) {
+              tma_load_3d(sa + j * C::A_SUB, &tm_a, fb, (kb + j) * BLOCK_K, row0, seg.g);
+            } else {
+              tma_load_2d(sa + j * C::A_SUB, &tm_a, fb, (kb + j) * BLOCK_K, row0);
+            }
+            if constexpr (kKind == Kind::Dense) {
+              tma_load_2d(sb + j * C::B_SUB, &tm_b, fb, (kb + j) * BLOCK_K, n0);
+            } else {
+              tma_load_3d(sb + j * C::B_SUB, &tm_b, fb, (kb + j) * BLOCK_K, n0, seg.g);
+            }
           }
           if (with_sf) {
             if constexpr (kKind == Kind::Masked) {
@@ -378,6 +399,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
         }
       }
     producer_done:
+      grid_launch_dependents();   // every load of this CTA is issued: the next grid may be scheduled
       // No TMA write may still be landing in this CTA's shared memory at exit: wait for
       // the last use of every stage (already consumed on the normal path).
       for (uint32_t s = 0; s < kStages && s < issued; ++s) {
@@ -408,7 +430,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
         {
           const uint32_t d_tmem = tmem_base + acc * BN;
           uint32_t sfa_tmem = 0, sfb_tmem = 0;
-          for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
+          for (int kb = seg.kb_begin; kb < seg.kb_end; kb += kKG) {
             if (!mbar_wait(&full_bar[stage], phase, p.timeout_ns)) {
               on_timeout();
               goto mma_done;
@@ -434,13 +456,18 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
               tc_fence_after();
             }
             // descriptor address field is (address >> 4): stage and 32-byte K steps add to it
-            const uint64_t adesc = a_desc0 + ((stage * C::A_BYTES) >> 4);
-            const uint64_t bdesc = b_desc0 + ((stage * C::B_BYTES) >> 4);
-            const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
 #pragma unroll
-            for (int k = 0; k < BLOCK_K / 32; ++k)
-              mma_mxf8_block_scale(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
-                                   (kb != seg.kb_begin || k != 0) ? 1u : 0u);
+            for (int j = 0; j < kKG; ++j) {
+              if (kb + j < seg.kb_end) {
+                const uint64_t adesc = a_desc0 + ((stage * C::A_BYTES + j * C::A_SUB) >> 4);
+                const uint64_t bdesc = b_desc0 + ((stage * C::B_BYTES + j * C::B_SUB) >> 4);
+                const uint32_t idesc = idesc_with_sf_id(kIdesc, (kb + j) % 4, (kb + j) % 4);
+#pragma unroll
+                for (int k = 0; k < BLOCK_K / 32; ++k)
+                  mma_mxf8_block_scale(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
+                                       (kb + j != seg.kb_begin || k != 0) ? 1u : 0u);
+              }
+            }
             tc_commit(&empty_bar[stage]);
             if (++stage == kStages) {
               stage = 0;
@@ -468,7 +495,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     while (sched.next(p, seg)) {
       const int n0 = seg.n_blk * BN;
       const int sfb_x = (n0 / SF_BLOCK_N) & ~3;
-      for (int kb = seg.kb_begin; kb < seg.kb_end; ++kb) {
+      for (int kb = seg.kb_begin; kb < seg.kb_end; kb += kKG) {
         if (!warp_wait(&full_bar[stage], phase, p.timeout_ns, abort_flag)) {
           if (lane == 0) on_timeout();
           goto sf_done;
@@ -543,9 +570,9 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
       const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
 
       // (+C) -> BF16 -> swizzled smem -> TMA store / predicated rows, for one 64-column chunk
-      auto store_chunk = [&](float (&f)[64], int col) {
+      auto store_chunk = [&](float (&f)[64], int col, bool c_added = false) {
         if constexpr (kHasC) {
-          if (row_ok) {
+          if (row_ok && !c_added) {
             const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -666,6 +693,75 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
           __threadfence();
           const float* tile_ws = p.sk_ws + static_cast<long long>(seg.tile) * p.sk_slots * C::SK_TILE_FLOATS +
                                  ew * C::SK_WARP_FLOATS;
+          // This CTA's last segment: the ring's shared memory is idle (every load consumed,
+          // every MMA complete), so each warp gathers all contributors' partials of a chunk
+          // (and its C rows) with asynchronous copies in one round trip, then sums them in
+          // slot order from shared memory.
+          constexpr int kRingBytes = C::OFF_EPI - C::OFF_A;
+          constexpr int kWarpRing = (kRingBytes / kEpiWarps) & ~1023;
+          constexpr int kChunkSlotBytes = 16 * 32 * 16;         // 16 float4 per lane per chunk
+          constexpr int kCBytes = kHasC ? 32 * 128 : 0;         // 32 rows x 64 BF16 columns
+          if (seg.cta_last && seg.n_contrib * kChunkSlotBytes + kCBytes <= kWarpRing) {
+            const uint32_t region = smem_addr(smem + C::OFF_A) + ew * kWarpRing;
+#pragma unroll 1
+            for (int ch = 0; ch < kChunks; ++ch) {
+              const int col = col_part * C::kColsPerEpiWarp + ch * 64;
+#pragma unroll 1
+              for (int s = 0; s < seg.n_contrib; ++s) {
+                const float* src = tile_ws + static_cast<long long>(s) * C::SK_TILE_FLOATS;
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                  cp_async_16(region + s * kChunkSlotBytes + (q * 32 + lane) * 16,
+                              src + ((ch * 16 + q) * 32 + lane) * 4);
+              }
+              if constexpr (kHasC) {
+                if (row_ok) {
+                  const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
+#pragma unroll
+                  for (int q = 0; q < 8; ++q)
+                    if (n0 + col + 8 * q < p.N)
+                      cp_async_16(region + seg.n_contrib * kChunkSlotBytes + lane * 128 + q * 16, crow + 8 * q);
+                }
+              }
+              cp_async_wait_all();
+              __syncwarp();
+              float f[64];
+#pragma unroll
+              for (int i = 0; i < 64; ++i) f[i] = 0.0f;
+#pragma unroll 1
+              for (int s = 0; s < seg.n_contrib; ++s) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                  const uint4 v = ld_shared_v4(region + s * kChunkSlotBytes + (q * 32 + lane) * 16);
+                  f[4 * q + 0] += __uint_as_float(v.x);
+                  f[4 * q + 1] += __uint_as_float(v.y);
+                  f[4 * q + 2] += __uint_as_float(v.z);
+                  f[4 * q + 3] += __uint_as_float(v.w);
+                }
+              }
+              if constexpr (kHasC) {
+                if (row_ok) {
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) {
+                    if (n0 + col + 8 * q < p.N) {
+                      const uint4 cv = ld_shared_v4(region + seg.n_contrib * kChunkSlotBytes + lane * 128 + q * 16);
+                      const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                      for (int e = 0; e < 4; ++e) {
+                        const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cw[e]));
+                        f[8 * q + 2 * e] = cf.x + f[8 * q + 2 * e];
+                        f[8 * q + 2 * e + 1] = cf.y + f[8 * q + 2 * e + 1];
+                      }
+                    }
+                  }
+                }
+              }
+              __syncwarp();   // all lanes have read the region before the next chunk's copies land
+              store_chunk(f, col, true);
+            }
+            if (lane == 0) *counter = 0;   // ready for the next launch
+            continue;
+          }
 #pragma unroll 1
           for (int ch = 0; ch < kChunks; ++ch) {
             const int col = col_part * C::kColsPerEpiWarp + ch * 64;

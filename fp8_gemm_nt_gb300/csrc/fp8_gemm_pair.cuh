@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dependency_wait();   // programmatic dependent launch: no global access before this
 
   auto on_timeout = [&]() {
     atomicOr(p.status, kStatusTimeoutBit);
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
         }
       }
     producer_done:
+      grid_launch_dependents();
       if (leader) {
         for (uint32_t s = 0; s < kStages && s < issued; ++s) {
           const uint32_t last_use = (issued - 1 - s) / kStages;

@@ -250,6 +250,21 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t saddr) {
   return v;
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only), and its completion wait.
+__device__ __forceinline__ void cp_async_16(uint32_t saddr, const void* gptr) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid in the stream (its memory
+// visible), and allow the next grid to be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"

@@ -1,8 +1,8 @@
 """The CTA-pair kernel (two SMs share one 256 x 256 tcgen05 MMA) against the oracle.
 
 Dense problems reach it in tile mode (at least as many 128 x 128 tiles as SMs used);
-the SM cap is lowered so that small problems qualify. Contiguous problems always use it
-(unless DG_PAIR=0)."""
+the SM cap is lowered so that small problems qualify. Contiguous problems use it when
+DG_PAIR=1 (their default is the single-CTA kernel)."""
 from __future__ import annotations
 
 import numpy as np
@@ -69,7 +69,8 @@ def test_pair_distinct_block_scales_exact(lib, few_sms):
     ([128, 0, 129, 255], 256, 384),
     ([1, 1, 1, 1, 1], 272, 256),
 ])
-def test_pair_contiguous(lib, counts, N, K):
+def test_pair_contiguous(lib, counts, N, K, monkeypatch):
+    monkeypatch.setenv("DG_PAIR", "1")
     p = W.make_contiguous(G=len(counts), tokens=sum(counts), N=N, K=K, seed=950 + N + K, counts=counts)
     d = run_contiguous(lib, p)
     ref, valid = O.m_grouped_fp8_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K, p.G)
@@ -90,3 +91,12 @@ def test_pair_timeout_path(lib, few_sms):
     ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, None, p.M, p.N, p.K)
     assert_parity(bf16_f64(run_dense(lib, p)), ref, "after pair timeout")
     assert lib.dg_get_device_status() == 0
+
+
+def test_pair_contiguous_bad_index_reported(lib, monkeypatch):
+    monkeypatch.setenv("DG_PAIR", "1")
+    p = W.make_contiguous(G=2, tokens=200, N=256, K=256, seed=2, counts=[100, 100])
+    p.m_indices[128:128 + 100] = 5          # out-of-range expert for the second segment
+    d = run_contiguous(lib, p)
+    assert lib.dg_get_device_status() == 6
+    assert (bf16_bits(d)[128:] == SENTINEL).all(), "rows of an invalid expert were written"

@@ -91,3 +91,16 @@ def test_stream_k_tile_widths(lib, sk_bn, M, N, K, monkeypatch):
     ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, M, N, K)
     assert_parity(bf16_f64(d), ref, f"stream-K bn={sk_bn}")
     assert lib.dg_get_device_status() == 0
+
+
+@pytest.mark.parametrize("kg", ["1", "2"])
+@pytest.mark.parametrize("M,N,K", [(128, 1024, 1152), (100, 640, 2944), (128, 7168, 16384)])
+def test_stream_k_kgroups_per_stage(lib, kg, M, N, K, monkeypatch):
+    # one or two K-groups per pipeline stage; odd K-group counts leave a half-filled last stage
+    monkeypatch.setenv("DG_KG", kg)
+    p = W.make_dense(M, N, K, seed=800 + M + N + K, with_c=True)
+    d = run_dense(lib, p)
+    rows = np.arange(M) if M * N * K < 2 ** 31 else np.arange(0, M, 5)
+    ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, M, N, K, rows=rows)
+    assert_parity(bf16_f64(d)[rows], ref, f"stream-K kg={kg}")
+    assert lib.dg_get_device_status() == 0
