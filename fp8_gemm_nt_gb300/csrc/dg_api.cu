@@ -270,13 +270,15 @@ dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const 
 }
 constexpr int kEpilogueWarps = 4;
 
-// CTA-pair configuration: 256 x 256 tiles over two SMs, 5-stage ring per CTA.
+// CTA-pair configurations: 256 x BN tiles over two SMs, 5-stage ring per CTA; BN = 256
+// with one accumulator, BN = 240 or 192 with two.
 constexpr int kPairStages = 5;
 
-template <dg::Kind kKind, bool kHasC>
+template <dg::Kind kKind, bool kHasC, int kBN>
 struct PairLauncher {
-  using Cfg = dg::PairConfig<kPairStages>;
-  static constexpr auto kernel() { return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kHasC>; }
+  static constexpr int kNumAccum = kBN == 256 ? 1 : 2;
+  using Cfg = dg::PairConfig<kPairStages, kBN, kNumAccum>;
+  static constexpr auto kernel() { return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kBN, kNumAccum, kHasC>; }
 
   // Largest number of co-resident CTA pairs (0 if the device cannot run the kernel).
   static int max_clusters() {
@@ -308,8 +310,8 @@ struct PairLauncher {
   }
 
   static dg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                          const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int clusters,
-                          cudaStream_t stream) {
+                          const CUtensorMap& tsb, const CUtensorMap& td, const CUtensorMap& td_tail,
+                          const dg::Params& p, int clusters, cudaStream_t stream) {
     auto kern = kernel();
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -325,11 +327,12 @@ struct PairLauncher {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, td_tail, p);
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
-      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d pair 256x256 stages=%d clusters=%d smem=%d\n",
-                   static_cast<int>(kKind), p.M, p.N, p.K, p.G, kPairStages, clusters, Cfg::SMEM_BYTES);
+      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d pair 256x%d accum=%d stages=%d clusters=%d smem=%d\n",
+                   static_cast<int>(kKind), p.M, p.N, p.K, p.G, kBN, kNumAccum, kPairStages, clusters,
+                   Cfg::SMEM_BYTES);
     return DG_OK;
   }
 };
@@ -411,16 +414,17 @@ bool map_out(CUtensorMap* m, void* base, int G, int rows, int N) {
 
 // Dense / contiguous GEMM on CTA pairs: converts the scale words into tcgen05.cp chunks in
 // the stream workspace (two small kernels), then launches the pair kernel.
-template <dg::Kind kKind, bool kHasC>
+template <dg::Kind kKind, bool kHasC, int kBN>
 dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d,
                    dg::Params p, int clusters, cudaStream_t stream) {
   const int KP = ceil_div(p.K / 128, 4);
   const int num_mb = ceil_div(p.M, 128);
   const int NB = ceil_div(p.N, 128);
+  const int sfb_rows = 2 * ceil_div(p.N, kBN);     // two chunks per tile
   const int G = kKind == dg::Kind::Dense ? 1 : p.G;
   const size_t sfa_words = static_cast<size_t>(KP) * num_mb * 128;
-  const size_t sfb_words = static_cast<size_t>(G) * KP * NB * 128;
-  if (static_cast<size_t>(KP) * num_mb > (1u << 30) || static_cast<size_t>(G) * KP * NB > (1u << 30))
+  const size_t sfb_words = static_cast<size_t>(G) * KP * sfb_rows * 128;
+  if (static_cast<size_t>(KP) * num_mb > (1u << 30) || static_cast<size_t>(G) * KP * sfb_rows > (1u << 30))
     return DG_ERR_UNSUPPORTED;
   void* ws = nullptr;
   if (dg_status s = stream_workspace(ds, stream, kSkCounterInts * 4 + (sfa_words + sfb_words) * 4, &ws); s != DG_OK)
@@ -429,19 +433,31 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   int32_t* sfb_t = sfa_t + sfa_words;
   auto blocks_for = [](size_t n) { return static_cast<unsigned>(std::min<size_t>((n + 255) / 256, 2048)); };
   dg::sf_to_utccp_kernel<<<blocks_for(sfa_words), 256, 0, stream>>>(sfa, sfa_t, 1, KP, p.M, ceil4(p.M), num_mb, 0);
-  dg::sf_to_utccp_kernel<<<blocks_for(sfb_words), 256, 0, stream>>>(sfb, sfb_t, G, KP, NB, ceil4(NB), NB, 1);
+  dg::sf_to_utccp_kernel<<<blocks_for(sfb_words), 256, 0, stream>>>(sfb, sfb_t, G, KP, p.N, ceil4(NB), sfb_rows,
+                                                                       kBN);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
 
-  CUtensorMap ta, tb, tsa, tsb, td;
+  CUtensorMap ta, tb, tsa, tsb, td, td_tail;
   bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) && map_out(&td, d, 0, p.M, p.N);
+  if constexpr (kBN % 64 != 0) {
+    // the narrower last chunk of each tile: kBN % 64 columns x 32 rows, no swizzle
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(p.N) * 2};
+    const uint32_t box[2] = {static_cast<uint32_t>(kBN % 64), 32};
+    ok = ok && make_map(&td_tail, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    td_tail = td;
+  }
+  // each CTA of the pair loads BN/2 rows of the B tile
   if (kKind == dg::Kind::Dense)
-    ok = ok && map_operand_2d(&tb, b, p.N, p.K, 128);
+    ok = ok && map_operand_2d(&tb, b, p.N, p.K, kBN / 2);
   else
-    ok = ok && map_operand_3d(&tb, b, G, p.N, p.K, 128);
+    ok = ok && map_operand_3d(&tb, b, G, p.N, p.K, kBN / 2);
   {
     const uint64_t dims_a[2] = {128, static_cast<uint64_t>(KP) * num_mb};
-    const uint64_t dims_b[2] = {128, static_cast<uint64_t>(G) * KP * NB};
+    const uint64_t dims_b[2] = {128, static_cast<uint64_t>(G) * KP * sfb_rows};
     const uint64_t strides[1] = {512};
     const uint32_t box_a[2] = {128, 1}, box_b[2] = {128, 2};
     ok = ok && make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa_t, dims_a, strides, box_a, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -449,8 +465,70 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   }
   if (!ok) return DG_ERR_CUDA;
   p.sf_num_mb = num_mb;
-  p.sf_nb = NB;
-  return PairLauncher<kKind, kHasC>::launch(ta, tb, tsa, tsb, td, p, clusters, stream);
+  p.sf_nb = sfb_rows;
+  return PairLauncher<kKind, kHasC, kBN>::launch(ta, tb, tsa, tsb, td, td_tail, p, clusters, stream);
+}
+
+// Pair tile width: DG_PAIR_BN (192, 240 or 256) overrides; 240 is offered for the dense
+// form only. Otherwise the width with the smallest estimated makespan: waves of pair tiles
+// x cycles per tile, from measurements on GB300 -- a K-group costs ~512 cycles at 256
+// columns (tensor-bound) and ~500 at 240 or 192 (bound by the issuing loop: ~125 cycles
+// per MMA with one barrier wait per K-group), and a single accumulator adds ~2300 cycles
+// per tile (the MMAs wait for the epilogue to drain it).
+int pick_pair_bn(long long pair_rows, int N, int K, int clusters, bool dense) {
+  if (const char* f = std::getenv("DG_PAIR_BN")) {
+    const int v = std::atoi(f);
+    if (v == 192 || v == 256 || (v == 240 && dense)) return v;
+  }
+  const long long kb = K / 128;
+  auto makespan = [&](int bn) {
+    const long long tiles = pair_rows * ceil_div(N, bn);
+    const long long waves = ceil_div(tiles, static_cast<long long>(std::max(clusters, 1)));
+    const long long per_tile = bn == 256 ? kb * 512 + 2300 : kb * 500;
+    return waves * per_tile;
+  };
+  int best = 256;
+  for (int bn : {240, 192}) {
+    if (bn == 240 && !dense) continue;
+    if (makespan(bn) < makespan(best)) best = bn;
+  }
+  return best;
+}
+
+// Launches the pair kernel for kKind if the device can run it; *launched tells whether it did.
+template <dg::Kind kKind>
+dg_status try_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                   const void* c, void* d, dg::Params pp, long long pair_rows, int sms, cudaStream_t stream,
+                   bool* launched) {
+  *launched = false;
+  if constexpr (kKind != dg::Kind::Dense) {
+    if (c) return DG_ERR_INVALID_ARG;   // only the dense form takes C
+  }
+  constexpr bool kDense = kKind == dg::Kind::Dense;
+  constexpr int kWideBN = kDense ? 240 : 192;     // the 240-wide configuration is dense-only
+  const bool with_c = kDense && c != nullptr;
+  const int max_cl = std::min({with_c ? PairLauncher<kKind, kDense, 256>::max_clusters()
+                                      : PairLauncher<kKind, false, 256>::max_clusters(),
+                               with_c ? PairLauncher<kKind, kDense, 192>::max_clusters()
+                                      : PairLauncher<kKind, false, 192>::max_clusters(),
+                               with_c ? PairLauncher<kKind, kDense, kWideBN>::max_clusters()
+                                      : PairLauncher<kKind, false, kWideBN>::max_clusters()});
+  if (max_cl <= 0) return DG_OK;
+  const int cl_cap = std::min(max_cl, sms / 2);
+  const int bn = pick_pair_bn(pair_rows, pp.N, pp.K, cl_cap, kDense);
+  const long long pair_tiles = pair_rows * ceil_div(pp.N, bn);
+  const int clusters = static_cast<int>(std::min<long long>(cl_cap, pair_tiles));
+  *launched = true;
+  if (bn == 240) {
+    if (with_c) return run_pair<kKind, kDense, kWideBN>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    return run_pair<kKind, false, kWideBN>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+  }
+  if (bn == 256) {
+    if (with_c) return run_pair<kKind, kDense, 256>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    return run_pair<kKind, false, 256>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+  }
+  if (with_c) return run_pair<kKind, kDense, 192>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+  return run_pair<kKind, false, 192>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
 }
 
 dg_status check_common(int N, int K) {
@@ -529,9 +607,7 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   }
   const int BN = tiles128 < sms ? sk_bn : pick_bn(dg::Kind::Dense, N);
   if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
-    const int max_cl = c ? PairLauncher<dg::Kind::Dense, true>::max_clusters()
-                         : PairLauncher<dg::Kind::Dense, false>::max_clusters();
-    if (max_cl > 0) {
+    {
       dg::Params pp{};
       pp.M = M;
       pp.N = N;
@@ -542,10 +618,10 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
       pp.status = ds->status;
       pp.timeout_ns = wait_timeout_ns();
       pp.fault = g_fault.load();
-      const long long pair_tiles = static_cast<long long>(ceil_div(M, 256)) * ceil_div(N, 256);
-      const int clusters = static_cast<int>(std::min<long long>(std::min(max_cl, sms / 2), pair_tiles));
-      if (c) return run_pair<dg::Kind::Dense, true>(*ds, a, sfa, b, sfb, d, pp, clusters, stream);
-      return run_pair<dg::Kind::Dense, false>(*ds, a, sfa, b, sfb, d, pp, clusters, stream);
+      bool launched = false;
+      const dg_status s = try_pair<dg::Kind::Dense>(*ds, a, sfa, b, sfb, c, d, pp, ceil_div(M, 256), sms, stream,
+                                                    &launched);
+      if (launched) return s;
     }
   }
   if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||
@@ -619,8 +695,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   // selects the pair kernel.
   const char* pair_env = std::getenv("DG_PAIR");
   if (pair_env && pair_env[0] == '1' && !std::getenv("DG_FORCE_BN")) {
-    const int max_cl = PairLauncher<dg::Kind::Contiguous, false>::max_clusters();
-    if (max_cl > 0) {
+    {
       dg::Params pp{};
       pp.M = M_total;
       pp.N = N;
@@ -632,10 +707,10 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
       pp.timeout_ns = wait_timeout_ns();
       pp.fault = g_fault.load();
       // the number of pair rows depends on m_indices (device): bound it by the block count
-      const long long pair_tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, 256);
-      const int clusters =
-          static_cast<int>(std::min<long long>(std::min(max_cl, sms_to_use(*ds) / 2), pair_tiles));
-      return run_pair<dg::Kind::Contiguous, false>(*ds, a, sfa, b, sfb, d, pp, clusters, stream);
+      bool launched = false;
+      const dg_status s = try_pair<dg::Kind::Contiguous>(*ds, a, sfa, b, sfb, nullptr, d, pp, ceil_div(M_total, 128),
+                                                         sms_to_use(*ds), stream, &launched);
+      if (launched) return s;
     }
   }
   const int KP = ceil_div(K / 128, 4);

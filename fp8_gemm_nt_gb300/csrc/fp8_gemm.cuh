@@ -68,7 +68,7 @@ struct Params {
   int fault;                      // kFault*
   // CTA-pair kernel: row counts of the tcgen05.cp-layout scale chunk tensors
   int sf_num_mb;                  // 128-row blocks of A per K-quad
-  int sf_nb;                      // 128-row blocks of B per (group, K-quad)
+  int sf_nb;                      // B chunk rows per (group, K-quad): two per tile
 };
 
 __host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) / b; }

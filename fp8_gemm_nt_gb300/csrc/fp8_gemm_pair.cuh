@@ -1,23 +1,33 @@
 // CTA-pair variant of the fine-grained-scaled FP8 GEMM for sm_103a: two CTAs of a
-// cluster share one tcgen05.mma.cta_group::2 of shape 256 x 256 (x 32).
+// cluster share one tcgen05.mma.cta_group::2 of shape 256 x BN (x 32): BN = 256 with one
+// accumulator, or BN = 240 / 192 with two (two 256-column accumulators would leave no TMEM
+// columns for the scale factors; 240 columns leave 16 beside each accumulator).
 //
-// Each CTA of the pair holds 128 rows of A and 128 of the 256 rows of the B tile in its
-// own shared memory; the pair's MMA reads both and each CTA's TMEM receives its 128 x 256
+// Each CTA of the pair holds 128 rows of A and BN/2 of the BN rows of the B tile in its
+// own shared memory; the pair's MMA reads both and each CTA's TMEM receives its 128 x BN
 // block of the accumulator. Per SM this halves the B bytes loaded and stored in shared
-// memory per FLOP compared with a 128 x 256 tile on one SM, which is what bounds the
-// single-CTA kernel on GB300 (L2->SM traffic and bytes in flight).
+// memory per FLOP compared with a 128 x BN tile on one SM, which is what bounds the
+// single-CTA kernel on GB300 (L2->SM traffic and bytes in flight). With two accumulators
+// the MMAs of the next tile run while the epilogue drains the previous one.
 //
 // Roles (both CTAs run the same code):
 //   warp 0      TMA producer: its own A rows, its own half of B and the scale chunks,
 //               counted on the full barrier of the leader CTA (rank 0).
-//   warp 1      allocates TMEM for the pair; in the leader one thread copies the scale
-//               chunks into TMEM (tcgen05.cp.cta_group::2) and issues the MMAs, then
-//               commits to the empty / accumulator-full barriers of both CTAs.
-//   warps 2..9  epilogue: each reads its 32 TMEM lanes x 128 columns into registers,
-//               hands the accumulator back to the leader, then adds C, rounds to BF16 and
-//               TMA-stores (or stores valid rows only).
+//   warp 1      allocates TMEM for the pair; in the leader one thread issues the MMAs
+//               (one ready-barrier wait and four MMAs per K-group) and commits to the
+//               empty / accumulator-full barriers of both CTAs.
+//   warps 2..   epilogue, BN/64 x 4 warps' worth of 64-column chunks: each warp reads its
+//               32 TMEM lanes of its chunks into registers, hands the accumulator back to
+//               the leader, then adds C, rounds to BF16 and TMA-stores (or stores valid
+//               rows only).
+//   last warp   (leader) hands each stage to the MMA thread: waits for its operands and,
+//               on a stage that carries scale chunks, copies them into TMEM
+//               (tcgen05.cp.cta_group::2) and signals through tcgen05.commit. Keeping the
+//               copies and the TMA-barrier waits off the issuing thread keeps its MMA stream
+//               dense (an issuing thread's own shared-memory accesses stall it).
 // The scale words are consumed in the tcgen05.cp source layout, produced beforehand in a
-// workspace by sf_to_utccp_kernel (one 512-byte chunk per 128 rows per 4 K-groups).
+// workspace by sf_to_utccp_kernel: one 512-byte chunk per 128 rows of A per 4 K-groups,
+// and two per BN-wide tile of B per 4 K-groups (tile columns 0..127 and 128..255).
 // Operation: D = C + A @ B.T (DeepGEMM README "Interfaces / Notices", "Normal dense GEMMs",
 // "Grouped GEMMs (contiguous layout)", as reproduced on the page "Weight gradient kernels
 // for dense and MoE models #95").
@@ -27,11 +37,17 @@
 
 namespace dg {
 
-template <int kStages>
+template <int kStages, int kBN, int kNumAccum>
 struct PairConfig {
-  static constexpr int BN = 256;                 // tile width of the pair; each CTA loads BN/2 B rows
-  static constexpr int kEpiWarps = 8;            // two per TMEM sub-partition, 128 columns each
-  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int BN = kBN;                 // tile width of the pair; each CTA loads BN/2 B rows
+  static_assert(BN % 16 == 0 && BN >= 128 && BN <= 256, "tile width: a multiple of 16 in [128, 256]");
+  static constexpr int kChunks = ceil_div_c(BN, 64);   // epilogue chunks of 64 columns (last may be narrower)
+  static constexpr int kTail = BN % 64;                // width of a narrower last chunk (0: none)
+  static constexpr int kWarpsPerQuad = kChunks % 2 == 0 ? 2 : kChunks;
+  static constexpr int kChunksPerWarp = kChunks / kWarpsPerQuad;
+  static constexpr int kEpiWarps = 4 * kWarpsPerQuad;
+  static constexpr int kReadyWarp = 2 + kEpiWarps;
+  static constexpr int kThreads = (3 + kEpiWarps) * 32;
   static constexpr int A_BYTES = BLOCK_M * BLOCK_K;
   static constexpr int B_BYTES = (BN / 2) * BLOCK_K;
   static constexpr int SFA_BYTES = 512;          // one tcgen05.cp chunk: this CTA's 128 rows
@@ -43,23 +59,31 @@ struct PairConfig {
   static constexpr int OFF_SF = OFF_B + kStages * B_BYTES;
   static constexpr int OFF_EPI = ((OFF_SF + kStages * SF_STRIDE + 1023) / 1024) * 1024;
   static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_BUF_BYTES;
-  static constexpr int NUM_BARS = 2 * kStages + 3;
+  // full / empty / ready per stage, tfull / tempty per accumulator, MMA drain, copy drain,
+  // one "scale buffer free" barrier per TMEM scale buffer
+  static constexpr int NUM_BARS = 3 * kStages + 2 * kNumAccum + 4;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
   static constexpr int TX_AB = 2 * (A_BYTES + B_BYTES);           // both CTAs, every stage
   static constexpr int TX_SF = 2 * (SFA_BYTES + SFB_BYTES);       // both CTAs, every 4th stage
-  // TMEM: one 256-column accumulator, then 2 x 4 SFA columns and 2 x 8 SFB columns
-  static constexpr int SFA_COL = BN;
-  static constexpr int SFB_COL = BN + 8;
+  // TMEM: kNumAccum BN-column accumulators and 2 x 4 SFA / 2 x 8 SFB columns, packed when
+  // they fit; otherwise (two 240-column accumulators) the accumulators start at columns 0
+  // and 256 and the scale columns sit in the 16 columns after each
+  static constexpr bool kPacked = kNumAccum * BN + 24 <= 512;
+  static constexpr int ACC_STRIDE = kPacked ? BN : 256;
+  static constexpr int SFA_COL = kPacked ? kNumAccum * BN : BN;
+  static constexpr int SFB_COL = kPacked ? SFA_COL + 8 : 256 + BN;
   static constexpr int TMEM_COLS = 512;
+  static_assert(kPacked || (kNumAccum == 2 && BN + 8 <= 256 && 256 + BN + 16 <= TMEM_COLS), "TMEM layout");
+  static_assert(!kPacked || SFB_COL + 16 <= TMEM_COLS, "TMEM columns exceeded");
 };
 
 // Walks the pair tiles of the sequence t = cluster, += clusters. A pair row is two
 // consecutive 128-row blocks; in the contiguous form both blocks belong to one expert
 // (an expert with an odd number of blocks ends with a pair whose second block is not its
 // own: that CTA's rows are computed and discarded).
-template <Kind kKind>
+template <Kind kKind, int kBN>
 struct PairScheduler {
   int num_n, num_mb, total;
   int t, step;
@@ -76,7 +100,7 @@ struct PairScheduler {
   }
 
   __device__ __forceinline__ PairScheduler(const Params& p, int cluster, int clusters) {
-    num_n = ceil_div_c(p.N, PairConfig<1>::BN);
+    num_n = ceil_div_c(p.N, kBN);
     num_mb = ceil_div_c(p.M, BLOCK_M);
     t = cluster;
     step = clusters;
@@ -141,22 +165,27 @@ struct PairScheduler {
   }
 };
 
-template <Kind kKind, int kStages, bool kHasC>
-__global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
+template <Kind kKind, int kStages, int kBN, int kNumAccum, bool kHasC>
+__global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
-                         const __grid_constant__ CUtensorMap tm_d, const Params p) {
+                         const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_d_tail,
+                         const Params p) {
   static_assert(kKind != Kind::Masked, "the masked form uses the single-CTA kernel");
-  using C = PairConfig<kStages>;
+  static_assert(kKind == Kind::Dense || kBN % 64 == 0, "narrow last chunks: dense form only");
+  using C = PairConfig<kStages, kBN, kNumAccum>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full_bar = bars;                    // used in the leader only
   uint64_t* empty_bar = bars + kStages;         // both CTAs (leader's commit, multicast)
-  uint64_t* tfull_bar = bars + 2 * kStages;     // both CTAs (leader's commit, multicast)
-  uint64_t* tempty_bar = bars + 2 * kStages + 1;  // leader: 8 epilogue warps x 2 CTAs
-  uint64_t* drain_bar = bars + 2 * kStages + 2;
+  uint64_t* tfull_bar = bars + 2 * kStages;     // [kNumAccum] both CTAs (leader's commit, multicast)
+  uint64_t* tempty_bar = tfull_bar + kNumAccum;  // [kNumAccum] leader: epilogue warps of both CTAs
+  uint64_t* drain_bar = tempty_bar + kNumAccum;
+  uint64_t* ready_bar = drain_bar + 1;          // [kStages] leader: stage handed to the MMA thread
+  uint64_t* sf_drain_bar = ready_bar + kStages;
+  uint64_t* sf_free_bar = sf_drain_bar + 1;     // [2] leader: MMAs reading TMEM scale buffer b completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -172,9 +201,15 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, 2 * C::kEpiWarps);
+    for (int i = 0; i < kNumAccum; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], 2 * C::kEpiWarps);
+    }
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&ready_bar[s], 1);
+    mbar_init(sf_drain_bar, 1);
+    mbar_init(&sf_free_bar[0], 1);
+    mbar_init(&sf_free_bar[1], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -201,7 +236,7 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
     *abort_flag = 1;
   };
 
-  PairScheduler<kKind> sched(p, static_cast<int>(blockIdx.x / 2), static_cast<int>(gridDim.x / 2));
+  PairScheduler<kKind, kBN> sched(p, static_cast<int>(blockIdx.x / 2), static_cast<int>(gridDim.x / 2));
   Segment seg;
 
   if (warp == 0) {
@@ -232,8 +267,7 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
             const int q = kb / 4;
             // SFA chunk row: (q, m_blk); SFB chunk rows: (g, q, n-block) and the next one
             tma_load_2d_pair(ssf, &tm_sfa, fb, 0, q * p.sf_num_mb + m_blk);
-            tma_load_2d_pair(ssf + C::SFA_BYTES, &tm_sfb, fb, 0,
-                             (seg.g * KP + q) * p.sf_nb + n0 / SF_BLOCK_N);
+            tma_load_2d_pair(ssf + C::SFA_BYTES, &tm_sfb, fb, 0, (seg.g * KP + q) * p.sf_nb + 2 * seg.n_blk);
           }
           ++issued;
           if (++stage == kStages) {
@@ -258,38 +292,38 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
       constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(2 * BLOCK_M, C::BN);
       const uint64_t a_desc0 = make_smem_desc(smem_addr(smem + C::OFF_A), 16, 1024, kLayoutSwizzle128B);
       const uint64_t b_desc0 = make_smem_desc(smem_addr(smem + C::OFF_B), 16, 1024, kLayoutSwizzle128B);
-      const uint64_t sf_desc0 = make_smem_desc(smem_addr(smem + C::OFF_SF), 0, 128, kLayoutNone);
       uint32_t stage = 0, phase = 0, tile_iter = 0, sf_iter = 0;
       while (sched.next(p, seg)) {
-        if (*abort_flag || !mbar_wait(tempty_bar, (tile_iter & 1) ^ 1, p.timeout_ns)) {
+        const uint32_t acc = tile_iter % kNumAccum;
+        if (*abort_flag || !mbar_wait(&tempty_bar[acc], ((tile_iter / kNumAccum) & 1) ^ 1, p.timeout_ns)) {
           on_timeout();
           goto mma_done;
         }
         tc_fence_after();
         {
+          const uint32_t d_tmem = tmem_base + acc * C::ACC_STRIDE;
           uint32_t sfa_tmem = 0, sfb_tmem = 0;
           for (int kb = 0; kb < num_kb; ++kb) {
-            if (!mbar_wait(&full_bar[stage], phase, p.timeout_ns)) {
+            if (!mbar_wait(&ready_bar[stage], phase, p.timeout_ns)) {
               on_timeout();
               goto mma_done;
             }
             tc_fence_after();
             if (kb % 4 == 0) {
+              // the scales of this K-quad are in TMEM buffer (sf_iter & 1); the other
+              // buffer's readers are all issued: it may be refilled once they complete
+              if (sf_iter > 0) tc_commit_pair(&sf_free_bar[(sf_iter - 1) & 1]);
               const uint32_t buf = sf_iter & 1;
               ++sf_iter;
               sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
               sfb_tmem = tmem_base + C::SFB_COL + 8 * buf;
-              const uint64_t sf_desc = sf_desc0 + ((stage * C::SF_STRIDE) >> 4);
-              tmem_copy_32x128b_warpx4_pair(sfa_tmem, sf_desc);
-              tmem_copy_32x128b_warpx4_pair(sfb_tmem, sf_desc + (C::SFA_BYTES >> 4));
-              tmem_copy_32x128b_warpx4_pair(sfb_tmem + 4, sf_desc + ((C::SFA_BYTES + 512) >> 4));
             }
             const uint64_t adesc = a_desc0 + ((stage * C::A_BYTES) >> 4);
             const uint64_t bdesc = b_desc0 + ((stage * C::B_BYTES) >> 4);
             const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
 #pragma unroll
             for (int k = 0; k < BLOCK_K / 32; ++k)
-              mma_mxf8_block_scale_pair(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
+              mma_mxf8_block_scale_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
                                         (kb | k) != 0);
             tc_commit_pair(&empty_bar[stage]);
             if (++stage == kStages) {
@@ -298,7 +332,7 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
             }
           }
         }
-        tc_commit_pair(tfull_bar);
+        tc_commit_pair(&tfull_bar[acc]);
         ++tile_iter;
       }
     mma_done:
@@ -306,33 +340,95 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
       mbar_wait(drain_bar, 0, 50000000ull);
     }
     __syncwarp();
+  } else if (warp == C::kReadyWarp) {
+    // ================================ stage hand-off (leader) =======================
+    // Walks the stages in the MMA thread's order. A TMEM scale buffer is refilled only
+    // after the MMAs reading its previous contents completed (use k waits for phase k - 1
+    // of its free barrier; phase k needs this very copy, so the parity cannot alias).
+    if (leader && lane == 0) {
+      const uint64_t sf_desc0 = make_smem_desc(smem_addr(smem + C::OFF_SF), 0, 128, kLayoutNone);
+      uint32_t stage = 0, phase = 0, sf_iter = 0;
+      while (sched.next(p, seg)) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (*abort_flag || !mbar_wait(&full_bar[stage], phase, p.timeout_ns)) {
+            on_timeout();
+            goto ready_done;
+          }
+          if (kb % 4 == 0) {
+            if (sf_iter >= 2 && !mbar_wait(&sf_free_bar[sf_iter & 1], ((sf_iter >> 1) - 1) & 1, p.timeout_ns)) {
+              on_timeout();
+              goto ready_done;
+            }
+            tc_fence_after();
+            const uint32_t buf = sf_iter & 1;
+            ++sf_iter;
+            const uint32_t sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
+            const uint32_t sfb_tmem = tmem_base + C::SFB_COL + 8 * buf;
+            const uint64_t sf_desc = sf_desc0 + ((stage * C::SF_STRIDE) >> 4);
+            tmem_copy_32x128b_warpx4_pair(sfa_tmem, sf_desc);
+            tmem_copy_32x128b_warpx4_pair(sfb_tmem, sf_desc + (C::SFA_BYTES >> 4));
+            tmem_copy_32x128b_warpx4_pair(sfb_tmem + 4, sf_desc + ((C::SFA_BYTES + 512) >> 4));
+            tc_commit_pair(&ready_bar[stage]);
+          } else {
+            mbar_arrive(&ready_bar[stage]);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    ready_done:
+      // no copy of this thread may still be running when TMEM is released
+      tc_commit_pair(sf_drain_bar);
+      mbar_wait(sf_drain_bar, 0, 50000000ull);
+    }
+    __syncwarp();
   } else {
     // ================================ epilogue (both CTAs) ==========================
     const int ew = warp - 2;
     const int quad = warp % 4;
-    const int half = ew / 4;                       // columns [128 * half, 128 * half + 128)
+    const int wq = ew / 4;                         // chunks [wq * kChunksPerWarp, (wq + 1) * kChunksPerWarp)
+    constexpr int kCols = 64 * C::kChunksPerWarp;   // this warp's columns (the last warp may use fewer)
+    const int col0 = kCols * wq;                     // first tile column of this warp
     uint8_t* sbuf = smem + C::OFF_EPI + ew * C::EPI_BUF_BYTES;
-    const uint32_t tempty_leader = map_to_rank(tempty_bar, 0);
     uint32_t tile_iter = 0;
     while (sched.next(p, seg)) {
-      if (!warp_wait(tfull_bar, tile_iter & 1, p.timeout_ns, abort_flag)) {
+      const uint32_t acc = tile_iter % kNumAccum;
+      if (!warp_wait(&tfull_bar[acc], (tile_iter / kNumAccum) & 1, p.timeout_ns, abort_flag)) {
         if (lane == 0) on_timeout();
         break;
       }
       ++tile_iter;
       tc_fence_after();
-      // the whole share of the accumulator into registers, then hand TMEM back at once
-      uint32_t v[128];
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + 128 * half;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::ACC_STRIDE + col0;
+      // One accumulator: the warp's whole share into registers, then TMEM handed back at
+      // once (the next tile's MMAs wait for it). Two accumulators: a chunk at a time, TMEM
+      // handed back after the last chunk is loaded.
+      constexpr int kHeld = kNumAccum == 1 ? kCols : 64;
+      uint32_t v[kHeld];
+      auto load_chunk = [&](int ch, uint32_t* dst) {
+        const int col = col0 + 64 * ch;
+        if (C::kTail == 0 || col + 64 <= C::BN) {
+          tmem_load_32x32b_x32(taddr + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(dst));
+          tmem_load_32x32b_x32(taddr + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(dst + 32));
+        } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t (&vj)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32 * j]);
-        tmem_load_32x32b_x32(taddr + 32 * j, vj);
+          for (int j = 0; j < C::kTail / 16; ++j) tmem_load_32x32b_x16(taddr + 64 * ch + 16 * j, dst + 16 * j);
+        }
+      };
+      auto release = [&]() {
+        tmem_load_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(map_to_rank(&tempty_bar[acc], 0));
+      };
+      if constexpr (kNumAccum == 1) {
+#pragma unroll
+        for (int ch = 0; ch < C::kChunksPerWarp; ++ch) load_chunk(ch, &v[64 * ch]);
+        release();
       }
-      tmem_load_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_leader);
 
       const int m_blk = seg.m_blk + static_cast<int>(rank);
       const int row = m_blk * BLOCK_M + quad * 32 + static_cast<int>(lane);
@@ -343,24 +439,38 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
         const int gi = row < p.M ? __ldg(p.m_indices + row) : -1;
         row_ok = gi == seg.g;
         // a row of the expert's own blocks that names another expert violates the layout
-        if (gi != seg.g && gi != -1 && static_cast<int>(rank) < seg.n_contrib && seg.n_blk == 0 && half == 0)
+        if (gi != seg.g && gi != -1 && static_cast<int>(rank) < seg.n_contrib && seg.n_blk == 0 && wq == 0)
           atomicOr(p.status, kStatusBadIndexBit);
       }
       const uint32_t ok_mask = __ballot_sync(0xffffffffu, row_ok);
       const long long d_row = row;
       const int n0 = seg.n_blk * C::BN;
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int col = 128 * half + 64 * ch;
+      for (int ch = 0; ch < C::kChunksPerWarp; ++ch) {
+        const int col = col0 + 64 * ch;
+        // 64 columns, or the narrower last chunk of a tile whose width is not a multiple of 64
+        const bool tail = C::kTail != 0 && col + 64 > C::BN;
+        const int units = tail ? C::kTail / 8 : 8;    // 8-column (16-byte) units of the chunk
+        const uint32_t* vc = &v[0];
+        if constexpr (kNumAccum == 1) {
+          vc = &v[64 * ch];
+        } else {
+          load_chunk(ch, v);
+          if (ch == C::kChunksPerWarp - 1) {
+            release();
+          } else {
+            tmem_load_wait();
+          }
+        }
         float f[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) f[i] = __uint_as_float(v[64 * ch + i]);
+        for (int i = 0; i < 64; ++i) f[i] = __uint_as_float(vc[i]);
         if constexpr (kHasC) {
           if (row_ok) {
             const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              if (n0 + col + 8 * q < p.N) {
+              if (q < units && n0 + col + 8 * q < p.N) {
                 const uint4 cv = ld_global_nc_v4(crow + 8 * q);
                 const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
@@ -375,22 +485,26 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
         }
         if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
-        const uint32_t srow = smem_addr(sbuf) + lane * 128;
+        // staging: 64-column chunks in the 128-byte-swizzled layout of tm_d; the narrower
+        // last chunk as plain rows of kTail * 2 bytes (tm_d_tail, no swizzle)
+        const uint32_t srow = smem_addr(sbuf) + lane * (tail ? C::kTail * 2 : 128);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          uint32_t w[4];
+          if (u < units) {
+            uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * u + 2 * e], f[8 * u + 2 * e + 1]);
-            w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * u + 2 * e], f[8 * u + 2 * e + 1]);
+              w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            st_shared_v4(srow + (tail ? u * 16 : (u ^ (lane & 7)) * 16), w[0], w[1], w[2], w[3]);
           }
-          st_shared_v4(srow + ((u ^ (lane & 7)) * 16), w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (kKind == Kind::Dense || ok_mask == 0xffffffffu) {
           if (lane == 0) {
-            tma_store_2d(&tm_d, sbuf, n0 + col, m_blk * BLOCK_M + quad * 32);
+            tma_store_2d(tail ? &tm_d_tail : &tm_d, sbuf, n0 + col, m_blk * BLOCK_M + quad * 32);
             bulk_commit_group();
           }
         } else if (ok_mask != 0) {
@@ -425,10 +539,12 @@ __global__ void __launch_bounds__(PairConfig<kStages>::kThreads, 1)
 
 // Scale words -> tcgen05.cp source chunks. For each (group, K-quad, 128-row block) a
 // 512-byte chunk whose row j (16 bytes) holds the words of rows j, j+32, j+64, j+96 of
-// the block. With `per_block` set the input holds one word per 128-row block (B scales)
-// and every row of the chunk repeats it.
+// the block. With `tile_bn` > 0 the input holds one word per 128-row block (B scales) and
+// the chunks follow BN-wide tiles instead: chunk 2t + c covers tile rows 128c..128c+127
+// of tile t (rows t*BN + 128c + ...), each row carrying the word of the block it falls in,
+// so that a tile may start inside a scale block.
 __global__ void sf_to_utccp_kernel(const int32_t* __restrict__ sf, int32_t* __restrict__ out, int groups, int kp,
-                                   int mn, int ld, int blocks, int per_block) {
+                                   int mn, int ld, int blocks, int tile_bn) {
   const long long total = static_cast<long long>(groups) * kp * blocks * 128;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -437,8 +553,9 @@ __global__ void sf_to_utccp_kernel(const int32_t* __restrict__ sf, int32_t* __re
     const int b = static_cast<int>(chunk % blocks);
     const long long gq = chunk / blocks;            // g * kp + q
     int32_t val = 0;
-    if (per_block) {
-      if (b < mn) val = __ldg(sf + gq * ld + b);
+    if (tile_bn > 0) {
+      const int row = (b / 2) * tile_bn + (b % 2) * 128 + 32 * (w % 4) + w / 4;
+      if (row < mn) val = __ldg(sf + gq * ld + row / 128);
     } else {
       const int row = b * 128 + 32 * (w % 4) + w / 4;
       if (row < mn) val = __ldg(sf + gq * ld + row);
