@@ -210,16 +210,47 @@ inline int ceil4(int x) { return 4 * ceil_div(x, 4); }
 // Kernel configurations
 // ------------------------------------------------------------------------------------
 template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps_, int kEpiBufs, bool kHasC,
-          int kKG = 1>
+          int kKG = 1, int kSplit = 0>
 struct Launcher {
   static constexpr int kEpiWarps = kEpiWarps_;
-  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG>;
+  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>;
   static constexpr int kBN = BN;
+  static constexpr auto kernel() {
+    return dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG, kSplit>;
+  }
+
+  // Largest number of co-resident clusters of kSplit CTAs (0 if the kernel cannot run).
+  static int max_clusters() {
+    static thread_local int dev_cached = -1, value = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev == dev_cached) return value;
+    auto kern = kernel();
+    value = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kSplit > 0 ? kSplit : 1;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(kSplit > 0 ? kSplit : 1, 1, 1);
+      cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess) value = n;
+    }
+    cudaGetLastError();
+    dev_cached = dev;
+    return value;
+  }
 
   static dg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                           const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
                           cudaStream_t stream) {
-    auto kern = dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG>;
+    auto kern = kernel();
     static thread_local int attr_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -229,24 +260,86 @@ struct Launcher {
       attr_dev = dev;
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n_attr = 0;
+    if (kSplit > 0) {
+      attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+      attr[n_attr].val.clusterDim.x = kSplit;
+      attr[n_attr].val.clusterDim.y = 1;
+      attr[n_attr].val.clusterDim.z = 1;
+      ++n_attr;
+    }
+    if (pdl_enabled()) {
+      attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+      ++n_attr;
+    }
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = n_attr;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, p);
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
-      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d BN=%d stages=%d accum=%d epi_warps=%d grid=%d smem=%d stream_k=%d\n",
+      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d BN=%d stages=%d accum=%d epi_warps=%d grid=%d smem=%d stream_k=%d split=%d\n",
                    static_cast<int>(kKind), p.M, p.N, p.K, p.G, BN, kStages, kNumAccum, kEpiWarps, grid,
-                   Cfg::SMEM_BYTES, p.sk_ctas);
+                   Cfg::SMEM_BYTES, p.sk_ctas, kSplit);
     return DG_OK;
   }
 };
+
+// Split-K over CTA pairs (clusters of two) for problems with too few tiles to fill the GPU:
+// one 128 x BN tile per pair, each CTA half of K, two K-groups per 3-stage ring slot; the
+// partials are summed through distributed shared memory (no workspace, no atomics).
+constexpr int kSplitWays = 2;
+template <bool kHasC, int BN>
+using SplitLauncher = Launcher<dg::Kind::Dense, BN, 3, 1, 4, 1, kHasC, 2, kSplitWays>;
+
+template <bool kHasC>
+int split_max_clusters(int bn) {
+  switch (bn) {
+    case 64: return SplitLauncher<kHasC, 64>::max_clusters();
+    case 96: return SplitLauncher<kHasC, 96>::max_clusters();
+    case 128: return SplitLauncher<kHasC, 128>::max_clusters();
+  }
+  return 0;
+}
+
+template <bool kHasC>
+dg_status launch_split(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                       const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
+                       cudaStream_t stream) {
+  switch (bn) {
+    case 64: return SplitLauncher<kHasC, 64>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 96: return SplitLauncher<kHasC, 96>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 128: return SplitLauncher<kHasC, 128>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+  }
+  return DG_ERR_INVALID_ARG;
+}
+
+// Split-K tile width for a problem with fewer 128 x 128 tiles than SMs: the narrowest of
+// 64 / 96 / 128 whose tiles fit one per co-resident CTA pair, if that keeps at least 3/4
+// of the SMs busy and gives each CTA two or more K-groups; 0 = use stream-K instead.
+// DG_SPLIT=0 disables the split form, DG_SPLIT_BN forces a width (if it fits).
+int pick_split_bn(int M, int N, int K, int sms, bool with_c) {
+  if (const char* f = std::getenv("DG_SPLIT")) {
+    if (f[0] == '0') return 0;
+  }
+  int forced = 0;
+  if (const char* f = std::getenv("DG_SPLIT_BN")) forced = std::atoi(f);
+  if (K / 128 < 2 * kSplitWays) return 0;
+  const long long m_blocks = ceil_div(M, 128);
+  for (int bn : {64, 96, 128}) {
+    if (forced && bn != forced) continue;
+    const int max_cl = std::min(with_c ? split_max_clusters<true>(bn) : split_max_clusters<false>(bn),
+                                sms / kSplitWays);
+    const long long tiles = m_blocks * ceil_div(N, bn);
+    if (max_cl > 0 && tiles <= max_cl && tiles * kSplitWays * 4 >= 3LL * sms) return bn;
+  }
+  return 0;
+}
 
 // Tile configurations (BN = tile width). All use 128-row tiles and 4 epilogue warps.
 //   128: 5-stage ring, double-buffered accumulators (TMEM 2 x 128 columns)
@@ -622,6 +715,27 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
       const dg_status s = try_pair<dg::Kind::Dense>(*ds, a, sfa, b, sfb, c, d, pp, ceil_div(M, 256), sms, stream,
                                                     &launched);
       if (launched) return s;
+    }
+  }
+  if (tiles128 < sms) {
+    if (const int sbn = pick_split_bn(M, N, K, sms, c != nullptr); sbn > 0) {
+      if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, sbn) ||
+          !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
+          !map_out(&td, d, 0, M, N))
+        return DG_ERR_CUDA;
+      dg::Params p{};
+      p.M = M;
+      p.N = N;
+      p.K = K;
+      p.G = 1;
+      p.c = static_cast<const __nv_bfloat16*>(c);
+      p.d = static_cast<__nv_bfloat16*>(d);
+      p.status = ds->status;
+      p.timeout_ns = wait_timeout_ns();
+      p.fault = g_fault.load();
+      const int grid = static_cast<int>(static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, sbn)) * kSplitWays;
+      if (c) return launch_split<true>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
+      return launch_split<false>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
     }
   }
   if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||

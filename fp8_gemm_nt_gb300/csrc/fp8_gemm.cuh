@@ -77,7 +77,11 @@ __host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) 
 // each TMA round trip moves; on GB300 a single producer thread streams markedly more from
 // HBM with 64 KB stages than with 32 KB ones (measured 5.2 vs 4.1 TB/s in a TMA-only
 // probe with the decode shape's A and B boxes), which is what the HBM-bound shapes need.
-template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, int kKG = 1>
+//
+// kSplit > 0 (dense only): split-K over a cluster of kSplit CTAs. Each cluster computes one
+// tile, CTA r of the cluster K-groups [r, r+1) * K / kSplit of it; the FP32 partials meet
+// in shared memory and CTA r sums (in rank order) and stores columns [r, r+1) * BN / kSplit.
+template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, int kKG = 1, int kSplit = 0>
 struct Config {
   static_assert(kKG == 1 || kKG == 2, "one or two K-groups per stage");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
@@ -85,7 +89,9 @@ struct Config {
   static constexpr int kSfWarp = 2 + kEpiWarps;                 // rearranges the scale words
   static constexpr int kThreads = (3 + kEpiWarps) * 32;
   static constexpr int kColsPerEpiWarp = BN / (kEpiWarps / 4);
-  static_assert(kColsPerEpiWarp % 64 == 0, "each epilogue warp stores whole 64-column chunks");
+  static_assert(kSplit > 0 || kColsPerEpiWarp % 64 == 0, "each epilogue warp stores whole 64-column chunks");
+  static_assert(kSplit == 0 || (kEpiWarps == 4 && kNumAccum == 1 && (BN / kSplit) % 8 == 0),
+                "split-K: 4 epilogue warps, one accumulator, 8-column slices");
 
   // shared memory (offsets from a 1024-byte-aligned base)
   static constexpr int A_SUB = BLOCK_M * BLOCK_K;               // one K-group of A
@@ -123,6 +129,9 @@ struct Config {
   // float4 (c4, lane) at index c4 * 32 + lane (a warp's 32 lanes write 512 contiguous bytes)
   static constexpr int SK_TILE_FLOATS = BLOCK_M * BN;
   static constexpr int SK_WARP_FLOATS = 32 * kColsPerEpiWarp;
+  // split-K: this CTA's FP32 partial, float4 (c4, row) at byte (c4 * 128 + row) * 16, in the
+  // ring's shared memory (idle once the CTA's only tile is accumulated)
+  static_assert(kSplit == 0 || BN * BLOCK_M * 4 <= OFF_EPI - OFF_A, "split-K partial exceeds the ring");
 };
 
 // ------------------------------------------------------------------------------------
@@ -141,7 +150,7 @@ struct Segment {
   bool cta_last;  // stream-K: no further segment for this CTA (its ring smem is free afterwards)
 };
 
-template <Kind kKind, int BN, int kKG = 1>
+template <Kind kKind, int BN, int kKG = 1, int kSplit = 0>
 struct Scheduler {
   int num_n, num_m, total, num_kb, num_kc;   // num_kc: stream-K units (kKG K-groups) per tile
   int g_cur, g_start, g_tiles;   // masked: incremental walk over groups
@@ -165,6 +174,15 @@ struct Scheduler {
     t = blockIdx.x;
     stream_k = false;
     u = u_end = U = 0;
+    if constexpr (kSplit > 0) {
+      // one tile per cluster; this CTA takes its rank's share of the tile's K units
+      total = num_m * num_n;
+      t = static_cast<int>(blockIdx.x) / kSplit;
+      const int r = static_cast<int>(blockIdx.x) % kSplit;
+      u = static_cast<long long>(r) * num_kc / kSplit;
+      u_end = static_cast<long long>(r + 1) * num_kc / kSplit;
+      return;
+    }
     if constexpr (kKind == Kind::Masked) {
       total = 0;
       for (int g = 0; g < p.G; ++g) total += ceil_div_c(clamped_mask(p, g), BLOCK_M) * num_n;
@@ -196,6 +214,21 @@ struct Scheduler {
   // Next segment of this CTA; false when there is none left. Contiguous padding blocks
   // are skipped here (every role skips the same ones).
   __device__ __forceinline__ bool next(const Params& p, Segment& s) {
+    if constexpr (kSplit > 0) {
+      if (t >= total || u >= u_end) return false;
+      s.tile = t;
+      s.m_blk = t / num_n;
+      s.n_blk = t % num_n;
+      s.g = 0;
+      s.valid_m = p.M;
+      s.kb_begin = static_cast<int>(u) * kKG;
+      s.kb_end = static_cast<int>(u_end) * kKG < num_kb ? static_cast<int>(u_end) * kKG : num_kb;
+      s.n_contrib = kSplit;
+      s.slot = static_cast<int>(blockIdx.x) % kSplit;
+      s.cta_last = true;
+      t = total;   // a single segment
+      return true;
+    }
     if (stream_k) {
       if (u >= u_end) return false;
       const int tile = static_cast<int>(u / num_kc);
@@ -280,12 +313,14 @@ __device__ __forceinline__ float4 ld_global_cg_v4f(const float* p) {
   return v;
 }
 
-template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC, int kKG = 1>
-__global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG>::kThreads, 1)
+template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC, int kKG = 1,
+          int kSplit = 0>
+__global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_d, const Params p) {
-  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG>;
+  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>;
+  static_assert(kSplit == 0 || kKind == Kind::Dense, "split-K clusters: dense form only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -343,7 +378,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     *abort_flag = 1;
   };
 
-  Scheduler<kKind, BN, kKG> sched(p);
+  Scheduler<kKind, BN, kKG, kSplit> sched(p);
   Segment seg;
 
   if (warp == 0) {
@@ -530,6 +565,91 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     }
   sf_done:
     __syncwarp();
+  } else if (kSplit > 0 && warp >= 2 && warp < 2 + kEpiWarps) {
+    // ============================ split-K epilogue (cluster) ========================
+    // 1. this CTA's FP32 partial: TMEM -> its shared memory; 2. cluster barrier; 3. CTA r
+    // sums the partials of its column slice over the cluster's CTAs in rank order (reading
+    // the others' shared memory), adds C, rounds to BF16 and stores; the kernel's closing
+    // cluster barrier keeps every CTA's shared memory alive until all reads are done.
+    // Every thread of the cluster passes both barriers on every path (timeouts included).
+    if constexpr (kSplit > 0) {
+      const int quad = warp % 4;
+      const int row_in_tile = quad * 32 + static_cast<int>(lane);
+      const uint32_t part = smem_addr(smem + C::OFF_A);
+      bool ok = sched.next(p, seg);
+      if (ok) {
+        ok = warp_wait(&tfull_bar[0], 0, p.timeout_ns, abort_flag);
+        if (!ok && lane == 0) on_timeout();
+      }
+      if (ok) {
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t v[32];
+          tmem_load_32x32b_x32(taddr + 32 * ch, v);
+          tmem_load_wait();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(part + ((8 * ch + q) * BLOCK_M + row_in_tile) * 16, v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                         v[4 * q + 3]);
+        }
+        tc_fence_before();
+      }
+      __syncwarp();
+      cluster_sync();   // partials of every CTA of the cluster are in shared memory
+      if (ok && *abort_flag == 0) {
+        constexpr int kSliceCols = BN / kSplit;
+        const int rank = seg.slot;
+        const int row = seg.m_blk * BLOCK_M + row_in_tile;
+        const bool row_ok = row < p.M;
+        uint32_t src[kSplit];
+#pragma unroll
+        for (int r = 0; r < kSplit; ++r) src[r] = r == rank ? part : map_to_rank(smem + C::OFF_A, r);
+#pragma unroll 1
+        for (int c8 = 0; c8 < kSliceCols / 8; ++c8) {
+          const int col = rank * kSliceCols + 8 * c8;          // column within the tile
+          const int gcol = seg.n_blk * BN + col;
+          const uint32_t off0 = ((col / 4) * BLOCK_M + row_in_tile) * 16;
+          const uint32_t off1 = off0 + BLOCK_M * 16;           // the next float4 column group
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+#pragma unroll
+          for (int r = 0; r < kSplit; ++r) {
+            const uint4 a = r == rank ? ld_shared_v4(src[r] + off0) : ld_shared_cluster_v4(src[r] + off0);
+            const uint4 b = r == rank ? ld_shared_v4(src[r] + off1) : ld_shared_cluster_v4(src[r] + off1);
+            f[0] += __uint_as_float(a.x);
+            f[1] += __uint_as_float(a.y);
+            f[2] += __uint_as_float(a.z);
+            f[3] += __uint_as_float(a.w);
+            f[4] += __uint_as_float(b.x);
+            f[5] += __uint_as_float(b.y);
+            f[6] += __uint_as_float(b.z);
+            f[7] += __uint_as_float(b.w);
+          }
+          if (row_ok && gcol < p.N) {
+            if constexpr (kHasC) {
+              const uint4 cv = ld_global_nc_v4(p.c + static_cast<long long>(row) * p.N + gcol);
+              const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cw[e]));
+                f[2 * e] = cf.x + f[2 * e];
+                f[2 * e + 1] = cf.y + f[2 * e + 1];
+              }
+            }
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+              w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            st_global_v4(p.d + static_cast<long long>(row) * p.N + gcol, w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
   } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // ================================ epilogue ====================================
     const int ew = warp - 2;
@@ -790,6 +910,12 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     __syncwarp();
   }
 
+  if constexpr (kSplit > 0) {
+    // the epilogue warps passed the first cluster barrier above; everyone passes the last
+    __syncwarp();
+    if (!(warp >= 2 && warp < 2 + kEpiWarps)) cluster_sync();
+    cluster_sync();
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -23,6 +23,12 @@ def lib():
     return L
 
 
+@pytest.fixture(autouse=True)
+def _stream_k_only(monkeypatch):
+    # shapes that would take the split-K cluster path (tests/test_split_gpu.py) stay on stream-K here
+    monkeypatch.setenv("DG_SPLIT", "0")
+
+
 # shapes with fewer 128 x 128 tiles than SMs, so the K-groups are shared among CTAs
 SK_SHAPES = [
     (128, 1024, 8192, False),     # 8 tiles, 64 K-groups each: many contributors per tile
