@@ -576,7 +576,22 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
       const int quad = warp % 4;
       const int row_in_tile = quad * 32 + static_cast<int>(lane);
       const uint32_t part = smem_addr(smem + C::OFF_A);
+      constexpr int kSliceCols = BN / kSplit;          // output columns this CTA reduces and stores
+      constexpr int kUnits = kSliceCols / 8;           // 8-column (16-byte BF16) units of a row
       bool ok = sched.next(p, seg);
+      const int rank = seg.slot;
+      const int row = seg.m_blk * BLOCK_M + row_in_tile;
+      const bool row_ok = ok && row < p.M;
+      // C of this CTA's output slice, loaded while the MMAs run
+      uint4 cv[kHasC ? kUnits : 1];
+      if constexpr (kHasC) {
+#pragma unroll
+        for (int u = 0; u < kUnits; ++u) {
+          const int gcol = seg.n_blk * BN + rank * kSliceCols + 8 * u;
+          cv[u] = (row_ok && gcol < p.N) ? ld_global_nc_v4(p.c + static_cast<long long>(row) * p.N + gcol)
+                                         : make_uint4(0, 0, 0, 0);
+        }
+      }
       if (ok) {
         ok = warp_wait(&tfull_bar[0], 0, p.timeout_ns, abort_flag);
         if (!ok && lane == 0) on_timeout();
@@ -599,39 +614,41 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
       __syncwarp();
       cluster_sync();   // partials of every CTA of the cluster are in shared memory
       if (ok && *abort_flag == 0) {
-        constexpr int kSliceCols = BN / kSplit;
-        const int rank = seg.slot;
-        const int row = seg.m_blk * BLOCK_M + row_in_tile;
-        const bool row_ok = row < p.M;
         uint32_t src[kSplit];
 #pragma unroll
         for (int r = 0; r < kSplit; ++r) src[r] = r == rank ? part : map_to_rank(smem + C::OFF_A, r);
-#pragma unroll 1
-        for (int c8 = 0; c8 < kSliceCols / 8; ++c8) {
-          const int col = rank * kSliceCols + 8 * c8;          // column within the tile
-          const int gcol = seg.n_blk * BN + col;
-          const uint32_t off0 = ((col / 4) * BLOCK_M + row_in_tile) * 16;
-          const uint32_t off1 = off0 + BLOCK_M * 16;           // the next float4 column group
+        // all partial loads first (one round trip), then sums in rank order
+        uint4 pv[kSplit][kUnits][2];
+#pragma unroll
+        for (int r = 0; r < kSplit; ++r) {
+#pragma unroll
+          for (int u = 0; u < kUnits; ++u) {
+            const uint32_t off0 = (((rank * kSliceCols + 8 * u) / 4) * BLOCK_M + row_in_tile) * 16;
+            const uint32_t off1 = off0 + BLOCK_M * 16;   // the next float4 column group
+            pv[r][u][0] = r == rank ? ld_shared_v4(src[r] + off0) : ld_shared_cluster_v4(src[r] + off0);
+            pv[r][u][1] = r == rank ? ld_shared_v4(src[r] + off1) : ld_shared_cluster_v4(src[r] + off1);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnits; ++u) {
+          const int gcol = seg.n_blk * BN + rank * kSliceCols + 8 * u;
           float f[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) f[i] = 0.0f;
 #pragma unroll
           for (int r = 0; r < kSplit; ++r) {
-            const uint4 a = r == rank ? ld_shared_v4(src[r] + off0) : ld_shared_cluster_v4(src[r] + off0);
-            const uint4 b = r == rank ? ld_shared_v4(src[r] + off1) : ld_shared_cluster_v4(src[r] + off1);
-            f[0] += __uint_as_float(a.x);
-            f[1] += __uint_as_float(a.y);
-            f[2] += __uint_as_float(a.z);
-            f[3] += __uint_as_float(a.w);
-            f[4] += __uint_as_float(b.x);
-            f[5] += __uint_as_float(b.y);
-            f[6] += __uint_as_float(b.z);
-            f[7] += __uint_as_float(b.w);
+            f[0] += __uint_as_float(pv[r][u][0].x);
+            f[1] += __uint_as_float(pv[r][u][0].y);
+            f[2] += __uint_as_float(pv[r][u][0].z);
+            f[3] += __uint_as_float(pv[r][u][0].w);
+            f[4] += __uint_as_float(pv[r][u][1].x);
+            f[5] += __uint_as_float(pv[r][u][1].y);
+            f[6] += __uint_as_float(pv[r][u][1].z);
+            f[7] += __uint_as_float(pv[r][u][1].w);
           }
           if (row_ok && gcol < p.N) {
             if constexpr (kHasC) {
-              const uint4 cv = ld_global_nc_v4(p.c + static_cast<long long>(row) * p.N + gcol);
-              const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+              const uint32_t cw[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cw[e]));
