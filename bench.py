@@ -42,6 +42,12 @@ HEADLINE = "dense_decode_128x7168x16384_c"
 METRIC = "FP8 GEMM TFLOPS (device-timed) and % of GB300 dense FP8 tensor peak"
 L2_BYTES = 126 * 2 ** 20
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate ratio (4.5 / 2.25 PFLOP/s)
+# DRAM bytes (read + write) of one launch of the headline's kernel, from one ncu capture of that
+# kernel as it stands (profiles/fp8_gemm_kernel_dense_decode_128x7168x16384_splitk_pair.md);
+# to be re-taken whenever the kernel changes.
+HEADLINE_TRAFFIC = {"kernel": "fp8_gemm_kernel<0, 96, 3, 1, 4, 1, 1, 2, 2> (split-K over CTA pairs, BN 96, with C)",
+                    "bytes_per_launch": 121_444_096 + 3_465_472,
+                    "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch"}
 
 
 # --------------------------------------------------------------------------------------
@@ -424,8 +430,9 @@ def main():
         "fp8_peak_tflops": fp8_peak,
         "fp8_peak_source": f"{peaks['source']} bf16 burst {peaks['bf16']} TFLOPS x {FP8_OVER_BF16} (nominal FP8/BF16 ratio)",
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
-                     "kernel": "fp8_gemm_kernel (dense, with C)", "kernel_ms": kern_ms,
+                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": HEADLINE_TRAFFIC["bytes_per_launch"],
+                     "traffic_source": HEADLINE_TRAFFIC["source"],
+                     "kernel": HEADLINE_TRAFFIC["kernel"], "kernel_ms": kern_ms,
                      "kernel_ms_how": "graph-replay region / K (back-to-back launches)",
                      "algorithmic_bytes_per_launch": alg_bytes, "peak_source": f"{peaks['source']} copy bandwidth"},
         "e2e": e2e,
