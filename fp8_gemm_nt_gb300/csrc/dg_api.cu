@@ -524,12 +524,34 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
     return s;
   int32_t* sfa_t = static_cast<int32_t*>(ws) + kSkCounterInts;
   int32_t* sfb_t = sfa_t + sfa_words;
-  auto blocks_for = [](size_t n) { return static_cast<unsigned>(std::min<size_t>((n + 255) / 256, 2048)); };
-  dg::sf_to_utccp_kernel<<<blocks_for(sfa_words), 256, 0, stream>>>(sfa, sfa_t, 1, KP, p.M, ceil4(p.M), num_mb, 0);
-  dg::sf_to_utccp_kernel<<<blocks_for(sfb_words), 256, 0, stream>>>(sfb, sfb_t, G, KP, p.N, ceil4(NB), sfb_rows,
-                                                                       kBN);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    dg::SfPrepArgs pa{};
+    pa.sfa = sfa;
+    pa.sfa_out = sfa_t;
+    pa.a_rows = p.M;
+    pa.lda = ceil4(p.M);
+    pa.a_blocks = num_mb;
+    pa.sfb = sfb;
+    pa.sfb_out = sfb_t;
+    pa.groups = G;
+    pa.b_rows = p.N;
+    pa.ldb = ceil4(NB);
+    pa.b_chunks = sfb_rows;
+    pa.tile_bn = kBN;
+    pa.kp = KP;
+    const size_t words = sfa_words + sfb_words;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<size_t>((words + 255) / 256, 2048)), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, dg::sf_to_utccp_kernel, pa);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
 
   CUtensorMap ta, tb, tsa, tsb, td, td_tail;
   bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) && map_out(&td, d, 0, p.M, p.N);

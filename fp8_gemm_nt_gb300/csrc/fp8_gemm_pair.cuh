@@ -537,30 +537,49 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
   }
 }
 
-// Scale words -> tcgen05.cp source chunks. For each (group, K-quad, 128-row block) a
-// 512-byte chunk whose row j (16 bytes) holds the words of rows j, j+32, j+64, j+96 of
-// the block. With `tile_bn` > 0 the input holds one word per 128-row block (B scales) and
-// the chunks follow BN-wide tiles instead: chunk 2t + c covers tile rows 128c..128c+127
-// of tile t (rows t*BN + 128c + ...), each row carrying the word of the block it falls in,
-// so that a tile may start inside a scale block.
-__global__ void sf_to_utccp_kernel(const int32_t* __restrict__ sf, int32_t* __restrict__ out, int groups, int kp,
-                                   int mn, int ld, int blocks, int tile_bn) {
-  const long long total = static_cast<long long>(groups) * kp * blocks * 128;
+// Scale words -> tcgen05.cp source chunks, for A and B in one launch. For each (group,
+// K-quad, 128-row block of A) a 512-byte chunk whose row j (16 bytes) holds the words of rows
+// j, j+32, j+64, j+96 of the block. B holds one word per 128-row block; its chunks follow
+// BN-wide tiles instead: chunk 2t + c covers tile rows 128c..128c+127 of tile t (rows
+// t*BN + 128c + ...), each row carrying the word of the block it falls in, so that a tile
+// may start inside a scale block. Launched as a programmatic dependent of the previous
+// kernel in the stream (waits for it before reading or writing global memory).
+struct SfPrepArgs {
+  const int32_t* sfa;   // [KP][lda] words
+  int32_t* sfa_out;     // [KP][a_blocks][128]
+  int a_rows, lda, a_blocks;
+  const int32_t* sfb;   // [G][KP][ldb] words
+  int32_t* sfb_out;     // [G][KP][b_chunks][128]
+  int groups, b_rows, ldb, b_chunks, tile_bn;
+  int kp;
+};
+
+__global__ void sf_to_utccp_kernel(const SfPrepArgs a) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const long long na = static_cast<long long>(a.kp) * a.a_blocks * 128;
+  const long long total = na + static_cast<long long>(a.groups) * a.kp * a.b_chunks * 128;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int w = static_cast<int>(idx % 128);
-    const long long chunk = idx / 128;              // (g * kp + q) * blocks + b
-    const int b = static_cast<int>(chunk % blocks);
-    const long long gq = chunk / blocks;            // g * kp + q
     int32_t val = 0;
-    if (tile_bn > 0) {
-      const int row = (b / 2) * tile_bn + (b % 2) * 128 + 32 * (w % 4) + w / 4;
-      if (row < mn) val = __ldg(sf + gq * ld + row / 128);
-    } else {
+    if (idx < na) {
+      const int w = static_cast<int>(idx % 128);
+      const long long chunk = idx / 128;              // q * a_blocks + b
+      const int b = static_cast<int>(chunk % a.a_blocks);
+      const long long q = chunk / a.a_blocks;
       const int row = b * 128 + 32 * (w % 4) + w / 4;
-      if (row < mn) val = __ldg(sf + gq * ld + row);
+      if (row < a.a_rows) val = __ldg(a.sfa + q * a.lda + row);
+      a.sfa_out[idx] = val;
+    } else {
+      const long long j = idx - na;
+      const int w = static_cast<int>(j % 128);
+      const long long chunk = j / 128;                // (g * kp + q) * b_chunks + c
+      const int c = static_cast<int>(chunk % a.b_chunks);
+      const long long gq = chunk / a.b_chunks;
+      const int row = (c / 2) * a.tile_bn + (c % 2) * 128 + 32 * (w % 4) + w / 4;
+      if (row < a.b_rows) val = __ldg(a.sfb + gq * a.ldb + row / 128);
+      a.sfb_out[j] = val;
     }
-    out[idx] = val;
   }
 }
 
