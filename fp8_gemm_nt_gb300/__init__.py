@@ -41,6 +41,7 @@ SIGNATURES = [
     ("dg_status_string", ctypes.c_char_p, [_I]),
     ("dg_last_cuda_error", _I, []),
     ("dg_set_debug", _I, [_I, ctypes.c_ulonglong]),
+    ("dg_measure_fp8_mma_tflops", _I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     ("dg_fp8_gemm_nt_no_alloc", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
 ]
 
@@ -207,6 +208,15 @@ def dg_set_debug(fault_mode: int, wait_timeout_ns: int = 0) -> None:
     """Failure-detection test hook: fault_mode 1 makes later launches time out on purpose
     (their producer issues nothing); wait_timeout_ns bounds every pipeline wait (0 = 2 s)."""
     _check("dg_set_debug", load_library().dg_set_debug(fault_mode, wait_timeout_ns))
+
+
+def dg_measure_fp8_mma_tflops(iters_per_sm: int = 4096) -> tuple[float, float]:
+    """Measured FP8 tensor-core ceiling of the current device: (TFLOP/s, kernel ms) of an
+    MMA-only kernel (block-scaled 128 x 256 x 32 MMAs from shared memory on every SM)."""
+    tf, ms = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _check("dg_measure_fp8_mma_tflops",
+           load_library().dg_measure_fp8_mma_tflops(int(iters_per_sm), ctypes.byref(tf), ctypes.byref(ms)))
+    return tf.value, ms.value
 
 
 def dg_fp8_gemm_nt_no_alloc(a, sfa, b, sfb, c, d, status, stream=None) -> torch.Tensor:

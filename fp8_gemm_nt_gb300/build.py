@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdg.so")
-SOURCES = [os.path.join(CSRC, "dg_api.cu"), os.path.join(CSRC, "dg_no_alloc.cu")]
+SOURCES = [os.path.join(CSRC, "dg_api.cu"), os.path.join(CSRC, "dg_no_alloc.cu"), os.path.join(CSRC, "dg_diag.cu")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

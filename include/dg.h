@@ -192,6 +192,19 @@ int dg_last_cuda_error(void);
  */
 dg_status dg_set_debug(int fault_mode, unsigned long long wait_timeout_ns);
 
+/*
+ * Diagnostic (no counterpart on the pages): the measured FP8 tensor-core ceiling of the
+ * current device. Every SM runs one CTA that issues `iters_per_sm` x 4 block-scaled
+ * 128 x 256 x 32 MMAs (kind::mxf8f6f4, E4M3, UE8M0 scales, FP32 accumulation in TMEM)
+ * back to back from shared memory, with no other work; the grid is timed with CUDA events
+ * on the legacy default stream. Writes the rate in TFLOP/s to *tflops and the kernel time
+ * to *ms (ms may be NULL). Synchronous; allocates and frees a 4-byte status word.
+ * Returns DG_ERR_INVALID_ARG for iters_per_sm outside [1, 2^20] or a null tflops,
+ * DG_ERR_TIMEOUT if the kernel's bounded completion wait ran out, DG_ERR_CUDA otherwise
+ * on failure.
+ */
+dg_status dg_measure_fp8_mma_tflops(int iters_per_sm, double* tflops, double* ms);
+
 #ifdef __cplusplus
 }
 #endif
