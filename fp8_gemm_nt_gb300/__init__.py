@@ -30,6 +30,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 SIGNATURES = [
     ("dg_fp8_gemm_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("dg_wgrad_gemm_fp8_fp8_fp32_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_pack_sf_ue8m0", _I, [_P, _P, _I, _I, _P]),
@@ -103,6 +104,10 @@ def _bf16(t: torch.Tensor, name: str) -> None:
     _need(t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16, f"{name} must be a contiguous CUDA bf16 tensor")
 
 
+def _f32(t: torch.Tensor, name: str) -> None:
+    _need(t.is_cuda and t.is_contiguous() and t.dtype == torch.float32, f"{name} must be a contiguous CUDA float32 tensor")
+
+
 def sf_shape(mn: int, k: int, groups: Optional[int] = None):
     """Shape of a packed scale tensor for an MN extent and K: [(G,) ceil(K/512), ceil4(mn)]."""
     shape = (-(-(k // 128) // 4), 4 * (-(-mn // 4)))
@@ -123,6 +128,25 @@ def dg_fp8_gemm_nt(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:
         _need(tuple(c.shape) == (M, N), "c shape mismatch")
     _check("dg_fp8_gemm_nt", lib.dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                                                 M, N, K, _stream(stream)))
+    return d
+
+
+def dg_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:
+    """Weight-gradient GEMM, D = C + A @ B.T with FP32 C and D (C may be D itself, which then
+    accumulates in place). a, sfa, b, sfb as dg_fp8_gemm_nt; c [M, N] float32 or None;
+    d [M, N] float32 (written)."""
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _f32(d, "d")
+    M, K = a.shape
+    N = b.shape[0]
+    _need(b.shape[1] == K and tuple(d.shape) == (M, N), "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(M, K) and tuple(sfb.shape) == sf_shape(-(-N // 128), K), "scale shape mismatch")
+    if c is not None:
+        _f32(c, "c")
+        _need(tuple(c.shape) == (M, N), "c shape mismatch")
+    _check("dg_wgrad_gemm_fp8_fp8_fp32_nt",
+           lib.dg_wgrad_gemm_fp8_fp8_fp32_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                             M, N, K, _stream(stream)))
     return d
 
 

@@ -210,13 +210,13 @@ inline int ceil4(int x) { return 4 * ceil_div(x, 4); }
 // Kernel configurations
 // ------------------------------------------------------------------------------------
 template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps_, int kEpiBufs, bool kHasC,
-          int kKG = 1, int kSplit = 0>
+          int kKG = 1, int kSplit = 0, bool kOutF32 = false>
 struct Launcher {
   static constexpr int kEpiWarps = kEpiWarps_;
   using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>;
   static constexpr int kBN = BN;
   static constexpr auto kernel() {
-    return dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG, kSplit>;
+    return dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG, kSplit, kOutF32>;
   }
 
   // Largest number of co-resident clusters of kSplit CTAs (0 if the kernel cannot run).
@@ -346,18 +346,18 @@ int pick_split_bn(int M, int N, int K, int sms, bool with_c) {
 //   192: 4-stage ring, double-buffered accumulators (TMEM 2 x 192 columns)
 //   256: 4-stage ring, single accumulator (TMEM 256 columns; 2 x 256 + scales exceeds 512)
 //   128 x 2: two K-groups per stage (64 KB stages, 3 of them), for HBM-bound stream-K shapes
-template <dg::Kind kKind, bool kHasC>
+template <dg::Kind kKind, bool kHasC, bool kOutF32 = false>
 dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                     const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
                     cudaStream_t stream, int kgroups_per_stage = 1) {
   if constexpr (kKind == dg::Kind::Dense) {
     if (kgroups_per_stage == 2 && bn == 128)
-      return Launcher<kKind, 128, 3, 2, 4, 1, kHasC, 2>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+      return Launcher<kKind, 128, 3, 2, 4, 1, kHasC, 2, 0, kOutF32>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
   }
   switch (bn) {
-    case 128: return Launcher<kKind, 128, 5, 2, 4, 2, kHasC>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
-    case 192: return Launcher<kKind, 192, 4, 2, 4, 2, kHasC>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
-    case 256: return Launcher<kKind, 256, 4, 1, 4, 1, kHasC>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 128: return Launcher<kKind, 128, 5, 2, 4, 2, kHasC, 1, 0, kOutF32>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 192: return Launcher<kKind, 192, 4, 2, 4, 2, kHasC, 1, 0, kOutF32>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 256: return Launcher<kKind, 256, 4, 1, 4, 1, kHasC, 1, 0, kOutF32>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
   }
   return DG_ERR_INVALID_ARG;
 }
@@ -503,6 +503,15 @@ bool map_out(CUtensorMap* m, void* base, int G, int rows, int N) {
   const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(N) * 2 * rows};
   const uint32_t box[3] = {64, 32, 1};
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// FP32 output D (and C) of the weight-gradient form: 32 rows x 32 columns (128 bytes) per TMA
+// store, 128-byte swizzle.
+bool map_out_f32(CUtensorMap* m, void* base, int rows, int N) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(N) * 4};
+  const uint32_t box[2] = {32, 32};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Dense / contiguous GEMM on CTA pairs: converts the scale words into tcgen05.cp chunks in
@@ -690,6 +699,67 @@ __global__ void pack_sf_kernel(const float* __restrict__ sf, int32_t* __restrict
   out[idx] = static_cast<int32_t>(w);
 }
 
+// Dense GEMM on the single-CTA kernel: whole tiles (tile mode) or, with fewer tiles than
+// SMs, stream-K. kOutF32: FP32 C / D (weight-gradient form), else BF16.
+template <bool kOutF32>
+dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                           const void* c, void* d, int M, int N, int K, int BN, int sms, cudaStream_t stream) {
+  DeviceState* ds = &dsr;
+  const int KP = ceil_div(K / 128, 4);
+  CUtensorMap ta, tb, tsa, tsb, td;
+  if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||
+      !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
+      !(kOutF32 ? map_out_f32(&td, d, M, N) : map_out(&td, d, 0, M, N)))
+    return DG_ERR_CUDA;
+  dg::Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.G = 1;
+  p.c = static_cast<const __nv_bfloat16*>(c);
+  p.d = static_cast<__nv_bfloat16*>(d);
+  p.status = ds->status;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
+  const long long tiles = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, BN);
+  int grid = static_cast<int>(tiles < sms ? tiles : sms);
+  // Fewer tiles than SMs: share the K-groups of all tiles among all SMs (stream-K) so that
+  // every SM streams operands; each CTA gets at least kMinKGroupsPerCta K-groups. The
+  // stream-K unit is one pipeline stage: two K-groups for 128-wide tiles (DG_KG=1 selects
+  // one K-group per stage), one otherwise.
+  int kg = 1;
+  if (BN == 128) {
+    const char* f = std::getenv("DG_KG");
+    kg = (f && f[0] == '1') ? 1 : 2;
+  }
+  const int num_kc = ceil_div(K / 128, kg);                 // stream-K units per tile
+  const long long units = tiles * num_kc;
+  const long long sk = std::min<long long>(sms, units * kg / kMinKGroupsPerCta);
+  if (tiles < sms && sk > tiles) {
+    int slots = 1;
+    for (long long t = 0; t < tiles; ++t) {
+      auto owner = [&](long long v) { return ((v + 1) * sk - 1) / units; };
+      const int n = static_cast<int>(owner(t * num_kc + num_kc - 1) - owner(t * num_kc) + 1);
+      slots = std::max(slots, n);
+    }
+    // Layout: a fixed-size counter region first (its position must not depend on the
+    // problem shape: completed launches leave it all-zero for the next one), then partials.
+    const size_t ws_floats = static_cast<size_t>(tiles) * slots * 128 * BN;
+    if (static_cast<size_t>(tiles) * kEpilogueWarps > kSkCounterInts) return DG_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    if (dg_status s = stream_workspace(*ds, stream, kSkCounterInts * 4 + ws_floats * 4, &ws); s != DG_OK) return s;
+    p.sk_ctas = static_cast<int>(sk);
+    p.sk_slots = slots;
+    p.sk_counters = static_cast<int*>(ws);
+    p.sk_ws = reinterpret_cast<float*>(static_cast<int*>(ws) + kSkCounterInts);
+    grid = static_cast<int>(sk);
+  } else {
+    kg = 1;   // tile mode: whole tiles, one K-group per stage
+  }
+  if (c) return launch_bn<dg::Kind::Dense, true, kOutF32>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
+  return launch_bn<dg::Kind::Dense, false, kOutF32>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
+}
+
 }  // namespace
 
 // ======================================================================================
@@ -760,57 +830,26 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
       return launch_split<false>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
     }
   }
-  if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||
-      !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
-      !map_out(&td, d, 0, M, N))
-    return DG_ERR_CUDA;
-  dg::Params p{};
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.G = 1;
-  p.c = static_cast<const __nv_bfloat16*>(c);
-  p.d = static_cast<__nv_bfloat16*>(d);
-  p.status = ds->status;
-  p.timeout_ns = wait_timeout_ns();
-  p.fault = g_fault.load();
-  const long long tiles = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, BN);
-  int grid = static_cast<int>(tiles < sms ? tiles : sms);
-  // Fewer tiles than SMs: share the K-groups of all tiles among all SMs (stream-K) so that
-  // every SM streams operands; each CTA gets at least kMinKGroupsPerCta K-groups. The
-  // stream-K unit is one pipeline stage: two K-groups for 128-wide tiles (DG_KG=1 selects
-  // one K-group per stage), one otherwise.
-  int kg = 1;
-  if (BN == 128) {
-    const char* f = std::getenv("DG_KG");
-    kg = (f && f[0] == '1') ? 1 : 2;
-  }
-  const int num_kc = ceil_div(K / 128, kg);                 // stream-K units per tile
-  const long long units = tiles * num_kc;
-  const long long sk = std::min<long long>(sms, units * kg / kMinKGroupsPerCta);
-  if (tiles < sms && sk > tiles) {
-    int slots = 1;
-    for (long long t = 0; t < tiles; ++t) {
-      auto owner = [&](long long v) { return ((v + 1) * sk - 1) / units; };
-      const int n = static_cast<int>(owner(t * num_kc + num_kc - 1) - owner(t * num_kc) + 1);
-      slots = std::max(slots, n);
-    }
-    // Layout: a fixed-size counter region first (its position must not depend on the
-    // problem shape: completed launches leave it all-zero for the next one), then partials.
-    const size_t ws_floats = static_cast<size_t>(tiles) * slots * 128 * BN;
-    if (static_cast<size_t>(tiles) * kEpilogueWarps > kSkCounterInts) return DG_ERR_UNSUPPORTED;
-    void* ws = nullptr;
-    if (dg_status s = stream_workspace(*ds, stream, kSkCounterInts * 4 + ws_floats * 4, &ws); s != DG_OK) return s;
-    p.sk_ctas = static_cast<int>(sk);
-    p.sk_slots = slots;
-    p.sk_counters = static_cast<int*>(ws);
-    p.sk_ws = reinterpret_cast<float*>(static_cast<int*>(ws) + kSkCounterInts);
-    grid = static_cast<int>(sk);
-  } else {
-    kg = 1;   // tile mode: whole tiles, one K-group per stage
-  }
-  if (c) return launch_bn<dg::Kind::Dense, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
-  return launch_bn<dg::Kind::Dense, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
+  return run_dense_single<false>(*ds, a, sfa, b, sfb, c, d, M, N, K, BN, sms, stream);
+}
+
+dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                        const float* c, float* d, int M, int N, int K, cudaStream_t stream) {
+  if (M < 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (M == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d) return DG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d) || (c && !aligned16(c)))
+    return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  const int sms = sms_to_use(*ds);
+  const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
+  // Tile mode: 192-wide tiles with two accumulators, so that the FP32 epilogue (twice the
+  // bytes of the BF16 one, plus the C read) overlaps the next tile's MMAs (measured on GB300,
+  // 7168x4096x4096 accumulated in place: 1916 TFLOPS at 192 vs 1736 at 256 and 1650 at 128).
+  const int BN = tiles128 < sms ? 128 : (std::getenv("DG_FORCE_BN") || N <= 128 ? pick_bn(dg::Kind::Dense, N) : 192);
+  return run_dense_single<true>(*ds, a, sfa, b, sfb, c, d, M, N, K, BN, sms, stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,

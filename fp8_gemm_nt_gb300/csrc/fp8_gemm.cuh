@@ -313,14 +313,17 @@ __device__ __forceinline__ float4 ld_global_cg_v4f(const float* p) {
   return v;
 }
 
+// kOutF32: C and D are FP32 (the weight-gradient form, D = C + A @ B.T accumulated in FP32);
+// otherwise BF16.
 template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC, int kKG = 1,
-          int kSplit = 0>
+          int kSplit = 0, bool kOutF32 = false>
 __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_d, const Params p) {
   using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>;
   static_assert(kSplit == 0 || kKind == Kind::Dense, "split-K clusters: dense form only");
+  static_assert(!kOutF32 || (kKind == Kind::Dense && kSplit == 0), "FP32 output: dense tile mode / stream-K only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -707,7 +710,47 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
       const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
 
       // (+C) -> BF16 -> swizzled smem -> TMA store / predicated rows, for one 64-column chunk
+      // (FP32 output: two 32-column halves, each one 128-byte-wide TMA box)
       auto store_chunk = [&](float (&f)[64], int col, bool c_added = false) {
+        if constexpr (kOutF32) {
+          const float* cbase = reinterpret_cast<const float*>(p.c);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int hcol = col + 32 * h;
+            if constexpr (kHasC) {
+              if (row_ok && !c_added) {
+                const float* crow = cbase + d_row * p.N + n0 + hcol;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  if (n0 + hcol + 4 * q < p.N) {
+                    const uint4 cv = ld_global_nc_v4(crow + 4 * q);
+                    f[32 * h + 4 * q + 0] = __uint_as_float(cv.x) + f[32 * h + 4 * q + 0];
+                    f[32 * h + 4 * q + 1] = __uint_as_float(cv.y) + f[32 * h + 4 * q + 1];
+                    f[32 * h + 4 * q + 2] = __uint_as_float(cv.z) + f[32 * h + 4 * q + 2];
+                    f[32 * h + 4 * q + 3] = __uint_as_float(cv.w) + f[32 * h + 4 * q + 3];
+                  }
+                }
+              }
+            }
+            uint8_t* sbuf = stage_base + (buf_iter % kEpiBufs) * C::EPI_BUF_BYTES;
+            ++buf_iter;
+            if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
+            __syncwarp();
+            const uint32_t srow = smem_addr(sbuf) + lane * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              st_shared_v4(srow + ((u ^ (lane & 7)) * 16), __float_as_uint(f[32 * h + 4 * u]),
+                           __float_as_uint(f[32 * h + 4 * u + 1]), __float_as_uint(f[32 * h + 4 * u + 2]),
+                           __float_as_uint(f[32 * h + 4 * u + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm_d, sbuf, n0 + hcol, seg.m_blk * BLOCK_M + quad * 32);
+              bulk_commit_group();
+            }
+          }
+          return;
+        }
         if constexpr (kHasC) {
           if (row_ok && !c_added) {
             const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
@@ -837,7 +880,8 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
           constexpr int kRingBytes = C::OFF_EPI - C::OFF_A;
           constexpr int kWarpRing = (kRingBytes / kEpiWarps) & ~1023;
           constexpr int kChunkSlotBytes = 16 * 32 * 16;         // 16 float4 per lane per chunk
-          constexpr int kCBytes = kHasC ? 32 * 128 : 0;         // 32 rows x 64 BF16 columns
+          constexpr bool kPrefetchC = kHasC && !kOutF32;        // an FP32 C is added by store_chunk
+          constexpr int kCBytes = kPrefetchC ? 32 * 128 : 0;    // 32 rows x 64 BF16 columns
           if (seg.cta_last && seg.n_contrib * kChunkSlotBytes + kCBytes <= kWarpRing) {
             const uint32_t region = smem_addr(smem + C::OFF_A) + ew * kWarpRing;
 #pragma unroll 1
@@ -851,7 +895,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
                   cp_async_16(region + s * kChunkSlotBytes + (q * 32 + lane) * 16,
                               src + ((ch * 16 + q) * 32 + lane) * 4);
               }
-              if constexpr (kHasC) {
+              if constexpr (kPrefetchC) {
                 if (row_ok) {
                   const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
 #pragma unroll
@@ -876,7 +920,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
                   f[4 * q + 3] += __uint_as_float(v.w);
                 }
               }
-              if constexpr (kHasC) {
+              if constexpr (kPrefetchC) {
                 if (row_ok) {
 #pragma unroll
                   for (int q = 0; q < 8; ++q) {
@@ -894,7 +938,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
                 }
               }
               __syncwarp();   // all lanes have read the region before the next chunk's copies land
-              store_chunk(f, col, true);
+              store_chunk(f, col, kPrefetchC);
             }
             if (lane == 0) *counter = 0;   // ready for the next launch
             continue;

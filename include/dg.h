@@ -71,6 +71,20 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa,
                          int M, int N, int K, cudaStream_t stream);
 
 /*
+ * Weight-gradient GEMM with FP32 output: D = C + A @ B.T (page "Weight gradient kernels
+ * for dense and MoE models #95", wgrad_gemm_fp8_fp8_fp32_nt: FP8 x FP8 -> FP32, NT). The
+ * pages give nothing beyond the name; the reading taken is the dense GEMM above with an
+ * FP32 addend and output: the gradient accumulated so far is passed as C and may be D
+ * itself (c == d), which then accumulates in place.
+ *   a, sfa, b, sfb, M, N, K : as dg_fp8_gemm_nt (same scale format and constraints).
+ *   c : float32 [M, N] row-major, or NULL (no addend); may alias d.
+ *   d : float32 [M, N] row-major.
+ * Errors as dg_fp8_gemm_nt. Asynchronous on `stream`.
+ */
+dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                        const float* c, float* d, int M, int N, int K, cudaStream_t stream);
+
+/*
  * M-grouped GEMM, contiguous layout ("Grouped GEMMs (contiguous layout)":
  * m_grouped_fp8_gemm_nt_contiguous). Only M is grouped; N and K are shared by the G
  * experts. Each expert's token rows are concatenated along M, and each expert segment

@@ -152,6 +152,27 @@ def fp8_gemm_nt(a, sfa, b, sfb, c: Optional[np.ndarray], M: int, N: int, K: int,
     return D
 
 
+def wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c: Optional[np.ndarray], M: int, N: int, K: int,
+                               rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Weight-gradient GEMM with FP32 output: D = C + A @ B.T, C and D FP32 (page "Weight
+    gradient kernels for dense and MoE models #95": wgrad_gemm_fp8_fp8_fp32_nt, FP8 x FP8 ->
+    FP32, NT layout). The pages give nothing beyond the name, so the reading is the plainest
+    one: the same operands and scale format as fp8_gemm_nt, and an FP32 addend C (the
+    gradient being accumulated; it may be the output buffer itself).
+
+    c: float32 [M, N] or None. Returns FP64 [len(rows), N].
+    """
+    assert K % GROUP_K == 0
+    KG = K // GROUP_K
+    rows = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    sa = unpack_sf(sfa, M, KG)[rows]
+    sb = unpack_sf(sfb, -(-N // BLOCK_N), KG)
+    D = _scaled_gemm(np.asarray(a)[rows], sa, np.asarray(b), sb, K)
+    if c is not None:
+        D = np.asarray(c, dtype=np.float32)[rows].astype(np.float64) + D
+    return D
+
+
 def m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, m_indices, M_total: int, N: int, K: int,
                                      G: int, rows: Optional[Sequence[int]] = None):
     """Contiguous M-grouped GEMM (README "Grouped GEMMs (contiguous layout)").

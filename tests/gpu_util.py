@@ -43,6 +43,18 @@ def run_dense(lib, p: W.Dense, c_alias: bool = False) -> torch.Tensor:
     return d
 
 
+def run_wgrad(lib, p: W.Wgrad, in_place: bool = False) -> torch.Tensor:
+    """FP32 D = C + A @ B.T; with in_place, D is the C buffer itself (accumulation)."""
+    c = dev(p.c) if p.c is not None else None
+    if in_place and c is not None:
+        d = c
+    else:
+        d = torch.full((p.M, p.N), float("nan"), dtype=torch.float32).cuda()
+    lib.dg_wgrad_gemm_fp8_fp8_fp32_nt(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), c, d)
+    torch.cuda.synchronize()
+    return d
+
+
 def run_contiguous(lib, p: W.Contiguous) -> torch.Tensor:
     d = sentinel_like((p.M_total, p.N))
     lib.dg_m_grouped_fp8_gemm_nt_contiguous(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d, dev(p.m_indices))

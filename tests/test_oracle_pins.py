@@ -260,9 +260,40 @@ def pin_masked_equals_dense(O_):
         assert np.array_equal(D[g, :m], ref)
 
 
+def pin_wgrad_brute_force(O_):
+    # FP32 addend values that BF16 cannot hold: an addend rounded to BF16, dropped or
+    # subtracted fails this exact rational check
+    rng = np.random.default_rng(21)
+    M, N, K = 3, 130, 256
+    a, b = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    ea = rng.integers(122, 133, size=(M, 2)).astype(np.uint8)
+    eb = rng.integers(122, 133, size=(2, 2)).astype(np.uint8)
+    c = (rng.standard_normal((M, N)) * 3).astype(np.float32)
+    c[0, 0] = np.float32(1.0) + np.float32(2.0 ** -20)
+    got = O_.wgrad_gemm_fp8_fp8_fp32_nt(a, words_from_codes(ea), b, words_from_codes(eb), c, M, N, K)
+    exact = brute_force(a, ea, b, eb)
+    for m in range(M):
+        for n in range(N):
+            want = float(Fraction(float(exact[m, n])) + Fraction(float(c[m, n])))
+            assert got[m, n] == pytest.approx(want, rel=1e-15, abs=1e-300), (m, n)
+    # no addend: the dense result exactly
+    assert np.array_equal(O_.wgrad_gemm_fp8_fp8_fp32_nt(a, words_from_codes(ea), b, words_from_codes(eb),
+                                                        None, M, N, K), dense(O_, a, ea, b, eb))
+
+
+def pin_wgrad_c_only(O_):
+    rng = np.random.default_rng(22)
+    M, N, K = 4, 96, 128
+    c = rng.standard_normal((M, N)).astype(np.float32)
+    got = O_.wgrad_gemm_fp8_fp8_fp32_nt(np.zeros((M, K), np.uint8), words_from_codes(np.full((M, 1), 127, np.uint8)),
+                                        random_codes(rng, (N, K)), words_from_codes(np.full((1, 1), 127, np.uint8)),
+                                        c, M, N, K)
+    assert np.array_equal(got, c.astype(np.float64))
+
+
 PINS = [pin_e4m3_table, pin_ue8m0_table, pin_bf16, pin_unpack, pin_brute_force, pin_identity,
         pin_one_hot, pin_pow2_invariance, pin_c_only, pin_dequantised_route,
-        pin_contiguous_equals_dense, pin_masked_equals_dense]
+        pin_contiguous_equals_dense, pin_masked_equals_dense, pin_wgrad_brute_force, pin_wgrad_c_only]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -375,6 +406,20 @@ def _masked_off_by_one(old):
     return f
 
 
+def _wgrad_c_as_bf16(old):
+    def f(a, sfa, b, sfb, c, M, N, K, rows=None):
+        if c is not None:
+            c = torch.from_numpy(np.asarray(c, np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
+        return old(a, sfa, b, sfb, c, M, N, K, rows)
+    return f
+
+
+def _wgrad_c_dropped(old):
+    def f(a, sfa, b, sfb, c, M, N, K, rows=None):
+        return old(a, sfa, b, sfb, None, M, N, K, rows)
+    return f
+
+
 MUTANTS = {
     "subnormal_implicit_one": _mut_table(_subnormal_with_implicit_one),
     "sign_ignored": _mut_table(lambda t: np.abs(t)),
@@ -387,6 +432,8 @@ MUTANTS = {
     "c_subtracted": _mut_attr("fp8_gemm_nt", _c_sign),
     "contiguous_pad_uses_last_expert": _mut_attr("m_grouped_fp8_gemm_nt_contiguous", _contig_negative_index),
     "masked_off_by_one": _mut_attr("m_grouped_fp8_gemm_nt_masked", _masked_off_by_one),
+    "wgrad_c_rounded_to_bf16": _mut_attr("wgrad_gemm_fp8_fp8_fp32_nt", _wgrad_c_as_bf16),
+    "wgrad_c_dropped": _mut_attr("wgrad_gemm_fp8_fp8_fp32_nt", _wgrad_c_dropped),
 }
 
 

@@ -1,4 +1,4 @@
-"""Parity at the five workload sizes, in the launch configuration the benchmark times.
+"""Parity at the workload sizes, in the launch configuration the benchmark times.
 
 The oracle computes sampled rows (all N columns) of each full-size problem; the
 integer decisions (padding rows of the contiguous layout, masked rows) are checked
@@ -12,7 +12,8 @@ import torch
 
 import oracle as O
 import workloads as W
-from gpu_util import SENTINEL, assert_parity, bf16_bits, bf16_f64, run_contiguous, run_dense, run_masked
+from gpu_util import (SENTINEL, assert_parity, bf16_bits, bf16_f64, run_contiguous, run_dense, run_masked,
+                      run_wgrad)
 
 pytestmark = pytest.mark.gpu
 
@@ -75,4 +76,15 @@ def test_masked_workload(lib):
                                             groups=groups)
     got = bf16_f64(d)[groups]
     assert_parity(got[v], ref[v], name)
+    assert lib.dg_get_device_status() == 0
+
+
+def test_wgrad_workload(lib):
+    name = "wgrad_7168x4096x4096_c"
+    p = W.make_workload(name)
+    d = run_wgrad(lib, p).cpu().numpy().astype(np.float64)
+    rows = _rows(p.M, 64, 4)
+    ref = O.wgrad_gemm_fp8_fp8_fp32_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K, rows=rows)
+    assert_parity(d[rows], ref, name)
+    assert np.isfinite(d).all()
     assert lib.dg_get_device_status() == 0

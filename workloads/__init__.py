@@ -128,6 +128,23 @@ class Dense:
 
 
 @dataclasses.dataclass
+class Wgrad:
+    """Weight-gradient GEMM operands: like Dense, with an FP32 addend / output."""
+    a: np.ndarray              # uint8 [M, K]
+    sfa: np.ndarray            # int32 [KP, ceil4(M)]
+    b: np.ndarray              # uint8 [N, K]
+    sfb: np.ndarray            # int32 [KP, ceil4(ceil(N/128))]
+    c: Optional[np.ndarray]    # float32 [M, N] or None
+    M: int
+    N: int
+    K: int
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+
+@dataclasses.dataclass
 class Contiguous:
     a: np.ndarray              # uint8 [M_total, K]
     sfa: np.ndarray            # int32 [KP, ceil4(M_total)]
@@ -190,6 +207,15 @@ def make_dense(M: int, N: int, K: int, seed: int, with_c: bool = False,
     return Dense(a, pack_sf(ea), b, pack_sf(eb), c, M, N, K)
 
 
+def make_wgrad(M: int, N: int, K: int, seed: int, with_c: bool = True) -> Wgrad:
+    """A, B quantised like make_dense; C ~ N(0,1) in FP32 (the gradient accumulated so far)."""
+    rng = _rng(seed)
+    a, ea = quantize_rows(_normal(rng, (M, K)))
+    b, eb = quantize_blocks(_normal(rng, (N, K)))
+    c = rng.standard_normal((M, N), dtype=np.float32) if with_c else None
+    return Wgrad(a, pack_sf(ea), b, pack_sf(eb), c, M, N, K)
+
+
 def _make_b_grouped(rng, G, N, K):
     bs, sfbs = [], []
     for _ in range(G):
@@ -250,6 +276,8 @@ WORKLOADS = {
                                           row_magnitude=True),
     "contiguous_g8_t32768_n4096_k7168": dict(kind="contiguous", G=8, tokens=32768, N=4096, K=7168),
     "masked_g32_m256_n7168_k2048": dict(kind="masked", G=32, max_m=256, N=7168, K=2048),
+    # weight gradient of a 7168 x 4096 projection over 4096 tokens, accumulated into FP32
+    "wgrad_7168x4096x4096_c": dict(kind="wgrad", M=7168, N=4096, K=4096, with_c=True),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -262,6 +290,8 @@ def make_workload(name: str):
         return make_dense(seed=seed, **spec)
     if kind == "contiguous":
         return make_contiguous(seed=seed, **spec)
+    if kind == "wgrad":
+        return make_wgrad(seed=seed, **spec)
     return make_masked(seed=seed, **spec)
 
 
