@@ -173,6 +173,47 @@ def wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c: Optional[np.ndarray], M: int, 
     return D
 
 
+def k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c: Optional[np.ndarray], ks, M: int, N: int,
+                                         groups: Optional[Sequence[int]] = None,
+                                         rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """K-grouped weight-gradient GEMM for MoE (page "Weight gradient kernels for dense and MoE
+    models #95": k_grouped_wgrad_gemm_fp8_fp8_fp32_nt; README "Grouped GEMMs": the K-axis-
+    grouped API with M and N fixed). Expert g owns the K-slice [off_g, off_g + ks[g]) of A
+    [M, K_total] and B [N, K_total] (off_g = ks[0] + ... + ks[g-1]) and gets its own FP32
+    output: D[g] = C[g] + A[:, slice_g] @ B[:, slice_g].T.
+
+    Readings (the pages name the function only): every ks[g] is a multiple of 128, so scale
+    K-groups never straddle experts; the packed scale words are laid out per expert (the
+    README lists a separate "K-grouped" packing utility): expert g's K-groups j = 0, 1, ...
+    sit in byte j % 4 of word row R_g + j // 4, R_g = sum over h < g of ceil(ks[h] / 512),
+    MN-major as elsewhere. An expert with ks[g] = 0 gets D[g] = C[g] (0 without C).
+
+    a: uint8 [M, K_total]; sfa: int32 [sum_g ceil(ks_g/512), ceil4(M)]; b: uint8 [N, K_total];
+    sfb: int32 [sum_g ceil(ks_g/512), ceil4(ceil(N/128))]; c: float32 [G, M, N] or None.
+    Returns FP64 [len(groups), len(rows), N].
+    """
+    ks = [int(k) for k in ks]
+    G = len(ks)
+    assert all(k >= 0 and k % GROUP_K == 0 for k in ks)
+    groups = range(G) if groups is None else groups
+    rows = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    NB = -(-N // BLOCK_N)
+    offs = np.concatenate([[0], np.cumsum(ks)]).astype(np.int64)
+    word_rows = np.concatenate([[0], np.cumsum([-(-k // (4 * GROUP_K)) for k in ks])]).astype(np.int64)
+    out = np.zeros((len(groups), len(rows), N), np.float64)
+    for i, g in enumerate(groups):
+        kg = ks[g] // GROUP_K
+        if kg > 0:
+            w0, w1 = word_rows[g], word_rows[g + 1]
+            sa = unpack_sf(np.asarray(sfa)[w0:w1], M, kg)[rows]
+            sb = unpack_sf(np.asarray(sfb)[w0:w1], NB, kg)
+            ksl = slice(offs[g], offs[g + 1])
+            out[i] = _scaled_gemm(np.asarray(a)[rows][:, ksl], sa, np.asarray(b)[:, ksl], sb, ks[g])
+        if c is not None:
+            out[i] = np.asarray(c, dtype=np.float32)[g][rows].astype(np.float64) + out[i]
+    return out
+
+
 def m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, m_indices, M_total: int, N: int, K: int,
                                      G: int, rows: Optional[Sequence[int]] = None):
     """Contiguous M-grouped GEMM (README "Grouped GEMMs (contiguous layout)").

@@ -291,9 +291,40 @@ def pin_wgrad_c_only(O_):
     assert np.array_equal(got, c.astype(np.float64))
 
 
+def pin_k_grouped_equals_per_expert(O_):
+    # each expert's output is the dense FP32-output GEMM of its own K-slice, with its own
+    # scales packed separately; an expert with no tokens returns its C; and against exact
+    # rationals on a few entries
+    rng = np.random.default_rng(23)
+    M, N, ks = 5, 200, [256, 0, 384, 128]
+    K_total = sum(ks)
+    a, b = random_codes(rng, (M, K_total)), random_codes(rng, (N, K_total))
+    ea = rng.integers(123, 132, size=(M, K_total // 128)).astype(np.uint8)
+    eb = rng.integers(123, 132, size=(2, K_total // 128)).astype(np.uint8)
+    c = rng.standard_normal((len(ks), M, N)).astype(np.float32)
+    sfa, sfb = W.pack_sf_k_grouped(ea, ks), W.pack_sf_k_grouped(eb, ks)
+    assert sfa.shape[0] == 1 + 0 + 1 + 1
+    D = O_.k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c, ks, M, N)
+    off = 0
+    for g, k in enumerate(ks):
+        kg = k // 128
+        if k == 0:
+            assert np.array_equal(D[g], c[g].astype(np.float64))
+            continue
+        sl = slice(off, off + k)
+        gs = slice(off // 128, off // 128 + kg)
+        ref = O_.wgrad_gemm_fp8_fp8_fp32_nt(a[:, sl], words_from_codes(ea[:, gs]), b[:, sl],
+                                            words_from_codes(eb[:, gs]), c[g], M, N, k)
+        assert np.array_equal(D[g], ref)
+        exact = brute_force(a[:2, sl], ea[:2, gs], b[:, sl], eb[:, gs])
+        np.testing.assert_allclose(D[g, :2], exact + c[g, :2].astype(np.float64), rtol=1e-14)
+        off += k
+
+
 PINS = [pin_e4m3_table, pin_ue8m0_table, pin_bf16, pin_unpack, pin_brute_force, pin_identity,
         pin_one_hot, pin_pow2_invariance, pin_c_only, pin_dequantised_route,
-        pin_contiguous_equals_dense, pin_masked_equals_dense, pin_wgrad_brute_force, pin_wgrad_c_only]
+        pin_contiguous_equals_dense, pin_masked_equals_dense, pin_wgrad_brute_force, pin_wgrad_c_only,
+        pin_k_grouped_equals_per_expert]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -420,6 +451,30 @@ def _wgrad_c_dropped(old):
     return f
 
 
+def _k_grouped_global_packing(old):
+    # reads the scale words as if packed over the whole K axis (not per expert)
+    def f(a, sfa, b, sfb, c, ks, M, N, groups=None, rows=None):
+        ks = [int(k) for k in ks]
+        K_total = sum(ks)
+        KG = K_total // 128
+        NB = -(-N // 128)
+        ea = O.unpack_sf(np.asarray(sfa), M, min(KG, 4 * np.asarray(sfa).shape[0]))
+        eb = O.unpack_sf(np.asarray(sfb), NB, min(KG, 4 * np.asarray(sfb).shape[0]))
+        pad = KG - ea.shape[1]
+        if pad > 0:
+            ea = np.concatenate([ea, np.full((M, pad), 127, ea.dtype)], 1)
+            eb = np.concatenate([eb, np.full((NB, pad), 127, eb.dtype)], 1)
+        out, off = [], 0
+        for g, k in enumerate(ks):
+            kg = k // 128
+            sl = slice(off * 128, (off + kg) * 128)
+            d = O._scaled_gemm(a[:, sl], ea[:, off:off + kg], b[:, sl], eb[:, off:off + kg], k) if kg else np.zeros((M, N))
+            out.append((np.asarray(c, np.float32)[g].astype(np.float64) if c is not None else 0) + d)
+            off += kg
+        return np.stack(out)
+    return f
+
+
 MUTANTS = {
     "subnormal_implicit_one": _mut_table(_subnormal_with_implicit_one),
     "sign_ignored": _mut_table(lambda t: np.abs(t)),
@@ -434,6 +489,7 @@ MUTANTS = {
     "masked_off_by_one": _mut_attr("m_grouped_fp8_gemm_nt_masked", _masked_off_by_one),
     "wgrad_c_rounded_to_bf16": _mut_attr("wgrad_gemm_fp8_fp8_fp32_nt", _wgrad_c_as_bf16),
     "wgrad_c_dropped": _mut_attr("wgrad_gemm_fp8_fp8_fp32_nt", _wgrad_c_dropped),
+    "k_grouped_scales_packed_globally": _mut_attr("k_grouped_wgrad_gemm_fp8_fp8_fp32_nt", _k_grouped_global_packing),
 }
 
 

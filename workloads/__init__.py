@@ -145,6 +145,31 @@ class Wgrad:
 
 
 @dataclasses.dataclass
+class KGrouped:
+    """K-grouped weight-gradient operands: expert g owns K-slice [off_g, off_g + ks[g])."""
+    a: np.ndarray              # uint8 [M, K_total]
+    sfa: np.ndarray            # int32 [sum_g ceil(ks_g/512), ceil4(M)], packed per expert
+    b: np.ndarray              # uint8 [N, K_total]
+    sfb: np.ndarray            # int32 [sum_g ceil(ks_g/512), ceil4(ceil(N/128))], packed per expert
+    c: Optional[np.ndarray]    # float32 [G, M, N] or None
+    ks: np.ndarray             # int32 [G], multiples of 128
+    M: int
+    N: int
+
+    @property
+    def G(self) -> int:
+        return len(self.ks)
+
+    @property
+    def K_total(self) -> int:
+        return int(self.ks.sum())
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * float(self.ks.sum())
+
+
+@dataclasses.dataclass
 class Contiguous:
     a: np.ndarray              # uint8 [M_total, K]
     sfa: np.ndarray            # int32 [KP, ceil4(M_total)]
@@ -216,6 +241,39 @@ def make_wgrad(M: int, N: int, K: int, seed: int, with_c: bool = True) -> Wgrad:
     return Wgrad(a, pack_sf(ea), b, pack_sf(eb), c, M, N, K)
 
 
+def pack_sf_k_grouped(exps: np.ndarray, ks) -> np.ndarray:
+    """Exponents [MN, K_total/128] -> words packed per expert K-slice, concatenated along the
+    word-row axis: [sum_g ceil(ks_g/512), ceil4(MN)]."""
+    parts, off = [], 0
+    for k in ks:
+        kg = int(k) // GROUP_K
+        if kg > 0:
+            parts.append(pack_sf(exps[:, off:off + kg]))
+        off += kg
+    if not parts:
+        return np.zeros((0, ceil4(exps.shape[0])), np.int32)
+    return np.ascontiguousarray(np.concatenate(parts, axis=0))
+
+
+def make_k_grouped(G: int, M: int, N: int, tokens: int, seed: int, with_c: bool = True,
+                   ks: Optional[np.ndarray] = None) -> KGrouped:
+    """Token counts ~ Multinomial(tokens, 1/G) per expert (or given), each rounded up to a
+    multiple of 128 (the alignment the K-grouped layout needs); A [M, K_total] and B [N, K_total]
+    quantised like make_dense over the concatenated K; C ~ N(0,1) FP32 per expert."""
+    rng = _rng(seed)
+    if ks is None:
+        counts = rng.multinomial(tokens, [1.0 / G] * G)
+        ks = np.array([MK_ALIGNMENT * ceil_div(int(c), MK_ALIGNMENT) for c in counts], np.int32)
+    ks = np.asarray(ks, dtype=np.int32)
+    K_total = int(ks.sum())
+    a, ea = quantize_rows(_normal(rng, (M, max(K_total, GROUP_K))))
+    b, eb = quantize_blocks(_normal(rng, (N, max(K_total, GROUP_K))))
+    a, ea, b, eb = a[:, :K_total], ea[:, :K_total // GROUP_K], b[:, :K_total], eb[:, :K_total // GROUP_K]
+    c = rng.standard_normal((len(ks), M, N), dtype=np.float32) if with_c else None
+    return KGrouped(np.ascontiguousarray(a), pack_sf_k_grouped(ea, ks), np.ascontiguousarray(b),
+                    pack_sf_k_grouped(eb, ks), c, ks, M, N)
+
+
 def _make_b_grouped(rng, G, N, K):
     bs, sfbs = [], []
     for _ in range(G):
@@ -278,6 +336,8 @@ WORKLOADS = {
     "masked_g32_m256_n7168_k2048": dict(kind="masked", G=32, max_m=256, N=7168, K=2048),
     # weight gradient of a 7168 x 4096 projection over 4096 tokens, accumulated into FP32
     "wgrad_7168x4096x4096_c": dict(kind="wgrad", M=7168, N=4096, K=4096, with_c=True),
+    # MoE weight gradient: 4 experts, 4096 x 7168 each, 16384 tokens split among them
+    "k_grouped_wgrad_g4_m4096_n7168_t16384": dict(kind="k_grouped", G=4, M=4096, N=7168, tokens=16384),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -292,6 +352,8 @@ def make_workload(name: str):
         return make_contiguous(seed=seed, **spec)
     if kind == "wgrad":
         return make_wgrad(seed=seed, **spec)
+    if kind == "k_grouped":
+        return make_k_grouped(seed=seed, **spec)
     return make_masked(seed=seed, **spec)
 
 
