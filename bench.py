@@ -81,6 +81,10 @@ def algorithmic(p):
         # the FP32 gradient is read (C) and written (D) in place
         by = _nbytes(p.a, p.sfa, p.b, p.sfb) + (p.M * p.N * 4 if p.c is not None else 0) + p.M * p.N * 4
         return p.flops, by
+    if isinstance(p, W.KGrouped):
+        out = p.G * p.M * p.N * 4
+        by = _nbytes(p.a, p.sfa, p.b, p.sfb, p.ks) + (out if p.c is not None else 0) + out
+        return p.flops, by
     if isinstance(p, W.Contiguous):
         v = p.valid_rows
         used = sorted(set(int(g) for g in p.m_indices if g >= 0))
@@ -106,6 +110,8 @@ class DeviceProblem:
         p = self.p
         if isinstance(p, (W.Dense, W.Wgrad)):
             return [x for x in (p.a, p.sfa, p.b, p.sfb, p.c) if x is not None]
+        if isinstance(p, W.KGrouped):
+            return [x for x in (p.a, p.sfa, p.b, p.sfb, p.c, p.ks) if x is not None]
         if isinstance(p, W.Contiguous):
             return [p.a, p.sfa, p.b, p.sfb, p.m_indices]
         return [p.a, p.sfa, p.b, p.sfb, p.masked_m]
@@ -116,6 +122,8 @@ class DeviceProblem:
             return p.M * p.N * 2
         if isinstance(p, W.Wgrad):
             return 0 if p.c is not None else p.M * p.N * 4   # D is C (accumulated in place)
+        if isinstance(p, W.KGrouped):
+            return 0 if p.c is not None else p.G * p.M * p.N * 4
         if isinstance(p, W.Contiguous):
             return p.M_total * p.N * 2
         return p.G * p.max_m * p.N * 2
@@ -131,6 +139,10 @@ class DeviceProblem:
         if isinstance(p, W.Wgrad):
             d = f(p.c) if p.c is not None else t.zeros((p.M, p.N), dtype=t.float32, device="cuda")
             return dict(a=f(p.a), sfa=f(p.sfa), b=f(p.b), sfb=f(p.sfb), c=d if p.c is not None else None, d=d)
+        if isinstance(p, W.KGrouped):
+            d = f(p.c) if p.c is not None else t.zeros((p.G, p.M, p.N), dtype=t.float32, device="cuda")
+            return dict(a=f(p.a), sfa=f(p.sfa), b=f(p.b), sfb=f(p.sfb), c=d if p.c is not None else None, d=d,
+                        ks=f(np.asarray(p.ks, np.int32)))
         if isinstance(p, W.Contiguous):
             return dict(a=f(p.a), sfa=f(p.sfa), b=f(p.b), sfb=f(p.sfb), idx=f(p.m_indices),
                         d=t.empty((p.M_total, p.N), dtype=t.bfloat16, device="cuda"))
@@ -144,6 +156,8 @@ class DeviceProblem:
             L.dg_fp8_gemm_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
         elif isinstance(p, W.Wgrad):
             L.dg_wgrad_gemm_fp8_fp8_fp32_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
+        elif isinstance(p, W.KGrouped):
+            L.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"], c["ks"])
         elif isinstance(p, W.Contiguous):
             L.dg_m_grouped_fp8_gemm_nt_contiguous(c["a"], c["sfa"], c["b"], c["sfb"], c["d"], c["idx"])
         else:

@@ -31,6 +31,7 @@ _I = ctypes.c_int
 SIGNATURES = [
     ("dg_fp8_gemm_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("dg_wgrad_gemm_fp8_fp8_fp32_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_pack_sf_ue8m0", _I, [_P, _P, _I, _I, _P]),
@@ -147,6 +148,29 @@ def dg_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c, d, stream=None) -> torch.Te
     _check("dg_wgrad_gemm_fp8_fp8_fp32_nt",
            lib.dg_wgrad_gemm_fp8_fp8_fp32_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                                              M, N, K, _stream(stream)))
+    return d
+
+
+def dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c, d, ks, stream=None) -> torch.Tensor:
+    """K-grouped weight-gradient GEMM: D[g] = C[g] + A[:, slice_g] @ B[:, slice_g].T in FP32,
+    expert g owning the K-slice of length ks[g]. a [M, K_total] e4m3, sfa [R, ceil4(M)] int32
+    (packed per expert, R word rows), b [N, K_total], sfb [R, ceil4(ceil(N/128))],
+    c [G, M, N] float32 or None (may be d), d [G, M, N] float32, ks [G] int32 (CUDA)."""
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _f32(d, "d"); _i32(ks, "ks")
+    M, K = a.shape
+    N = b.shape[0]
+    G = ks.shape[0]
+    _need(b.shape[1] == K and tuple(d.shape) == (G, M, N), "shape mismatch")
+    R = sfa.shape[0]
+    _need(sfa.dim() == 2 and sfa.shape[1] == 4 * (-(-M // 4)) and sfb.dim() == 2 and sfb.shape[0] == R
+          and sfb.shape[1] == 4 * (-(-(-(-N // 128)) // 4)), "scale shape mismatch")
+    if c is not None:
+        _f32(c, "c")
+        _need(tuple(c.shape) == (G, M, N), "c shape mismatch")
+    _check("dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt",
+           lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                                       _ptr(ks), G, M, N, K, R, _stream(stream)))
     return d
 
 

@@ -852,6 +852,57 @@ dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const
   return run_dense_single<true>(*ds, a, sfa, b, sfb, c, d, M, N, K, BN, sms, stream);
 }
 
+dg_status dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const void* b,
+                                                const int32_t* sfb, const float* c, float* d, const int32_t* ks,
+                                                int G, int M, int N, int K_total, int sf_k_rows,
+                                                cudaStream_t stream) {
+  if (G <= 0 || M < 0 || K_total < 0 || sf_k_rows < 0) return DG_ERR_INVALID_ARG;
+  if (N <= 0 || N % 16 != 0 || K_total % 128 != 0) return DG_ERR_INVALID_ARG;
+  if (M == 0) return DG_OK;
+  if (!d || !ks || (K_total > 0 && (!a || !sfa || !b || !sfb || sf_k_rows == 0))) return DG_ERR_INVALID_ARG;
+  if ((K_total > 0 && (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb))) || !aligned16(d) ||
+      (c && !aligned16(c)) || (reinterpret_cast<uintptr_t>(ks) & 3u))
+    return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  const size_t out_bytes = static_cast<size_t>(G) * M * N * sizeof(float);
+  if (K_total == 0) {
+    // no tokens at all: every expert's output is its addend (or zero)
+    cudaError_t e = c ? (c == d ? cudaSuccess : cudaMemcpyAsync(d, c, out_bytes, cudaMemcpyDeviceToDevice, stream))
+                      : cudaMemsetAsync(d, 0, out_bytes, stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e);
+  }
+  const int sms = sms_to_use(*ds);
+  const int BN = std::getenv("DG_FORCE_BN") || N <= 128 ? pick_bn(dg::Kind::Dense, N) : 192;
+  CUtensorMap ta, tb, tsa, tsb, td;
+  bool ok = map_operand_2d(&ta, a, M, K_total, 128) && map_operand_2d(&tb, b, N, K_total, BN) &&
+            map_sf(&tsa, sfa, 0, M, sf_k_rows, 128) && map_sf(&tsb, sfb, 0, ceil_div(N, 128), sf_k_rows, 8);
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(N) * 4, static_cast<uint64_t>(N) * M * 4};
+    const uint32_t box[3] = {32, 32, 1};
+    ok = ok && make_map(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return DG_ERR_CUDA;
+  dg::Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K_total;
+  p.G = G;
+  p.c = reinterpret_cast<const __nv_bfloat16*>(c);   // FP32 in this form (the kernel reinterprets)
+  p.d = reinterpret_cast<__nv_bfloat16*>(d);
+  p.ks = ks;
+  p.sf_k_rows = sf_k_rows;
+  p.status = ds->status;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
+  const long long tiles = static_cast<long long>(G) * ceil_div(M, 128) * ceil_div(N, BN);
+  if (tiles > (1LL << 30)) return DG_ERR_UNSUPPORTED;
+  const int grid = static_cast<int>(std::min<long long>(tiles, sms));
+  if (c) return launch_bn<dg::Kind::KGrouped, true, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+  return launch_bn<dg::Kind::KGrouped, false, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+}
+
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
                                               void* d, const int32_t* m_indices, int M_total, int N, int K, int G,
                                               cudaStream_t stream) {

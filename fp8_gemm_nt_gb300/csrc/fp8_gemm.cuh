@@ -37,7 +37,8 @@
 
 namespace dg {
 
-enum class Kind : int { Dense = 0, Contiguous = 1, Masked = 2 };
+// KGrouped: the K-grouped weight-gradient form (expert g owns a K-slice; FP32 output per expert)
+enum class Kind : int { Dense = 0, Contiguous = 1, Masked = 2, KGrouped = 3 };
 
 // Device status bits: bit (1 << s) for dg_status s.
 enum : uint32_t { kStatusTimeoutBit = 1u << 5, kStatusBadIndexBit = 1u << 6 };
@@ -69,6 +70,10 @@ struct Params {
   // CTA-pair kernel: row counts of the tcgen05.cp-layout scale chunk tensors
   int sf_num_mb;                  // 128-row blocks of A per K-quad
   int sf_nb;                      // B chunk rows per (group, K-quad): two per tile
+  // K-grouped form: K-slice length of each expert (device, multiples of 128) and the number
+  // of packed scale-word rows (the scales of each expert start a new word row)
+  const int32_t* ks;
+  int sf_k_rows;
 };
 
 __host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) / b; }
@@ -148,12 +153,15 @@ struct Segment {
   int n_contrib;  // CTAs contributing to this tile (1 = this segment is the whole tile)
   int slot;       // this CTA's position among them
   bool cta_last;  // stream-K: no further segment for this CTA (its ring smem is free afterwards)
+  int k_base;     // K-grouped: first K-group of the expert's slice (0 otherwise)
+  int sf_row;     // K-grouped: first packed scale-word row of the expert (0 otherwise)
 };
 
 template <Kind kKind, int BN, int kKG = 1, int kSplit = 0>
 struct Scheduler {
   int num_n, num_m, total, num_kb, num_kc;   // num_kc: stream-K units (kKG K-groups) per tile
   int g_cur, g_start, g_tiles;   // masked: incremental walk over groups
+  int kbase_cur, sfrow_cur;      // K-grouped: K-group and scale-row offsets of expert g_cur
   int t;                         // tile mode: next tile index
   long long u, u_end, U;         // stream-K: this CTA's K-group range, total K-groups
   bool stream_k;
@@ -172,6 +180,8 @@ struct Scheduler {
     g_start = 0;
     g_tiles = 0;
     t = blockIdx.x;
+    kbase_cur = 0;
+    sfrow_cur = 0;
     stream_k = false;
     u = u_end = U = 0;
     if constexpr (kSplit > 0) {
@@ -181,6 +191,25 @@ struct Scheduler {
       const int r = static_cast<int>(blockIdx.x) % kSplit;
       u = static_cast<long long>(r) * num_kc / kSplit;
       u_end = static_cast<long long>(r + 1) * num_kc / kSplit;
+      return;
+    }
+    if constexpr (kKind == Kind::KGrouped) {
+      total = p.G * num_m * num_n;
+      if (blockIdx.x == 0 && threadIdx.x == 0) {
+        // every slice a non-negative multiple of 128, the slices covering K, the scale rows
+        // matching the per-expert packing; otherwise the layout is violated (reported)
+        long long kg_sum = 0, rows = 0;
+        bool bad = false;
+        for (int g = 0; g < p.G; ++g) {
+          const int k = __ldg(p.ks + g);
+          if (k < 0 || k % BLOCK_K != 0) bad = true;
+          if (k > 0) {
+            kg_sum += k / BLOCK_K;
+            rows += (k + 4 * BLOCK_K - 1) / (4 * BLOCK_K);
+          }
+        }
+        if (bad || kg_sum != num_kb || rows != p.sf_k_rows) atomicOr(p.status, kStatusBadIndexBit);
+      }
       return;
     }
     if constexpr (kKind == Kind::Masked) {
@@ -214,6 +243,38 @@ struct Scheduler {
   // Next segment of this CTA; false when there is none left. Contiguous padding blocks
   // are skipped here (every role skips the same ones).
   __device__ __forceinline__ bool next(const Params& p, Segment& s) {
+    s.k_base = 0;
+    s.sf_row = 0;
+    if constexpr (kKind == Kind::KGrouped) {
+      if (t >= total) return false;
+      const int cur = t;
+      t += gridDim.x;
+      const int tpg = num_m * num_n;
+      const int g = cur / tpg;
+      while (g_cur < g) {   // experts are visited in increasing order
+        const int k = __ldg(p.ks + g_cur);
+        if (k > 0) {
+          kbase_cur += k / BLOCK_K;
+          sfrow_cur += (k + 4 * BLOCK_K - 1) / (4 * BLOCK_K);
+        }
+        ++g_cur;
+      }
+      const int local = cur - g * tpg;
+      const int k = __ldg(p.ks + g);
+      s.tile = cur;
+      s.g = g;
+      s.m_blk = local / num_n;
+      s.n_blk = local % num_n;
+      s.valid_m = p.M;
+      s.kb_begin = 0;
+      s.kb_end = k > 0 ? k / BLOCK_K : 0;   // 0: an expert without tokens (D = C)
+      s.k_base = kbase_cur;
+      s.sf_row = sfrow_cur;
+      s.n_contrib = 1;
+      s.slot = 0;
+      s.cta_last = false;
+      return true;
+    }
     if constexpr (kSplit > 0) {
       if (t >= total || u >= u_end) return false;
       s.tile = t;
@@ -323,7 +384,9 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
                     const __grid_constant__ CUtensorMap tm_d, const Params p) {
   using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>;
   static_assert(kSplit == 0 || kKind == Kind::Dense, "split-K clusters: dense form only");
-  static_assert(!kOutF32 || (kKind == Kind::Dense && kSplit == 0), "FP32 output: dense tile mode / stream-K only");
+  static_assert(!kOutF32 || ((kKind == Kind::Dense || kKind == Kind::KGrouped) && kSplit == 0),
+                "FP32 output: dense (tile mode / stream-K) and K-grouped forms only");
+  static_assert(kKind != Kind::KGrouped || (kOutF32 && kKG == 1), "the K-grouped form writes FP32, one K-group per stage");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -409,10 +472,10 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
             if constexpr (kKind == Kind::Masked) {
               tma_load_3d(sa + j * C::A_SUB, &tm_a, fb, (kb + j) * BLOCK_K, row0, seg.g);
             } else {
-              tma_load_2d(sa + j * C::A_SUB, &tm_a, fb, (kb + j) * BLOCK_K, row0);
+              tma_load_2d(sa + j * C::A_SUB, &tm_a, fb, (seg.k_base + kb + j) * BLOCK_K, row0);
             }
-            if constexpr (kKind == Kind::Dense) {
-              tma_load_2d(sb + j * C::B_SUB, &tm_b, fb, (kb + j) * BLOCK_K, n0);
+            if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
+              tma_load_2d(sb + j * C::B_SUB, &tm_b, fb, (seg.k_base + kb + j) * BLOCK_K, n0);
             } else {
               tma_load_3d(sb + j * C::B_SUB, &tm_b, fb, (kb + j) * BLOCK_K, n0, seg.g);
             }
@@ -421,10 +484,10 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
             if constexpr (kKind == Kind::Masked) {
               tma_load_3d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, kb / 4, seg.g);
             } else {
-              tma_load_2d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, kb / 4);
+              tma_load_2d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, seg.sf_row + kb / 4);
             }
-            if constexpr (kKind == Kind::Dense) {
-              tma_load_2d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, kb / 4);
+            if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
+              tma_load_2d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, seg.sf_row + kb / 4);
             } else {
               tma_load_3d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, kb / 4, seg.g);
             }
@@ -745,7 +808,11 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tm_d, sbuf, n0 + hcol, seg.m_blk * BLOCK_M + quad * 32);
+              if constexpr (kKind == Kind::KGrouped) {
+                tma_store_3d(&tm_d, sbuf, n0 + hcol, seg.m_blk * BLOCK_M + quad * 32, seg.g);
+              } else {
+                tma_store_2d(&tm_d, sbuf, n0 + hcol, seg.m_blk * BLOCK_M + quad * 32);
+              }
               bulk_commit_group();
             }
           }
@@ -813,14 +880,21 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
       };
 
       if (seg.n_contrib == 1) {
+        // a K-grouped expert without tokens has no MMAs: its accumulator is zero, not TMEM
+        const bool empty = kKind == Kind::KGrouped && seg.kb_end <= seg.kb_begin;
 #pragma unroll 1
         for (int ch = 0; ch < kChunks; ++ch) {
           const int col = col_part * C::kColsPerEpiWarp + ch * 64;   // column within the tile
           uint32_t v0[32], v1[32];
           const uint32_t taddr = tmem_base + t_lane + acc * BN + col;
-          tmem_load_32x32b_x32(taddr, v0);
-          tmem_load_32x32b_x32(taddr + 32, v1);
-          tmem_load_wait();
+          if (!empty) {
+            tmem_load_32x32b_x32(taddr, v0);
+            tmem_load_32x32b_x32(taddr + 32, v1);
+            tmem_load_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0u;
+          }
           if (ch == kChunks - 1) {
             // this warp has read its whole share of the accumulator: hand it back
             tc_fence_before();

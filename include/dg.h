@@ -85,6 +85,31 @@ dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const
                                         const float* c, float* d, int M, int N, int K, cudaStream_t stream);
 
 /*
+ * K-grouped weight-gradient GEMM for MoE experts, FP32 output (page "Weight gradient kernels
+ * for dense and MoE models #95": k_grouped_wgrad_gemm_fp8_fp8_fp32_nt; README "Grouped GEMMs":
+ * the K-axis-grouped API, M and N fixed). Expert g owns the K-slice [off_g, off_g + ks[g]) of
+ * A and B, off_g = ks[0] + ... + ks[g-1], and D[g] = C[g] + A[:, slice_g] @ B[:, slice_g].T.
+ *   a   : e4m3 [M, K_total] row-major (the experts' token columns concatenated along K).
+ *   sfa : int32 [sf_k_rows][ceil4(M)] UE8M0 words packed per expert: expert g's K-groups
+ *         j = 0, 1, ... in byte j % 4 of word row R_g + j / 4, R_g = sum over h < g of
+ *         ceil(ks[h] / 512) (each expert starts a new word row).
+ *   b   : e4m3 [N, K_total] row-major; sfb : int32 [sf_k_rows][ceil4(ceil(N/128))], the same
+ *         per-expert packing over 128 x 128 blocks.
+ *   c   : float32 [G, M, N] or NULL; may alias d.   d : float32 [G, M, N].
+ *   ks  : DEVICE int32 [G], each a non-negative multiple of 128, summing to K_total; an
+ *         expert with ks[g] = 0 gets D[g] = C[g] (zero without C).
+ *   sf_k_rows : word rows of sfa / sfb (= sum over g of ceil(ks[g] / 512)).
+ * Synchronous errors: G <= 0, M < 0, N not a positive multiple of 16, K_total not a
+ * multiple of 128, null or misaligned pointers -> DG_ERR_INVALID_ARG / DG_ERR_MISALIGNED.
+ * Device-detected: ks values that are negative, not multiples of 128, do not sum to K_total
+ * or do not match sf_k_rows set DG_ERR_BAD_INDEX (reads stay within the declared extents).
+ */
+dg_status dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const void* b,
+                                                const int32_t* sfb, const float* c, float* d, const int32_t* ks,
+                                                int G, int M, int N, int K_total, int sf_k_rows,
+                                                cudaStream_t stream);
+
+/*
  * M-grouped GEMM, contiguous layout ("Grouped GEMMs (contiguous layout)":
  * m_grouped_fp8_gemm_nt_contiguous). Only M is grouped; N and K are shared by the G
  * experts. Each expert's token rows are concatenated along M, and each expert segment

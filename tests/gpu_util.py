@@ -55,6 +55,19 @@ def run_wgrad(lib, p: W.Wgrad, in_place: bool = False) -> torch.Tensor:
     return d
 
 
+def run_k_grouped(lib, p: W.KGrouped, in_place: bool = False) -> torch.Tensor:
+    """FP32 D[g] = C[g] + A_g @ B_g.T per expert; with in_place, D is the C buffer itself."""
+    c = dev(p.c) if p.c is not None else None
+    if in_place and c is not None:
+        d = c
+    else:
+        d = torch.full((p.G, p.M, p.N), float("nan"), dtype=torch.float32).cuda()
+    lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), c, d,
+                                                dev(np.asarray(p.ks, np.int32)))
+    torch.cuda.synchronize()
+    return d
+
+
 def run_contiguous(lib, p: W.Contiguous) -> torch.Tensor:
     d = sentinel_like((p.M_total, p.N))
     lib.dg_m_grouped_fp8_gemm_nt_contiguous(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d, dev(p.m_indices))

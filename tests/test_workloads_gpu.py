@@ -12,8 +12,8 @@ import torch
 
 import oracle as O
 import workloads as W
-from gpu_util import (SENTINEL, assert_parity, bf16_bits, bf16_f64, run_contiguous, run_dense, run_masked,
-                      run_wgrad)
+from gpu_util import (SENTINEL, assert_parity, bf16_bits, bf16_f64, run_contiguous, run_dense, run_k_grouped,
+                      run_masked, run_wgrad)
 
 pytestmark = pytest.mark.gpu
 
@@ -87,4 +87,18 @@ def test_wgrad_workload(lib):
     ref = O.wgrad_gemm_fp8_fp8_fp32_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K, rows=rows)
     assert_parity(d[rows], ref, name)
     assert np.isfinite(d).all()
+    assert lib.dg_get_device_status() == 0
+
+
+def test_k_grouped_workload(lib):
+    name = "k_grouped_wgrad_g4_m4096_n7168_t16384"
+    p = W.make_workload(name)
+    d = run_k_grouped(lib, p)
+    rows = _rows(p.M, 24, 5)
+    groups = [0, p.G - 1]
+    ref = O.k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.ks, p.M, p.N, groups=groups, rows=rows)
+    got = d[groups].cpu().numpy().astype(np.float64)[:, rows]
+    for i, g in enumerate(groups):
+        assert_parity(got[i], ref[i], f"{name} expert {g}")
+    assert torch.isfinite(d).all()
     assert lib.dg_get_device_status() == 0
