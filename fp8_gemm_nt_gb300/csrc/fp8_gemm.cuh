@@ -49,6 +49,7 @@ enum : int { kFaultNone = 0, kFaultProducerSilent = 1 };
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_K = 128;   // one scale group per pipeline stage
 constexpr int SF_BLOCK_N = 128;
+constexpr int kPrefetchKGroups = 4;   // K-groups of the first segment prefetched into L2 at launch
 
 struct Params {
   int M;   // dense: M; contiguous: M_total; masked: max_m (rows per group)
@@ -436,7 +437,23 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
   const uint32_t tmem_base = *tmem_slot;
   // With programmatic dependent launch this kernel may start while the previous one in the
   // stream is finishing: everything above overlapped it; nothing below may read or write
-  // global memory before that grid has completed.
+  // global memory before that grid has completed. The one exception: the dense forms ask L2
+  // for the first K-groups of their first segment's A and B boxes now. A prefetch into L2
+  // returns nothing to this SM and L2 is the point of coherence, so a load issued after
+  // the wait still sees any write the previous grid makes to those bytes.
+  if constexpr (kKind == Kind::Dense) {
+    if (warp == 0 && lane == 0) {
+      Scheduler<kKind, BN, kKG, kSplit> first(p);   // the dense schedule reads no global memory
+      Segment s0;
+      if (first.next(p, s0)) {
+        const int kb_end = s0.kb_begin + kPrefetchKGroups < s0.kb_end ? s0.kb_begin + kPrefetchKGroups : s0.kb_end;
+        for (int kb = s0.kb_begin; kb < kb_end; ++kb) {
+          tma_prefetch_l2_2d(&tm_a, kb * BLOCK_K, s0.m_blk * BLOCK_M);
+          tma_prefetch_l2_2d(&tm_b, kb * BLOCK_K, s0.n_blk * BN);
+        }
+      }
+    }
+  }
   grid_dependency_wait();
 
   auto on_timeout = [&]() {
