@@ -367,11 +367,13 @@ constexpr int kEpilogueWarps = 4;
 // with one accumulator, BN = 240 or 192 with two.
 constexpr int kPairStages = 5;
 
-template <dg::Kind kKind, bool kHasC, int kBN>
+template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false>
 struct PairLauncher {
   static constexpr int kNumAccum = kBN == 256 ? 1 : 2;
   using Cfg = dg::PairConfig<kPairStages, kBN, kNumAccum>;
-  static constexpr auto kernel() { return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kBN, kNumAccum, kHasC>; }
+  static constexpr auto kernel() {
+    return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kBN, kNumAccum, kHasC, kOutF32>;
+  }
 
   // Largest number of co-resident CTA pairs (0 if the device cannot run the kernel).
   static int max_clusters() {
@@ -516,7 +518,7 @@ bool map_out_f32(CUtensorMap* m, void* base, int rows, int N) {
 
 // Dense / contiguous GEMM on CTA pairs: converts the scale words into tcgen05.cp chunks in
 // the stream workspace (two small kernels), then launches the pair kernel.
-template <dg::Kind kKind, bool kHasC, int kBN>
+template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false>
 dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d,
                    dg::Params p, int clusters, cudaStream_t stream) {
   const int KP = ceil_div(p.K / 128, 4);
@@ -563,14 +565,16 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   }
 
   CUtensorMap ta, tb, tsa, tsb, td, td_tail;
-  bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) && map_out(&td, d, 0, p.M, p.N);
+  bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) && (kOutF32 ? map_out_f32(&td, d, p.M, p.N) : map_out(&td, d, 0, p.M, p.N));
   if constexpr (kBN % 64 != 0) {
-    // the narrower last chunk of each tile: kBN % 64 columns x 32 rows, no swizzle
+    // the narrower end of each tile, 32 rows high, no swizzle: BF16 its last kBN % 64
+    // columns; FP32 its last (kBN % 64) % 32 columns (the rest goes out as 32-column boxes)
     const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(p.N) * 2};
-    const uint32_t box[2] = {static_cast<uint32_t>(kBN % 64), 32};
-    ok = ok && make_map(&td_tail, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    const uint64_t strides[1] = {static_cast<uint64_t>(p.N) * (kOutF32 ? 4 : 2)};
+    const uint32_t box[2] = {static_cast<uint32_t>(kOutF32 ? (kBN % 64) % 32 : kBN % 64), 32};
+    static_assert(!kOutF32 || (kBN % 64) % 32 != 0, "an FP32 narrow box needs a remainder");
+    ok = ok && make_map(&td_tail, kOutF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d,
+                        dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     td_tail = td;
   }
@@ -590,15 +594,16 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   if (!ok) return DG_ERR_CUDA;
   p.sf_num_mb = num_mb;
   p.sf_nb = sfb_rows;
-  return PairLauncher<kKind, kHasC, kBN>::launch(ta, tb, tsa, tsb, td, td_tail, p, clusters, stream);
+  return PairLauncher<kKind, kHasC, kBN, kOutF32>::launch(ta, tb, tsa, tsb, td, td_tail, p, clusters, stream);
 }
 
 // Pair tile width: DG_PAIR_BN (192, 240 or 256) overrides; 240 is offered for the dense
 // form only. Otherwise the width with the smallest estimated makespan: waves of pair tiles
-// x cycles per tile, from measurements on GB300 -- a K-group costs ~512 cycles at 256
-// columns (tensor-bound) and ~500 at 240 or 192 (bound by the issuing loop: ~125 cycles
-// per MMA with one barrier wait per K-group), and a single accumulator adds ~2300 cycles
-// per tile (the MMAs wait for the epilogue to drain it).
+// x cycles per tile. Cycles per K-group and the single accumulator's per-tile cost (the
+// MMAs wait for the epilogue to drain it) are fitted to GB300 measurements of
+// 4096x24576x1536 (BF16 out: 240 -> 2733, 256 -> 2340, 192 -> 2312 TFLOPS) and
+// 7168x4096x4096 (FP32 out: 256 -> 2485, 240 -> 2204): ~512 cycles per K-group at 256
+// columns (tensor-bound) + ~2000 per tile, ~556 at 240 and ~535 at 192 (issue-bound).
 int pick_pair_bn(long long pair_rows, int N, int K, int clusters, bool dense) {
   if (const char* f = std::getenv("DG_PAIR_BN")) {
     const int v = std::atoi(f);
@@ -608,7 +613,7 @@ int pick_pair_bn(long long pair_rows, int N, int K, int clusters, bool dense) {
   auto makespan = [&](int bn) {
     const long long tiles = pair_rows * ceil_div(N, bn);
     const long long waves = ceil_div(tiles, static_cast<long long>(std::max(clusters, 1)));
-    const long long per_tile = bn == 256 ? kb * 512 + 2300 : kb * 500;
+    const long long per_tile = bn == 256 ? kb * 512 + 2000 : kb * (bn == 240 ? 556 : 535);
     return waves * per_tile;
   };
   int best = 256;
@@ -620,7 +625,7 @@ int pick_pair_bn(long long pair_rows, int N, int K, int clusters, bool dense) {
 }
 
 // Launches the pair kernel for kKind if the device can run it; *launched tells whether it did.
-template <dg::Kind kKind>
+template <dg::Kind kKind, bool kOutF32 = false>
 dg_status try_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
                    const void* c, void* d, dg::Params pp, long long pair_rows, int sms, cudaStream_t stream,
                    bool* launched) {
@@ -631,12 +636,12 @@ dg_status try_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   constexpr bool kDense = kKind == dg::Kind::Dense;
   constexpr int kWideBN = kDense ? 240 : 192;     // the 240-wide configuration is dense-only
   const bool with_c = kDense && c != nullptr;
-  const int max_cl = std::min({with_c ? PairLauncher<kKind, kDense, 256>::max_clusters()
-                                      : PairLauncher<kKind, false, 256>::max_clusters(),
-                               with_c ? PairLauncher<kKind, kDense, 192>::max_clusters()
-                                      : PairLauncher<kKind, false, 192>::max_clusters(),
-                               with_c ? PairLauncher<kKind, kDense, kWideBN>::max_clusters()
-                                      : PairLauncher<kKind, false, kWideBN>::max_clusters()});
+  const int max_cl = std::min({with_c ? PairLauncher<kKind, kDense, 256, kOutF32>::max_clusters()
+                                      : PairLauncher<kKind, false, 256, kOutF32>::max_clusters(),
+                               with_c ? PairLauncher<kKind, kDense, 192, kOutF32>::max_clusters()
+                                      : PairLauncher<kKind, false, 192, kOutF32>::max_clusters(),
+                               with_c ? PairLauncher<kKind, kDense, kWideBN, kOutF32>::max_clusters()
+                                      : PairLauncher<kKind, false, kWideBN, kOutF32>::max_clusters()});
   if (max_cl <= 0) return DG_OK;
   const int cl_cap = std::min(max_cl, sms / 2);
   const int bn = pick_pair_bn(pair_rows, pp.N, pp.K, cl_cap, kDense);
@@ -644,15 +649,15 @@ dg_status try_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   const int clusters = static_cast<int>(std::min<long long>(cl_cap, pair_tiles));
   *launched = true;
   if (bn == 240) {
-    if (with_c) return run_pair<kKind, kDense, kWideBN>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
-    return run_pair<kKind, false, kWideBN>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    if (with_c) return run_pair<kKind, kDense, kWideBN, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    return run_pair<kKind, false, kWideBN, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
   }
   if (bn == 256) {
-    if (with_c) return run_pair<kKind, kDense, 256>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
-    return run_pair<kKind, false, 256>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    if (with_c) return run_pair<kKind, kDense, 256, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    return run_pair<kKind, false, 256, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
   }
-  if (with_c) return run_pair<kKind, kDense, 192>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
-  return run_pair<kKind, false, 192>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+  if (with_c) return run_pair<kKind, kDense, 192, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+  return run_pair<kKind, false, 192, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
 }
 
 dg_status check_common(int N, int K) {
@@ -845,6 +850,22 @@ dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
   const int sms = sms_to_use(*ds);
   const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
+  if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
+    dg::Params pp{};
+    pp.M = M;
+    pp.N = N;
+    pp.K = K;
+    pp.G = 1;
+    pp.c = reinterpret_cast<const __nv_bfloat16*>(c);   // FP32 in this form (the kernel reinterprets)
+    pp.d = reinterpret_cast<__nv_bfloat16*>(d);
+    pp.status = ds->status;
+    pp.timeout_ns = wait_timeout_ns();
+    pp.fault = g_fault.load();
+    bool launched = false;
+    const dg_status s = try_pair<dg::Kind::Dense, true>(*ds, a, sfa, b, sfb, c, d, pp, ceil_div(M, 256), sms, stream,
+                                                        &launched);
+    if (launched) return s;
+  }
   // Tile mode: 192-wide tiles with two accumulators, so that the FP32 epilogue (twice the
   // bytes of the BF16 one, plus the C read) overlaps the next tile's MMAs (measured on GB300,
   // 7168x4096x4096 accumulated in place: 1916 TFLOPS at 192 vs 1736 at 256 and 1650 at 128).

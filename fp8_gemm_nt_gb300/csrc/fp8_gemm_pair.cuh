@@ -165,7 +165,8 @@ struct PairScheduler {
   }
 };
 
-template <Kind kKind, int kStages, int kBN, int kNumAccum, bool kHasC>
+// kOutF32: FP32 C / D (the dense weight-gradient form), else BF16.
+template <Kind kKind, int kStages, int kBN, int kNumAccum, bool kHasC, bool kOutF32 = false>
 __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
                          const Params p) {
   static_assert(kKind != Kind::Masked, "the masked form uses the single-CTA kernel");
   static_assert(kKind == Kind::Dense || kBN % 64 == 0, "narrow last chunks: dense form only");
+  static_assert(!kOutF32 || kKind == Kind::Dense, "FP32 output: dense form only");
   using C = PairConfig<kStages, kBN, kNumAccum>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -465,6 +467,51 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
         float f[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) f[i] = __uint_as_float(vc[i]);
+        if constexpr (kOutF32) {
+          // FP32: 32-column halves, one 128-byte swizzled TMA box each (tm_d); a 16-column
+          // half (the end of a 240-wide tile) as plain 64-byte rows (tm_d_tail)
+          const float* cbase = reinterpret_cast<const float*>(p.c);
+          const int width = tail ? C::kTail : 64;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int hw = width - 32 * h < 32 ? width - 32 * h : 32;
+            if (hw <= 0) break;
+            const int hcol = col + 32 * h;
+            if constexpr (kHasC) {
+              if (row_ok) {
+                const float* crow = cbase + d_row * p.N + n0 + hcol;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  if (4 * q < hw && n0 + hcol + 4 * q < p.N) {
+                    const uint4 cv = ld_global_nc_v4(crow + 4 * q);
+                    f[32 * h + 4 * q + 0] = __uint_as_float(cv.x) + f[32 * h + 4 * q + 0];
+                    f[32 * h + 4 * q + 1] = __uint_as_float(cv.y) + f[32 * h + 4 * q + 1];
+                    f[32 * h + 4 * q + 2] = __uint_as_float(cv.z) + f[32 * h + 4 * q + 2];
+                    f[32 * h + 4 * q + 3] = __uint_as_float(cv.w) + f[32 * h + 4 * q + 3];
+                  }
+                }
+              }
+            }
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
+            const bool narrow = hw < 32;
+            const uint32_t srow = smem_addr(sbuf) + lane * (narrow ? 64 : 128);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if (4 * u < hw)
+                st_shared_v4(srow + (narrow ? u * 16 : (u ^ (lane & 7)) * 16), __float_as_uint(f[32 * h + 4 * u]),
+                             __float_as_uint(f[32 * h + 4 * u + 1]), __float_as_uint(f[32 * h + 4 * u + 2]),
+                             __float_as_uint(f[32 * h + 4 * u + 3]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(narrow ? &tm_d_tail : &tm_d, sbuf, n0 + hcol, m_blk * BLOCK_M + quad * 32);
+              bulk_commit_group();
+            }
+          }
+          continue;
+        }
         if constexpr (kHasC) {
           if (row_ok) {
             const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;

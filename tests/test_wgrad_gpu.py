@@ -82,3 +82,22 @@ def test_wgrad_identity_exact(lib):
                 None, M, N, K)
     d = run_wgrad(lib, p).cpu().numpy().astype(np.float64)
     assert np.array_equal(d, O.decode_e4m3(b[:, :M]).T)
+
+
+@pytest.mark.parametrize("pair_bn", [256, 240, 192])
+@pytest.mark.parametrize("M,N,K,with_c", [
+    (512, 496, 640, True),     # N = 2 x 240 + 16: the 240-wide tile's 16-column FP32 box lies past N
+    (384, 768, 1152, False),   # an odd number of 128-row blocks
+])
+def test_wgrad_pair(lib, monkeypatch, pair_bn, M, N, K, with_c):
+    # the CTA-pair kernel with its FP32 epilogue (the SM cap makes these shapes tile-mode)
+    monkeypatch.setenv("DG_PAIR_BN", str(pair_bn))
+    lib.dg_set_num_sms(8)
+    try:
+        p = W.make_wgrad(M, N, K, seed=850 + M + N + K + pair_bn, with_c=with_c)
+        d = run_wgrad(lib, p).cpu().numpy().astype(np.float64)
+    finally:
+        lib.dg_set_num_sms(0)
+    ref = O.wgrad_gemm_fp8_fp8_fp32_nt(p.a, p.sfa, p.b, p.sfb, p.c, M, N, K)
+    rep = assert_parity(d, ref, f"wgrad pair {pair_bn} {M}x{N}x{K}")
+    assert rep["max_err"] <= 1e-5 * rep["rms"], rep
