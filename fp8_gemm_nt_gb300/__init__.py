@@ -36,6 +36,8 @@ SIGNATURES = [
     ("dg_m_grouped_fp8_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_pack_sf_ue8m0", _I, [_P, _P, _I, _I, _P]),
     ("dg_get_mk_alignment_for_contiguous_layout", _I, []),
+    ("dg_set_mk_alignment_for_contiguous_layout", _I, [_I]),
+    ("dg_get_theoretical_mk_alignment_for_contiguous_layout", _I, []),
     ("dg_get_tma_aligned_size", _I, [_I, _I]),
     ("dg_set_num_sms", _I, [_I]),
     ("dg_get_num_sms", _I, []),
@@ -224,6 +226,16 @@ def dg_pack_sf_ue8m0(sf: torch.Tensor, out: Optional[torch.Tensor] = None, strea
 
 def dg_get_mk_alignment_for_contiguous_layout() -> int:
     return load_library().dg_get_mk_alignment_for_contiguous_layout()
+
+
+def dg_set_mk_alignment_for_contiguous_layout(alignment: int) -> None:
+    """Set the segment alignment callers are told to pad to (a positive multiple of 128)."""
+    _check("dg_set_mk_alignment_for_contiguous_layout",
+           load_library().dg_set_mk_alignment_for_contiguous_layout(int(alignment)))
+
+
+def dg_get_theoretical_mk_alignment_for_contiguous_layout() -> int:
+    return load_library().dg_get_theoretical_mk_alignment_for_contiguous_layout()
 
 
 def dg_get_tma_aligned_size(mn: int, elem_bytes: int) -> int:

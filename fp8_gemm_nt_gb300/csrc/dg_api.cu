@@ -21,6 +21,7 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_num_sms_cap{0};
+std::atomic<int> g_mk_alignment{128};   // what callers are told to pad expert segments to
 std::atomic<int> g_fault{0};
 std::atomic<unsigned long long> g_timeout_ns{0};
 
@@ -1035,7 +1036,15 @@ dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgrou
   return e == cudaSuccess ? DG_OK : cuda_fail(e);
 }
 
-int dg_get_mk_alignment_for_contiguous_layout(void) { return dg::BLOCK_M; }
+int dg_get_mk_alignment_for_contiguous_layout(void) { return g_mk_alignment.load(); }
+
+dg_status dg_set_mk_alignment_for_contiguous_layout(int alignment) {
+  if (alignment <= 0 || alignment % dg::BLOCK_M != 0 || alignment > (1 << 20)) return DG_ERR_INVALID_ARG;
+  g_mk_alignment.store(alignment);
+  return DG_OK;
+}
+
+int dg_get_theoretical_mk_alignment_for_contiguous_layout(void) { return dg::BLOCK_M; }
 
 int dg_get_tma_aligned_size(int mn, int elem_bytes) {
   if (mn < 0 || (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)) return -1;

@@ -197,8 +197,16 @@ dg_status dg_fp8_gemm_nt_no_alloc(const void* a, const int32_t* sfa,
                                   const void* c, void* d, uint32_t* status,
                                   int M, int N, int K, cudaStream_t stream);
 
-/* Row alignment of each expert segment in the contiguous layout (the M block): 128. */
+/* Row (M) alignment of each expert segment in the contiguous layout, and K alignment of each
+ * expert slice in the K-grouped form, that callers should pad to (README "Utilities":
+ * set/get_mk_alignment_for_contiguous_layout). Default 128. The setter accepts positive
+ * multiples of 128 up to 2^20 (the kernels accept any multiple of 128, so a larger value
+ * only changes what callers are told to pad to) and returns DG_ERR_INVALID_ARG otherwise;
+ * process-wide. The theoretical minimum ("get_theoretical_mk_alignment_for_contiguous_layout")
+ * is the kernels' M block, 128. Host-only: no device is touched. */
 int dg_get_mk_alignment_for_contiguous_layout(void);
+dg_status dg_set_mk_alignment_for_contiguous_layout(int alignment);
+int dg_get_theoretical_mk_alignment_for_contiguous_layout(void);
 
 /* Smallest MN extent >= mn whose size in bytes is a multiple of 16 ("get_tma_aligned_size").
  * elem_bytes must be 1, 2, 4 or 8; returns -1 on a bad argument. */

@@ -80,3 +80,31 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert lib.dg_m_grouped_fp8_gemm_nt_masked(x, x, x, x, x, x, 4, -1, 128, 128, None) == INVALID
     assert lib.dg_m_grouped_fp8_gemm_nt_contiguous(x, x, x, x, x, P(0x10002), 128, 128, 128, 2, None) == MISALIGNED
     assert lib.dg_pack_sf_ue8m0(None, x, 4, 4, None) == INVALID
+
+
+def test_mk_alignment_setter(lib):
+    try:
+        assert lib.dg_get_theoretical_mk_alignment_for_contiguous_layout() == 128
+        assert lib.dg_set_mk_alignment_for_contiguous_layout(256) == 0
+        assert lib.dg_get_mk_alignment_for_contiguous_layout() == 256
+        for bad in (0, -128, 100, 192 + 1, 1 << 21):
+            assert lib.dg_set_mk_alignment_for_contiguous_layout(bad) == 1
+        assert lib.dg_get_mk_alignment_for_contiguous_layout() == 256
+    finally:
+        assert lib.dg_set_mk_alignment_for_contiguous_layout(128) == 0
+    assert lib.dg_get_mk_alignment_for_contiguous_layout() == 128
+
+
+def test_weight_gradient_forms_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    x = P(0x10000)
+    INVALID, MISALIGNED = 1, 3
+    assert lib.dg_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, None, None, 128, 128, 128, None) == INVALID
+    assert lib.dg_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, None, x, 128, 120, 128, None) == INVALID
+    assert lib.dg_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, P(0x10004), x, 128, 128, 128, None) == MISALIGNED
+    # K-grouped: G <= 0, K_total not a multiple of 128, null ks, misaligned ks
+    assert lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, None, x, x, 0, 128, 128, 128, 1, None) == INVALID
+    assert lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, None, x, x, 2, 128, 128, 100, 1, None) == INVALID
+    assert lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, None, x, None, 2, 128, 128, 128, 1, None) == INVALID
+    assert lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, None, x, P(0x10002), 2, 128, 128, 128, 1,
+                                                       None) == MISALIGNED

@@ -229,3 +229,29 @@ def test_pack_sf_matches_layout(lib):
     torch.cuda.synchronize()
     e2 = np.where(e >= 254, e, e + 1).astype(np.uint8)
     assert np.array_equal(out2.cpu().numpy(), W.pack_sf(e2))
+
+
+def test_masked_graph_replay_reads_counts_on_the_device(lib):
+    # the masked form is captured once into a CUDA graph; replays pick up new per-expert
+    # counts written to device memory (the CPU never learns them), as the pages intend for
+    # decoding with CUDA graphs
+    p = W.make_masked(G=4, max_m=256, N=384, K=512, seed=61, masked_m=[256, 0, 100, 3])
+    a, sfa, b, sfb = dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb)
+    mm = dev(p.masked_m.astype(np.int32))
+    d = sentinel_like((p.G, p.max_m, p.N))
+    lib.dg_m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, d, mm)          # outside capture: lazy set-up
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        lib.dg_m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, d, mm)
+    for counts in ([17, 256, 0, 129], [0, 0, 0, 1], [256, 256, 256, 256]):
+        counts = np.array(counts, np.int32)
+        mm.copy_(torch.from_numpy(counts))
+        d.view(torch.int16).fill_(SENTINEL - 65536 if SENTINEL >= 32768 else SENTINEL)
+        graph.replay()
+        torch.cuda.synchronize()
+        ref, valid = O.m_grouped_fp8_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, counts, p.G, p.max_m, p.N, p.K)
+        bits = bf16_bits(d)
+        assert (bits[~valid] == SENTINEL).all(), counts
+        assert_parity(bf16_f64(d)[valid], ref[valid], f"graph replay {counts.tolist()}")
