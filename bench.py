@@ -362,7 +362,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
-        return run_reference(args, rank)
+        return run_reference(args, rank, world)
 
     import torch
     torch.cuda.set_device(local_rank)
@@ -389,18 +389,13 @@ def main():
     region_ms, eager_ms = time_steps(torch, prob, args.steps, args.warmup, barrier)
     if L.dg_get_device_status() != 0:
         raise RuntimeError("device status reported an error during the benchmark")
-    t_max = region_ms
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([region_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(region_ms, world, "cuda")
     flops, alg_bytes = algorithmic(p)
     # measured FP8 tensor ceiling (MMA-only kernel on every SM), reported beside the peak;
     # skipped with --headline-only so that profiles of that command show only the timed path
     mma_ceiling = None if args.headline_only else L.dg_measure_fp8_mma_tflops(4096)[0]
     ms_per_step = t_max / args.steps
-    value = world * flops * args.steps / (t_max * 1e-3) / 1e12
+    value = job_tflops(world, flops, args.steps, t_max)
     kern_ms = region_ms / args.steps
     achieved_gbs = alg_bytes / (kern_ms * 1e-3) / 1e9
 
@@ -502,8 +497,27 @@ def profile_case(name, launches):
     print(f"profile-case {name}: {launches} launches ok")
 
 
-def run_reference(args, rank):
-    """The CPU oracle timed on the headline workload, each step a bounded sample."""
+def max_over_ranks(value: float, world: int, device: str) -> float:
+    """The largest of every rank's value (a timed region): one all-reduce MAX over the
+    process group (NCCL on GPUs, gloo on CPUs); the value itself with one rank."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, t_max_ms: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of `flops_per_step` (weak scaling),
+    and the job takes as long as its slowest rank."""
+    return world * flops_per_step * steps / (t_max_ms * 1e-3) / 1e12
+
+
+def run_reference(args, rank, world=1):
+    """The CPU oracle timed on the headline workload, each step a bounded sample. Under a
+    multi-rank launch rank 0 alone runs and prints; the other ranks return at once."""
     if rank != 0:
         return
     import oracle as O
@@ -521,7 +535,7 @@ def run_reference(args, rank):
     value = flops_step * args.steps / el / 1e12
     sample = f"{rows_per_step} output rows x all N={p.N} columns of {HEADLINE} per step, FP64 numpy/OpenBLAS"
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded PCG64)", "config": {"workload": HEADLINE, "M": p.M, "N": p.N, "K": p.K},
