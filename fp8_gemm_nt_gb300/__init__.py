@@ -31,6 +31,9 @@ _I = ctypes.c_int
 SIGNATURES = [
     ("dg_fp8_gemm_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("dg_wgrad_gemm_fp8_fp8_fp32_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("dg_fp8_gemm_nn", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("dg_fp8_gemm_tn", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("dg_fp8_gemm_tt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
@@ -132,6 +135,37 @@ def dg_fp8_gemm_nt(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:
     _check("dg_fp8_gemm_nt", lib.dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                                                 M, N, K, _stream(stream)))
     return d
+
+
+def _dense_layout(name, a_kmajor, b_kmajor, a, sfa, b, sfb, c, d, stream):
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d")
+    M, K = a.shape if a_kmajor else a.shape[::-1]
+    N = b.shape[0] if b_kmajor else b.shape[1]
+    Kb = b.shape[1] if b_kmajor else b.shape[0]
+    _need(Kb == K and tuple(d.shape) == (M, N), "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(M, K) and tuple(sfb.shape) == sf_shape(-(-N // 128), K), "scale shape mismatch")
+    if c is not None:
+        _bf16(c, "c")
+        _need(tuple(c.shape) == (M, N), "c shape mismatch")
+    _check(name, getattr(lib, name)(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d), M, N, K,
+                                    _stream(stream)))
+    return d
+
+
+def dg_fp8_gemm_nn(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:
+    """D = C + A @ B with a [M, K] (K-major) and b [K, N] (N-major); scales as dg_fp8_gemm_nt."""
+    return _dense_layout("dg_fp8_gemm_nn", True, False, a, sfa, b, sfb, c, d, stream)
+
+
+def dg_fp8_gemm_tn(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:
+    """D = C + A.T @ B with a [K, M] (M-major, M a multiple of 16) and b [K, N]."""
+    return _dense_layout("dg_fp8_gemm_tn", False, False, a, sfa, b, sfb, c, d, stream)
+
+
+def dg_fp8_gemm_tt(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:
+    """D = C + A.T @ B.T with a [K, M] (M-major, M a multiple of 16) and b [N, K]."""
+    return _dense_layout("dg_fp8_gemm_tt", False, True, a, sfa, b, sfb, c, d, stream)
 
 
 def dg_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:

@@ -211,13 +211,14 @@ inline int ceil4(int x) { return 4 * ceil_div(x, 4); }
 // Kernel configurations
 // ------------------------------------------------------------------------------------
 template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps_, int kEpiBufs, bool kHasC,
-          int kKG = 1, int kSplit = 0, bool kOutF32 = false>
+          int kKG = 1, int kSplit = 0, bool kOutF32 = false, bool kAMN = false, bool kBMN = false>
 struct Launcher {
   static constexpr int kEpiWarps = kEpiWarps_;
   using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>;
   static constexpr int kBN = BN;
   static constexpr auto kernel() {
-    return dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG, kSplit, kOutF32>;
+    return dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG, kSplit, kOutF32,
+                               kAMN, kBMN>;
   }
 
   // Largest number of co-resident clusters of kSplit CTAs (0 if the kernel cannot run).
@@ -347,13 +348,27 @@ int pick_split_bn(int M, int N, int K, int sms, bool with_c) {
 //   192: 4-stage ring, double-buffered accumulators (TMEM 2 x 192 columns)
 //   256: 4-stage ring, single accumulator (TMEM 256 columns; 2 x 256 + scales exceeds 512)
 //   128 x 2: two K-groups per stage (64 KB stages, 3 of them), for HBM-bound stream-K shapes
-template <dg::Kind kKind, bool kHasC, bool kOutF32 = false>
+template <dg::Kind kKind, bool kHasC, bool kOutF32 = false, bool kAMN = false, bool kBMN = false>
 dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                     const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
                     cudaStream_t stream, int kgroups_per_stage = 1) {
   if constexpr (kKind == dg::Kind::Dense) {
     if (kgroups_per_stage == 2 && bn == 128)
-      return Launcher<kKind, 128, 3, 2, 4, 1, kHasC, 2, 0, kOutF32>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+      return Launcher<kKind, 128, 3, 2, 4, 1, kHasC, 2, 0, kOutF32, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, p, grid,
+                                                                                        stream);
+  }
+  if constexpr (kAMN || kBMN) {
+    // the MN-major layouts use 128- and 256-wide tiles (an N-major B tile is whole
+    // 128-column atoms)
+    switch (bn) {
+      case 128:
+        return Launcher<kKind, 128, 5, 2, 4, 2, kHasC, 1, 0, false, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, p, grid,
+                                                                                         stream);
+      case 256:
+        return Launcher<kKind, 256, 4, 1, 4, 1, kHasC, 1, 0, false, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, p, grid,
+                                                                                         stream);
+    }
+    return DG_ERR_INVALID_ARG;
   }
   switch (bn) {
     case 128: return Launcher<kKind, 128, 5, 2, 4, 2, kHasC, 1, 0, kOutF32>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
@@ -506,6 +521,15 @@ bool map_out(CUtensorMap* m, void* base, int G, int rows, int N) {
   const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(N) * 2 * rows};
   const uint32_t box[3] = {64, 32, 1};
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// MN-major operand ("t" A given as [K, M], "n" B given as [K, N]): boxes of 128 K-rows x 128
+// M/N-bytes with 128-byte swizzle; mn must be a multiple of 16 (its row stride in bytes).
+bool map_operand_mn(CUtensorMap* m, const void* base, int mn, int K) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(mn), static_cast<uint64_t>(K)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(mn)};
+  const uint32_t box[2] = {128, 128};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // FP32 output D (and C) of the weight-gradient form: 32 rows x 32 columns (128 bytes) per TMA
@@ -707,13 +731,14 @@ __global__ void pack_sf_kernel(const float* __restrict__ sf, int32_t* __restrict
 
 // Dense GEMM on the single-CTA kernel: whole tiles (tile mode) or, with fewer tiles than
 // SMs, stream-K. kOutF32: FP32 C / D (weight-gradient form), else BF16.
-template <bool kOutF32>
+template <bool kOutF32, bool kAMN = false, bool kBMN = false>
 dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
                            const void* c, void* d, int M, int N, int K, int BN, int sms, cudaStream_t stream) {
   DeviceState* ds = &dsr;
   const int KP = ceil_div(K / 128, 4);
   CUtensorMap ta, tb, tsa, tsb, td;
-  if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_2d(&tb, b, N, K, BN) ||
+  if (!(kAMN ? map_operand_mn(&ta, a, M, K) : map_operand_2d(&ta, a, M, K, 128)) ||
+      !(kBMN ? map_operand_mn(&tb, b, N, K) : map_operand_2d(&tb, b, N, K, BN)) ||
       !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
       !(kOutF32 ? map_out_f32(&td, d, M, N) : map_out(&td, d, 0, M, N)))
     return DG_ERR_CUDA;
@@ -762,8 +787,8 @@ dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, 
   } else {
     kg = 1;   // tile mode: whole tiles, one K-group per stage
   }
-  if (c) return launch_bn<dg::Kind::Dense, true, kOutF32>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
-  return launch_bn<dg::Kind::Dense, false, kOutF32>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
+  if (c) return launch_bn<dg::Kind::Dense, true, kOutF32, kAMN, kBMN>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
+  return launch_bn<dg::Kind::Dense, false, kOutF32, kAMN, kBMN>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
 }
 
 }  // namespace
@@ -837,6 +862,54 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
     }
   }
   return run_dense_single<false>(*ds, a, sfa, b, sfb, c, d, M, N, K, BN, sms, stream);
+}
+
+}  // extern "C"
+
+namespace {
+// fp8_gemm_{nn,tn,tt}: the dense GEMM with A given as [K, M] (kAMN) and/or B as [K, N] (kBMN),
+// on the single-CTA kernel (tile mode or stream-K), 128- or 256-wide tiles.
+template <bool kAMN, bool kBMN>
+dg_status dense_layout_entry(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                             void* d, int M, int N, int K, cudaStream_t stream) {
+  if (M < 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (kAMN && M % 16 != 0) return DG_ERR_INVALID_ARG;   // [K, M] rows must be 16-byte multiples
+  if (M == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d) return DG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d) || (c && !aligned16(c)))
+    return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  const int sms = sms_to_use(*ds);
+  const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
+  int BN = 128;
+  if (tiles128 >= sms) {
+    BN = ceil_div(N, 256) * 256 <= ceil_div(N, 128) * 128 ? 256 : 128;   // the wider unless it wastes columns
+    if (const char* f = std::getenv("DG_FORCE_BN")) {
+      const int v = std::atoi(f);
+      if (v == 128 || v == 256) BN = v;
+    }
+  }
+  return run_dense_single<false, kAMN, kBMN>(*ds, a, sfa, b, sfb, c, d, M, N, K, BN, sms, stream);
+}
+}  // namespace
+
+extern "C" {
+
+dg_status dg_fp8_gemm_nn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                         void* d, int M, int N, int K, cudaStream_t stream) {
+  return dense_layout_entry<false, true>(a, sfa, b, sfb, c, d, M, N, K, stream);
+}
+
+dg_status dg_fp8_gemm_tn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                         void* d, int M, int N, int K, cudaStream_t stream) {
+  return dense_layout_entry<true, true>(a, sfa, b, sfb, c, d, M, N, K, stream);
+}
+
+dg_status dg_fp8_gemm_tt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                         void* d, int M, int N, int K, cudaStream_t stream) {
+  return dense_layout_entry<true, false>(a, sfa, b, sfb, c, d, M, N, K, stream);
 }
 
 dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,

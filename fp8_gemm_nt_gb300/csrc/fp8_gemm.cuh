@@ -376,9 +376,14 @@ __device__ __forceinline__ float4 ld_global_cg_v4f(const float* p) {
 }
 
 // kOutF32: C and D are FP32 (the weight-gradient form, D = C + A @ B.T accumulated in FP32);
-// otherwise BF16.
+// otherwise BF16. kAMN / kBMN: A given as [K, M] / B given as [K, N] (M- / N-major: the
+// "t" A and "n" B layouts of fp8_gemm_{nn,tn,tt}); otherwise K-major [M, K] / [N, K].
+// An MN-major operand arrives as 128 x 128-byte boxes (128 K-rows of 128 M/N-bytes, 128-byte
+// swizzle) stacked along M/N every 16 KB; its smem descriptor takes LBO = 16 KB (stride
+// between 128-byte atoms along M/N) and SBO = 1024 (stride between 8-row groups along K),
+// and each 32-deep K step of the MMA advances it by 32 rows = 4 KB.
 template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC, int kKG = 1,
-          int kSplit = 0, bool kOutF32 = false>
+          int kSplit = 0, bool kOutF32 = false, bool kAMN = false, bool kBMN = false>
 __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
@@ -388,6 +393,8 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
   static_assert(!kOutF32 || ((kKind == Kind::Dense || kKind == Kind::KGrouped) && kSplit == 0),
                 "FP32 output: dense (tile mode / stream-K) and K-grouped forms only");
   static_assert(kKind != Kind::KGrouped || (kOutF32 && kKG == 1), "the K-grouped form writes FP32, one K-group per stage");
+  static_assert((!kAMN && !kBMN) || (kKind == Kind::Dense && kSplit == 0 && !kOutF32), "MN-major operands: dense BF16");
+  static_assert(!kBMN || BN % 128 == 0, "an N-major B tile is whole 128-column atoms");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -448,8 +455,17 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
       if (first.next(p, s0)) {
         const int kb_end = s0.kb_begin + kPrefetchKGroups < s0.kb_end ? s0.kb_begin + kPrefetchKGroups : s0.kb_end;
         for (int kb = s0.kb_begin; kb < kb_end; ++kb) {
-          tma_prefetch_l2_2d(&tm_a, kb * BLOCK_K, s0.m_blk * BLOCK_M);
-          tma_prefetch_l2_2d(&tm_b, kb * BLOCK_K, s0.n_blk * BN);
+          if constexpr (kAMN) {
+            tma_prefetch_l2_2d(&tm_a, s0.m_blk * BLOCK_M, kb * BLOCK_K);
+          } else {
+            tma_prefetch_l2_2d(&tm_a, kb * BLOCK_K, s0.m_blk * BLOCK_M);
+          }
+          if constexpr (kBMN) {
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h) tma_prefetch_l2_2d(&tm_b, s0.n_blk * BN + 128 * h, kb * BLOCK_K);
+          } else {
+            tma_prefetch_l2_2d(&tm_b, kb * BLOCK_K, s0.n_blk * BN);
+          }
         }
       }
     }
@@ -488,10 +504,16 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
           for (int j = 0; j < kKG; ++j) {
             if constexpr (kKind == Kind::Masked) {
               tma_load_3d(sa + j * C::A_SUB, &tm_a, fb, (kb + j) * BLOCK_K, row0, seg.g);
+            } else if constexpr (kAMN) {
+              tma_load_2d(sa + j * C::A_SUB, &tm_a, fb, row0, (kb + j) * BLOCK_K);
             } else {
               tma_load_2d(sa + j * C::A_SUB, &tm_a, fb, (seg.k_base + kb + j) * BLOCK_K, row0);
             }
-            if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
+            if constexpr (kBMN) {
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
+                tma_load_2d(sb + j * C::B_SUB + h * (128 * BLOCK_K), &tm_b, fb, n0 + 128 * h, (kb + j) * BLOCK_K);
+            } else if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
               tma_load_2d(sb + j * C::B_SUB, &tm_b, fb, (seg.k_base + kb + j) * BLOCK_K, n0);
             } else {
               tma_load_3d(sb + j * C::B_SUB, &tm_b, fb, (kb + j) * BLOCK_K, n0, seg.g);
@@ -532,9 +554,16 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     // GB300: each tcgen05.mma issue costs ~75 cycles and a warp-wide wait path ~400, so the
     // loop, not the tensor pipe, set the pace).
     if (lane == 0) {
-      constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(BLOCK_M, BN);
-      const uint64_t a_desc0 = make_smem_desc(smem_addr(smem + C::OFF_A), 16, 1024, kLayoutSwizzle128B);
-      const uint64_t b_desc0 = make_smem_desc(smem_addr(smem + C::OFF_B), 16, 1024, kLayoutSwizzle128B);
+      constexpr uint32_t kIdesc =
+          make_idesc_mxf8_e4m3(BLOCK_M, BN) | (kAMN ? 1u << 15 : 0u) | (kBMN ? 1u << 16 : 0u);
+      const uint64_t a_desc0 =
+          make_smem_desc(smem_addr(smem + C::OFF_A), kAMN ? 128 * BLOCK_K : 16, 1024, kLayoutSwizzle128B);
+      const uint64_t b_desc0 =
+          make_smem_desc(smem_addr(smem + C::OFF_B), kBMN ? 128 * BLOCK_K : 16, 1024, kLayoutSwizzle128B);
+      // descriptor steps (address >> 4) per 32-deep K step: 32 bytes along a K-major row, or
+      // 32 rows of 128 bytes down an MN-major box
+      constexpr uint64_t kAStep = kAMN ? (32 * 128) >> 4 : 2;
+      constexpr uint64_t kBStep = kBMN ? (32 * 128) >> 4 : 2;
       const uint64_t sf_desc0 = make_smem_desc(smem_addr(smem + C::OFF_SF), 0, 128, kLayoutNone);
       uint32_t stage = 0, phase = 0, seg_iter = 0, sf_iter = 0, sf_parity = 0;
       while (sched.next(p, seg)) {
@@ -582,7 +611,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
                 const uint32_t idesc = idesc_with_sf_id(kIdesc, (kb + j) % 4, (kb + j) % 4);
 #pragma unroll
                 for (int k = 0; k < BLOCK_K / 32; ++k)
-                  mma_mxf8_block_scale(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
+                  mma_mxf8_block_scale(d_tmem, adesc + kAStep * k, bdesc + kBStep * k, idesc, sfa_tmem, sfb_tmem,
                                        (kb + j != seg.kb_begin || k != 0) ? 1u : 0u);
               }
             }

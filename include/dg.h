@@ -71,6 +71,24 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa,
                          int M, int N, int K, cudaStream_t stream);
 
 /*
+ * The other memory layouts (README "Interfaces / Notices": the SM100 implementation supports
+ * NT, TN, NN and TT; "Normal dense GEMMs": fp8_gemm_{nt, nn, tn, tt}). The same product
+ * D = C + A' @ B'' of an M x K matrix A' and a K x N matrix B'', with A and B stored as:
+ *   dg_fp8_gemm_nn : a = A' [M, K] row-major (K-major),  b = B'' [K, N] row-major (N-major)
+ *   dg_fp8_gemm_tn : a = A'^T [K, M] row-major (M-major), b = B'' [K, N] row-major
+ *   dg_fp8_gemm_tt : a = A'^T [K, M] row-major,          b = B''^T [N, K] row-major (as nt)
+ * Scales do not depend on the storage: sfa holds one UE8M0 per row of A' (M) per 128-wide
+ * K-group, sfb one per 128 (N) x 128 (K) block, packed as for dg_fp8_gemm_nt. An M-major A
+ * needs M to be a multiple of 16 (its rows are M bytes); otherwise as dg_fp8_gemm_nt.
+ */
+dg_status dg_fp8_gemm_nn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                         void* d, int M, int N, int K, cudaStream_t stream);
+dg_status dg_fp8_gemm_tn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                         void* d, int M, int N, int K, cudaStream_t stream);
+dg_status dg_fp8_gemm_tt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                         void* d, int M, int N, int K, cudaStream_t stream);
+
+/*
  * Weight-gradient GEMM with FP32 output: D = C + A @ B.T (page "Weight gradient kernels
  * for dense and MoE models #95", wgrad_gemm_fp8_fp8_fp32_nt: FP8 x FP8 -> FP32, NT). The
  * pages give nothing beyond the name; the reading taken is the dense GEMM above with an

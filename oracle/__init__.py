@@ -152,6 +152,25 @@ def fp8_gemm_nt(a, sfa, b, sfb, c: Optional[np.ndarray], M: int, N: int, K: int,
     return D
 
 
+def fp8_gemm_nn(a, sfa, b, sfb, c, M: int, N: int, K: int) -> np.ndarray:
+    """D = C + A @ B with A stored [M, K] and B stored [K, N] (README "Interfaces / Notices":
+    the SM100 library supports the NT, TN, NN and TT layouts; "Normal dense GEMMs":
+    fp8_gemm_{nt, nn, tn, tt}). The layout is storage only: the scales keep their meaning
+    (A per row per 128-wide K-group, B per 128 x 128 block of the N x K view)."""
+    return fp8_gemm_nt(a, sfa, np.ascontiguousarray(np.asarray(b).T), sfb, c, M, N, K)
+
+
+def fp8_gemm_tn(a, sfa, b, sfb, c, M: int, N: int, K: int) -> np.ndarray:
+    """D = C + A @ B with A stored transposed [K, M] and B stored [K, N] (see fp8_gemm_nn)."""
+    return fp8_gemm_nt(np.ascontiguousarray(np.asarray(a).T), sfa, np.ascontiguousarray(np.asarray(b).T), sfb, c,
+                       M, N, K)
+
+
+def fp8_gemm_tt(a, sfa, b, sfb, c, M: int, N: int, K: int) -> np.ndarray:
+    """D = C + A @ B.T with A stored transposed [K, M] and B stored [N, K] (see fp8_gemm_nn)."""
+    return fp8_gemm_nt(np.ascontiguousarray(np.asarray(a).T), sfa, b, sfb, c, M, N, K)
+
+
 def wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c: Optional[np.ndarray], M: int, N: int, K: int,
                                rows: Optional[Sequence[int]] = None) -> np.ndarray:
     """Weight-gradient GEMM with FP32 output: D = C + A @ B.T, C and D FP32 (page "Weight

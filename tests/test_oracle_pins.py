@@ -321,10 +321,28 @@ def pin_k_grouped_equals_per_expert(O_):
         off += k
 
 
+def pin_layouts(O_):
+    # each storage layout against exact rationals over the logical M x K and N x K matrices
+    rng = np.random.default_rng(24)
+    M, N, K = 3, 140, 256
+    a, b = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    ea = rng.integers(123, 132, size=(M, 2)).astype(np.uint8)
+    eb = rng.integers(123, 132, size=(2, 2)).astype(np.uint8)
+    exact = brute_force(a, ea, b, eb)
+    sfa, sfb = words_from_codes(ea), words_from_codes(eb)
+    got = {
+        "nn": O_.fp8_gemm_nn(a, sfa, np.ascontiguousarray(b.T), sfb, None, M, N, K),
+        "tn": O_.fp8_gemm_tn(np.ascontiguousarray(a.T), sfa, np.ascontiguousarray(b.T), sfb, None, M, N, K),
+        "tt": O_.fp8_gemm_tt(np.ascontiguousarray(a.T), sfa, b, sfb, None, M, N, K),
+    }
+    for name, d in got.items():
+        np.testing.assert_allclose(d, exact, rtol=1e-14, err_msg=name)
+
+
 PINS = [pin_e4m3_table, pin_ue8m0_table, pin_bf16, pin_unpack, pin_brute_force, pin_identity,
         pin_one_hot, pin_pow2_invariance, pin_c_only, pin_dequantised_route,
         pin_contiguous_equals_dense, pin_masked_equals_dense, pin_wgrad_brute_force, pin_wgrad_c_only,
-        pin_k_grouped_equals_per_expert]
+        pin_k_grouped_equals_per_expert, pin_layouts]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -475,6 +493,12 @@ def _k_grouped_global_packing(old):
     return f
 
 
+def _tn_forgets_to_transpose_a(old):
+    def f(a, sfa, b, sfb, c, M, N, K):
+        return O.fp8_gemm_nt(np.asarray(a).reshape(M, K), sfa, np.ascontiguousarray(np.asarray(b).T), sfb, c, M, N, K)
+    return f
+
+
 MUTANTS = {
     "subnormal_implicit_one": _mut_table(_subnormal_with_implicit_one),
     "sign_ignored": _mut_table(lambda t: np.abs(t)),
@@ -490,6 +514,7 @@ MUTANTS = {
     "wgrad_c_rounded_to_bf16": _mut_attr("wgrad_gemm_fp8_fp8_fp32_nt", _wgrad_c_as_bf16),
     "wgrad_c_dropped": _mut_attr("wgrad_gemm_fp8_fp8_fp32_nt", _wgrad_c_dropped),
     "k_grouped_scales_packed_globally": _mut_attr("k_grouped_wgrad_gemm_fp8_fp8_fp32_nt", _k_grouped_global_packing),
+    "tn_reads_a_as_k_major": _mut_attr("fp8_gemm_tn", _tn_forgets_to_transpose_a),
 }
 
 
