@@ -134,7 +134,9 @@ class DeviceProblem:
         f = lambda x: t.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
         if isinstance(p, W.Dense):
             c = t.from_numpy(p.c.view(np.int16)).view(t.bfloat16).cuda() if p.c is not None else None
-            return dict(a=f(p.a), sfa=f(p.sfa), b=f(p.b), sfb=f(p.sfb), c=c,
+            a = p.a if p.layout[0] == "n" else np.ascontiguousarray(p.a.T)
+            b = p.b if p.layout[1] == "t" else np.ascontiguousarray(p.b.T)
+            return dict(a=f(a), sfa=f(p.sfa), b=f(b), sfb=f(p.sfb), c=c,
                         d=t.empty((p.M, p.N), dtype=t.bfloat16, device="cuda"))
         if isinstance(p, W.Wgrad):
             d = f(p.c) if p.c is not None else t.zeros((p.M, p.N), dtype=t.float32, device="cuda")
@@ -153,7 +155,7 @@ class DeviceProblem:
         c = self.copies[i % self.R]
         L, p = self.lib, self.p
         if isinstance(p, W.Dense):
-            L.dg_fp8_gemm_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
+            getattr(L, f"dg_fp8_gemm_{p.layout}")(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
         elif isinstance(p, W.Wgrad):
             L.dg_wgrad_gemm_fp8_fp8_fp32_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
         elif isinstance(p, W.KGrouped):

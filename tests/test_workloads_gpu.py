@@ -12,8 +12,8 @@ import torch
 
 import oracle as O
 import workloads as W
-from gpu_util import (SENTINEL, assert_parity, bf16_bits, bf16_f64, run_contiguous, run_dense, run_k_grouped,
-                      run_masked, run_wgrad)
+from gpu_util import (SENTINEL, assert_parity, bf16_bits, bf16_f64, dev, run_contiguous, run_dense, run_k_grouped,
+                      run_masked, run_wgrad, sentinel_like)
 
 pytestmark = pytest.mark.gpu
 
@@ -101,4 +101,18 @@ def test_k_grouped_workload(lib):
     for i, g in enumerate(groups):
         assert_parity(got[i], ref[i], f"{name} expert {g}")
     assert torch.isfinite(d).all()
+    assert lib.dg_get_device_status() == 0
+
+
+def test_layout_workload(lib):
+    name = "dense_nn_4096x7168x2048"
+    p = W.make_workload(name)
+    assert p.layout == "nn"
+    b_kn = dev(np.ascontiguousarray(p.b.T))
+    d = sentinel_like((p.M, p.N))
+    lib.dg_fp8_gemm_nn(dev(p.a), dev(p.sfa), b_kn, dev(p.sfb), None, d)
+    torch.cuda.synchronize()
+    rows = _rows(p.M, 64, 6)
+    ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, None, p.M, p.N, p.K, rows=rows)
+    assert_parity(bf16_f64(d)[rows], ref, name)
     assert lib.dg_get_device_status() == 0

@@ -121,6 +121,7 @@ class Dense:
     M: int
     N: int
     K: int
+    layout: str = "nt"         # how a and b are stored on the device (the arrays here are always NT)
 
     @property
     def flops(self) -> float:
@@ -336,6 +337,8 @@ WORKLOADS = {
     "masked_g32_m256_n7168_k2048": dict(kind="masked", G=32, max_m=256, N=7168, K=2048),
     # weight gradient of a 7168 x 4096 projection over 4096 tokens, accumulated into FP32
     "wgrad_7168x4096x4096_c": dict(kind="wgrad", M=7168, N=4096, K=4096, with_c=True),
+    # data gradient of a 7168 -> 2048 projection over 4096 tokens: dX = dY @ W, W stored [K, N]
+    "dense_nn_4096x7168x2048": dict(kind="dense_layout", layout="nn", M=4096, N=7168, K=2048, with_c=False),
     # MoE weight gradient: 4 experts, 4096 x 7168 each, 16384 tokens split among them
     "k_grouped_wgrad_g4_m4096_n7168_t16384": dict(kind="k_grouped", G=4, M=4096, N=7168, tokens=16384),
 }
@@ -352,6 +355,11 @@ def make_workload(name: str):
         return make_contiguous(seed=seed, **spec)
     if kind == "wgrad":
         return make_wgrad(seed=seed, **spec)
+    if kind == "dense_layout":
+        layout = spec.pop("layout")
+        p = make_dense(seed=seed, **spec)
+        p.layout = layout          # storage of A ("n": [M, K], "t": [K, M]) and B ("n": [K, N], "t": [N, K])
+        return p
     if kind == "k_grouped":
         return make_k_grouped(seed=seed, **spec)
     return make_masked(seed=seed, **spec)
