@@ -35,6 +35,8 @@ SIGNATURES = [
     ("dg_fp8_gemm_tn", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("dg_fp8_gemm_tt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    ("dg_k_grouped_fp8_gemm_tn_contiguous", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    ("dg_m_grouped_fp8_gemm_nn_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_pack_sf_ue8m0", _I, [_P, _P, _I, _I, _P]),
@@ -207,6 +209,44 @@ def dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c, d, ks, stream=Non
     _check("dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt",
            lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                                                        _ptr(ks), G, M, N, K, R, _stream(stream)))
+    return d
+
+
+def dg_k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, c, d, ks, stream=None) -> torch.Tensor:
+    """K-grouped GEMM, TN layout: a [K_total, M] e4m3 (M a multiple of 16), b [K_total, N] e4m3,
+    scales packed per expert as for dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt, c [G, M, N] float32
+    or None (may be d), d [G, M, N] float32, ks [G] int32 (CUDA)."""
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _f32(d, "d"); _i32(ks, "ks")
+    K, M = a.shape
+    Kb, N = b.shape
+    G = ks.shape[0]
+    _need(Kb == K and tuple(d.shape) == (G, M, N), "shape mismatch")
+    R = sfa.shape[0]
+    _need(sfa.dim() == 2 and sfa.shape[1] == 4 * (-(-M // 4)) and sfb.dim() == 2 and sfb.shape[0] == R
+          and sfb.shape[1] == 4 * (-(-(-(-N // 128)) // 4)), "scale shape mismatch")
+    if c is not None:
+        _f32(c, "c")
+        _need(tuple(c.shape) == (G, M, N), "c shape mismatch")
+    _check("dg_k_grouped_fp8_gemm_tn_contiguous",
+           lib.dg_k_grouped_fp8_gemm_tn_contiguous(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                                   _ptr(ks), G, M, N, K, R, _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_gemm_nn_contiguous(a, sfa, b, sfb, d, m_indices, stream=None) -> torch.Tensor:
+    """Contiguous M-grouped GEMM with N-major weights: a [M_total, K], b [G, K, N] (N contiguous),
+    other arguments as dg_m_grouped_fp8_gemm_nt_contiguous."""
+    lib = load_library()
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d"); _i32(m_indices, "m_indices")
+    M, K = a.shape
+    G, Kb, N = b.shape
+    _need(Kb == K and tuple(d.shape) == (M, N) and tuple(m_indices.shape) == (M,), "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(M, K) and tuple(sfb.shape) == sf_shape(-(-N // 128), K, G),
+          "scale shape mismatch")
+    _check("dg_m_grouped_fp8_gemm_nn_contiguous",
+           lib.dg_m_grouped_fp8_gemm_nn_contiguous(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d),
+                                                   _ptr(m_indices), M, N, K, G, _stream(stream)))
     return d
 
 

@@ -362,11 +362,11 @@ dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const 
     // 128-column atoms)
     switch (bn) {
       case 128:
-        return Launcher<kKind, 128, 5, 2, 4, 2, kHasC, 1, 0, false, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, p, grid,
-                                                                                         stream);
+        return Launcher<kKind, 128, 5, 2, 4, 2, kHasC, 1, 0, kOutF32, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, p,
+                                                                                           grid, stream);
       case 256:
-        return Launcher<kKind, 256, 4, 1, 4, 1, kHasC, 1, 0, false, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, p, grid,
-                                                                                         stream);
+        return Launcher<kKind, 256, 4, 1, 4, 1, kHasC, 1, 0, kOutF32, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, p,
+                                                                                           grid, stream);
     }
     return DG_ERR_INVALID_ARG;
   }
@@ -947,12 +947,17 @@ dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const
   return run_dense_single<true>(*ds, a, sfa, b, sfb, c, d, M, N, K, BN, sms, stream);
 }
 
-dg_status dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const void* b,
+}  // extern "C"
+
+namespace {
+template <bool kMN>
+dg_status k_grouped_entry(const void* a, const int32_t* sfa, const void* b,
                                                 const int32_t* sfb, const float* c, float* d, const int32_t* ks,
                                                 int G, int M, int N, int K_total, int sf_k_rows,
                                                 cudaStream_t stream) {
   if (G <= 0 || M < 0 || K_total < 0 || sf_k_rows < 0) return DG_ERR_INVALID_ARG;
   if (N <= 0 || N % 16 != 0 || K_total % 128 != 0) return DG_ERR_INVALID_ARG;
+  if (kMN && M % 16 != 0) return DG_ERR_INVALID_ARG;   // [K, M] rows must be 16-byte multiples
   if (M == 0) return DG_OK;
   if (!d || !ks || (K_total > 0 && (!a || !sfa || !b || !sfb || sf_k_rows == 0))) return DG_ERR_INVALID_ARG;
   if ((K_total > 0 && (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb))) || !aligned16(d) ||
@@ -968,9 +973,11 @@ dg_status dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* 
     return e == cudaSuccess ? DG_OK : cuda_fail(e);
   }
   const int sms = sms_to_use(*ds);
-  const int BN = std::getenv("DG_FORCE_BN") || N <= 128 ? pick_bn(dg::Kind::Dense, N) : 192;
+  int BN = std::getenv("DG_FORCE_BN") || N <= 128 ? pick_bn(dg::Kind::Dense, N) : 192;
+  if (kMN && BN == 192) BN = 256;   // an N-major B tile is whole 128-column atoms
   CUtensorMap ta, tb, tsa, tsb, td;
-  bool ok = map_operand_2d(&ta, a, M, K_total, 128) && map_operand_2d(&tb, b, N, K_total, BN) &&
+  bool ok = (kMN ? map_operand_mn(&ta, a, M, K_total) : map_operand_2d(&ta, a, M, K_total, 128)) &&
+            (kMN ? map_operand_mn(&tb, b, N, K_total) : map_operand_2d(&tb, b, N, K_total, BN)) &&
             map_sf(&tsa, sfa, 0, M, sf_k_rows, 128) && map_sf(&tsb, sfb, 0, ceil_div(N, 128), sf_k_rows, 8);
   {
     const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
@@ -994,8 +1001,24 @@ dg_status dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* 
   const long long tiles = static_cast<long long>(G) * ceil_div(M, 128) * ceil_div(N, BN);
   if (tiles > (1LL << 30)) return DG_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(std::min<long long>(tiles, sms));
-  if (c) return launch_bn<dg::Kind::KGrouped, true, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
-  return launch_bn<dg::Kind::KGrouped, false, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+  if (c) return launch_bn<dg::Kind::KGrouped, true, true, kMN, kMN>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+  return launch_bn<dg::Kind::KGrouped, false, true, kMN, kMN>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+}
+}  // namespace
+
+extern "C" {
+
+dg_status dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const void* b,
+                                                const int32_t* sfb, const float* c, float* d, const int32_t* ks,
+                                                int G, int M, int N, int K_total, int sf_k_rows,
+                                                cudaStream_t stream) {
+  return k_grouped_entry<false>(a, sfa, b, sfb, c, d, ks, G, M, N, K_total, sf_k_rows, stream);
+}
+
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              const float* c, float* d, const int32_t* ks, int G, int M, int N,
+                                              int K_total, int sf_k_rows, cudaStream_t stream) {
+  return k_grouped_entry<true>(a, sfa, b, sfb, c, d, ks, G, M, N, K_total, sf_k_rows, stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
@@ -1054,6 +1077,57 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
   return launch_bn<dg::Kind::Contiguous, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+}
+
+dg_status dg_m_grouped_fp8_gemm_nn_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              void* d, const int32_t* m_indices, int M_total, int N, int K, int G,
+                                              cudaStream_t stream) {
+  if (M_total < 0 || G <= 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (M_total == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d || !m_indices) return DG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d) ||
+      (reinterpret_cast<uintptr_t>(m_indices) & 3u))
+    return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+
+  const int KP = ceil_div(K / 128, 4);
+  CUtensorMap ta, tb, tsa, tsb, td;
+  // 128- or 256-wide tiles (an N-major B tile is whole 128-column atoms), the wider unless
+  // it wastes columns
+  int BN = ceil_div(N, 256) * 256 <= ceil_div(N, 128) * 128 ? 256 : 128;
+  if (const char* f = std::getenv("DG_FORCE_BN")) {
+    const int v = std::atoi(f);
+    if (v == 128 || v == 256) BN = v;
+  }
+  CUtensorMap tb_mn;
+  {
+    // B stored [G][K][N]: boxes of 128 K-rows x 128 N-bytes, 128-byte swizzle
+    const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(G)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(N) * K};
+    const uint32_t box[3] = {128, 128, 1};
+    if (!make_map(&tb_mn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return DG_ERR_CUDA;
+  }
+  tb = tb_mn;
+  if (!map_operand_2d(&ta, a, M_total, K, 128) ||
+      !map_sf(&tsa, sfa, 0, M_total, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
+      !map_out(&td, d, 0, M_total, N))
+    return DG_ERR_CUDA;
+  dg::Params p{};
+  p.M = M_total;
+  p.N = N;
+  p.K = K;
+  p.G = G;
+  p.m_indices = m_indices;
+  p.d = static_cast<__nv_bfloat16*>(d);
+  p.status = ds->status;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
+  const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
+  const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
+  return launch_bn<dg::Kind::Contiguous, false, false, false, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,

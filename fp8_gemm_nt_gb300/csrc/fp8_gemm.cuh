@@ -393,7 +393,10 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
   static_assert(!kOutF32 || ((kKind == Kind::Dense || kKind == Kind::KGrouped) && kSplit == 0),
                 "FP32 output: dense (tile mode / stream-K) and K-grouped forms only");
   static_assert(kKind != Kind::KGrouped || (kOutF32 && kKG == 1), "the K-grouped form writes FP32, one K-group per stage");
-  static_assert((!kAMN && !kBMN) || (kKind == Kind::Dense && kSplit == 0 && !kOutF32), "MN-major operands: dense BF16");
+  static_assert((!kAMN && !kBMN) ||
+                    (kSplit == 0 && ((kKind == Kind::Dense && !kOutF32) || (kKind == Kind::Contiguous && !kAMN && !kOutF32) ||
+                                     (kKind == Kind::KGrouped && kOutF32))),
+                "MN-major operands: dense (BF16), contiguous N-major B (BF16), K-grouped (FP32)");
   static_assert(!kBMN || BN % 128 == 0, "an N-major B tile is whole 128-column atoms");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -505,14 +508,21 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
             if constexpr (kKind == Kind::Masked) {
               tma_load_3d(sa + j * C::A_SUB, &tm_a, fb, (kb + j) * BLOCK_K, row0, seg.g);
             } else if constexpr (kAMN) {
-              tma_load_2d(sa + j * C::A_SUB, &tm_a, fb, row0, (kb + j) * BLOCK_K);
+              tma_load_2d(sa + j * C::A_SUB, &tm_a, fb, row0, (seg.k_base + kb + j) * BLOCK_K);
             } else {
               tma_load_2d(sa + j * C::A_SUB, &tm_a, fb, (seg.k_base + kb + j) * BLOCK_K, row0);
             }
             if constexpr (kBMN) {
 #pragma unroll
-              for (int h = 0; h < BN / 128; ++h)
-                tma_load_2d(sb + j * C::B_SUB + h * (128 * BLOCK_K), &tm_b, fb, n0 + 128 * h, (kb + j) * BLOCK_K);
+              for (int h = 0; h < BN / 128; ++h) {
+                if constexpr (kKind == Kind::Contiguous) {
+                  tma_load_3d(sb + j * C::B_SUB + h * (128 * BLOCK_K), &tm_b, fb, n0 + 128 * h, (kb + j) * BLOCK_K,
+                              seg.g);
+                } else {
+                  tma_load_2d(sb + j * C::B_SUB + h * (128 * BLOCK_K), &tm_b, fb, n0 + 128 * h,
+                              (seg.k_base + kb + j) * BLOCK_K);
+                }
+              }
             } else if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
               tma_load_2d(sb + j * C::B_SUB, &tm_b, fb, (seg.k_base + kb + j) * BLOCK_K, n0);
             } else {

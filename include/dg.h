@@ -128,6 +128,20 @@ dg_status dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* 
                                                 cudaStream_t stream);
 
 /*
+ * K-grouped GEMM in the TN layout (README "Grouped GEMMs (contiguous layout)": the K-axis-
+ * grouped API for MoE weight backward, k_grouped_fp8_gemm_tn_contiguous). The same operation
+ * and arguments as dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt, with A and B stored token-major:
+ *   a : E4M3 [K_total, M] row-major (M contiguous; M a multiple of 16),
+ *   b : E4M3 [K_total, N] row-major (N contiguous),
+ * so that D[g] = C[g] + A_g @ B_g.T with A_g = a[slice_g, :].T and B_g = b[slice_g, :].T.
+ * Output FP32 (a weight gradient; the pages give no output type: the reading taken is the
+ * K-grouped weight-gradient form's).
+ */
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              const float* c, float* d, const int32_t* ks, int G, int M, int N,
+                                              int K_total, int sf_k_rows, cudaStream_t stream);
+
+/*
  * M-grouped GEMM, contiguous layout ("Grouped GEMMs (contiguous layout)":
  * m_grouped_fp8_gemm_nt_contiguous). Only M is grouped; N and K are shared by the G
  * experts. Each expert's token rows are concatenated along M, and each expert segment
@@ -146,6 +160,17 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
                                               const void* b, const int32_t* sfb,
                                               void* d, const int32_t* m_indices,
                                               int M_total, int N, int K, int G,
+                                              cudaStream_t stream);
+
+/*
+ * Contiguous M-grouped GEMM with the weights stored N-major (README "Grouped GEMMs
+ * (contiguous layout)": m_grouped_fp8_gemm_{nt, nn}_contiguous): as
+ * dg_m_grouped_fp8_gemm_nt_contiguous except b = E4M3 [G, K, N] row-major (expert g's
+ * weights at b + g*K*N, N contiguous), i.e. D = A @ B_g for rows of expert g. Scales as for
+ * the NT form (sfb per 128 (N) x 128 (K) block of expert g).
+ */
+dg_status dg_m_grouped_fp8_gemm_nn_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              void* d, const int32_t* m_indices, int M_total, int N, int K, int G,
                                               cudaStream_t stream);
 
 /*

@@ -233,6 +233,27 @@ def k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c: Optional[np.ndarray]
     return out
 
 
+def k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, c: Optional[np.ndarray], ks, M: int, N: int,
+                                     groups: Optional[Sequence[int]] = None,
+                                     rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """The K-grouped GEMM with A stored [K_total, M] and B stored [K_total, N] (README
+    "Grouped GEMMs (contiguous layout)": k_grouped_fp8_gemm_tn_contiguous, the K-axis-grouped
+    API for MoE weight backward). Storage only: the same D[g] = C[g] + A_g @ B_g.T as
+    k_grouped_wgrad_gemm_fp8_fp8_fp32_nt over the logical [M, K_total] and [N, K_total]."""
+    return k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(np.ascontiguousarray(np.asarray(a).T), sfa,
+                                                np.ascontiguousarray(np.asarray(b).T), sfb, c, ks, M, N,
+                                                groups=groups, rows=rows)
+
+
+def m_grouped_fp8_gemm_nn_contiguous(a, sfa, b, sfb, m_indices, M_total: int, N: int, K: int, G: int,
+                                     rows: Optional[Sequence[int]] = None):
+    """Contiguous M-grouped GEMM with each expert's B stored [K, N] (README "Grouped GEMMs
+    (contiguous layout)": m_grouped_fp8_gemm_{nt, nn}_contiguous). Storage only: b[g].T is
+    the [N, K] matrix of the NT form."""
+    bt = np.ascontiguousarray(np.transpose(np.asarray(b), (0, 2, 1)))
+    return m_grouped_fp8_gemm_nt_contiguous(a, sfa, bt, sfb, m_indices, M_total, N, K, G, rows=rows)
+
+
 def m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, m_indices, M_total: int, N: int, K: int,
                                      G: int, rows: Optional[Sequence[int]] = None):
     """Contiguous M-grouped GEMM (README "Grouped GEMMs (contiguous layout)").

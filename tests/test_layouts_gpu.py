@@ -98,3 +98,56 @@ def test_t_layout_rejects_m_not_multiple_of_16(lib):
     x = ctypes.c_void_p(0x10000)
     assert raw.dg_fp8_gemm_tn(x, x, x, x, None, x, 100, 128, 128, None) == 1
     assert raw.dg_fp8_gemm_tt(x, x, x, x, None, x, 100, 128, 128, None) == 1
+
+
+@pytest.mark.parametrize("bn", [None, "128"])
+@pytest.mark.parametrize("counts,N,K", [
+    ([130, 0, 170, 1], 144, 256),
+    ([128, 256, 5, 300], 400, 640),
+])
+def test_nn_contiguous_parity(lib, monkeypatch, bn, counts, N, K):
+    from gpu_util import SENTINEL
+    if bn is not None:
+        monkeypatch.setenv("DG_FORCE_BN", bn)
+    p = W.make_contiguous(G=len(counts), tokens=sum(counts), N=N, K=K, seed=1500 + N, counts=counts)
+    b_kn = np.ascontiguousarray(p.b.transpose(0, 2, 1))
+    d = sentinel_like((p.M_total, p.N))
+    lib.dg_m_grouped_fp8_gemm_nn_contiguous(dev(p.a), dev(p.sfa), dev(b_kn), dev(p.sfb), d, dev(p.m_indices))
+    torch.cuda.synchronize()
+    ref, valid = O.m_grouped_fp8_gemm_nn_contiguous(p.a, p.sfa, b_kn, p.sfb, p.m_indices, p.M_total, p.N, p.K, p.G)
+    bits = bf16_bits(d)
+    assert (bits[~valid] == SENTINEL).all()
+    assert_parity(bf16_f64(d)[valid], ref[valid], f"nn contiguous {counts}")
+    # the NT form at the same width computes the same bits
+    monkeypatch.setenv("DG_FORCE_BN", bn or ("256" if -(-N // 256) * 256 <= -(-N // 128) * 128 else "128"))
+    d_nt = sentinel_like((p.M_total, p.N))
+    lib.dg_m_grouped_fp8_gemm_nt_contiguous(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d_nt, dev(p.m_indices))
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(d_nt), bits)
+
+
+@pytest.mark.parametrize("ks,M,N,with_c", [
+    ([256, 0, 384], 256, 384, True),
+    ([128, 512, 640], 208, 272, False),      # ragged M (multiple of 16) and N
+])
+def test_tn_k_grouped_parity(lib, monkeypatch, ks, M, N, with_c):
+    p = W.make_k_grouped(G=len(ks), M=M, N=N, tokens=0, seed=1600 + M + N, with_c=with_c, ks=np.array(ks))
+    a_t, b_t = np.ascontiguousarray(p.a.T), np.ascontiguousarray(p.b.T)
+    c = dev(p.c) if p.c is not None else None
+    d = torch.full((p.G, M, N), float("nan"), dtype=torch.float32, device="cuda")
+    lib.dg_k_grouped_fp8_gemm_tn_contiguous(dev(a_t), dev(p.sfa), dev(b_t), dev(p.sfb), c, d,
+                                            dev(np.asarray(p.ks, np.int32)))
+    torch.cuda.synchronize()
+    got = d.cpu().numpy().astype(np.float64)
+    ref = O.k_grouped_fp8_gemm_tn_contiguous(a_t, p.sfa, b_t, p.sfb, p.c, p.ks, M, N)
+    for g in range(p.G):
+        rep = assert_parity(got[g], ref[g], f"tn k-grouped expert {g}")
+        assert rep["max_err"] <= 1e-5 * max(rep["rms"], 1e-30), rep
+    # the NT K-grouped form at the same width computes the same bits
+    monkeypatch.setenv("DG_FORCE_BN", "256" if -(-N // 256) * 256 <= -(-N // 128) * 128 else "128")
+    d_nt = torch.full((p.G, M, N), float("nan"), dtype=torch.float32, device="cuda")
+    lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), c, d_nt,
+                                                dev(np.asarray(p.ks, np.int32)))
+    torch.cuda.synchronize()
+    monkeypatch.delenv("DG_FORCE_BN")
+    assert torch.equal(d_nt, d)

@@ -339,10 +339,37 @@ def pin_layouts(O_):
         np.testing.assert_allclose(d, exact, rtol=1e-14, err_msg=name)
 
 
+def pin_grouped_layouts(O_):
+    # the N-major contiguous form and the TN K-grouped form against exact rationals over the
+    # logical matrices
+    rng = np.random.default_rng(25)
+    K, N = 256, 136
+    m_idx = np.array([0] * 2 + [-1] * 126 + [1] * 3 + [-1] * 125, np.int32)
+    M_total = len(m_idx)
+    a = random_codes(rng, (M_total, K))
+    b = random_codes(rng, (2, N, K))
+    ea = rng.integers(123, 132, size=(M_total, 2)).astype(np.uint8)
+    eb = rng.integers(123, 132, size=(2, 2, 2)).astype(np.uint8)
+    sfb = np.stack([words_from_codes(eb[g]) for g in range(2)])
+    D, valid = O_.m_grouped_fp8_gemm_nn_contiguous(a, words_from_codes(ea), np.ascontiguousarray(b.transpose(0, 2, 1)),
+                                                   sfb, m_idx, M_total, N, K, 2)
+    assert np.array_equal(valid, m_idx >= 0)
+    for r in np.nonzero(m_idx >= 0)[0][:4]:
+        g = m_idx[r]
+        np.testing.assert_allclose(D[r], brute_force(a[r:r + 1], ea[r:r + 1], b[g], eb[g])[0], rtol=1e-14)
+    M, Nk, ks = 4, 160, [128, 256]
+    a2, b2 = random_codes(rng, (M, sum(ks))), random_codes(rng, (Nk, sum(ks)))
+    ea2 = rng.integers(123, 132, size=(M, 3)).astype(np.uint8)
+    eb2 = rng.integers(123, 132, size=(2, 3)).astype(np.uint8)
+    D2 = O_.k_grouped_fp8_gemm_tn_contiguous(np.ascontiguousarray(a2.T), W.pack_sf_k_grouped(ea2, ks),
+                                             np.ascontiguousarray(b2.T), W.pack_sf_k_grouped(eb2, ks), None, ks, M, Nk)
+    np.testing.assert_allclose(D2[1], brute_force(a2[:, 128:], ea2[:, 1:], b2[:, 128:], eb2[:, 1:]), rtol=1e-14)
+
+
 PINS = [pin_e4m3_table, pin_ue8m0_table, pin_bf16, pin_unpack, pin_brute_force, pin_identity,
         pin_one_hot, pin_pow2_invariance, pin_c_only, pin_dequantised_route,
         pin_contiguous_equals_dense, pin_masked_equals_dense, pin_wgrad_brute_force, pin_wgrad_c_only,
-        pin_k_grouped_equals_per_expert, pin_layouts]
+        pin_k_grouped_equals_per_expert, pin_layouts, pin_grouped_layouts]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
