@@ -555,11 +555,15 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   const size_t sfb_words = static_cast<size_t>(G) * KP * sfb_rows * 128;
   if (static_cast<size_t>(KP) * num_mb > (1u << 30) || static_cast<size_t>(G) * KP * sfb_rows > (1u << 30))
     return DG_ERR_UNSUPPORTED;
+  // contiguous form: the pair-row list (3 ints per pair row, at most one per block) and its length
+  const size_t list_words = kKind == dg::Kind::Contiguous ? 4 + 4 * static_cast<size_t>(ceil_div(3 * num_mb, 4)) : 0;
   void* ws = nullptr;
-  if (dg_status s = stream_workspace(ds, stream, kSkCounterInts * 4 + (sfa_words + sfb_words) * 4, &ws); s != DG_OK)
+  if (dg_status s = stream_workspace(ds, stream, kSkCounterInts * 4 + (sfa_words + sfb_words + list_words) * 4, &ws);
+      s != DG_OK)
     return s;
   int32_t* sfa_t = static_cast<int32_t*>(ws) + kSkCounterInts;
   int32_t* sfb_t = sfa_t + sfa_words;
+  int32_t* list = sfb_t + sfb_words;
   {
     dg::SfPrepArgs pa{};
     pa.sfa = sfa;
@@ -575,13 +579,26 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
     pa.b_chunks = sfb_rows;
     pa.tile_bn = kBN;
     pa.kp = KP;
+    if constexpr (kKind == dg::Kind::Contiguous) {
+      pa.m_indices = p.m_indices;
+      pa.num_mb = num_mb;
+      pa.groups_g = p.G;
+      pa.pair_count = list;
+      pa.pair_list = list + 4;   // 16-byte aligned after the count
+      pa.status = ds.status;
+      p.pair_count = pa.pair_count;
+      p.pair_list = pa.pair_list;
+    }
     const size_t words = sfa_words + sfb_words;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(std::min<size_t>((words + 255) / 256, 2048)), 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    // (+ one block that lists the contiguous form's pair rows)
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<size_t>((words + 255) / 256, 2048) +
+                                             (kKind == dg::Kind::Contiguous ? 1 : 0)),
+                       1, 1);
+    cfg.blockDim = dim3(256, 1, 1);   // the pair-row scan assumes 256 threads
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;

@@ -57,7 +57,10 @@ struct Params {
   int K;
   int G;
   const int32_t* m_indices;       // contiguous: expert of each row, -1 = padding
-  const int32_t* masked_m;        // masked: valid rows per group (device)
+  union {
+    const int32_t* masked_m;      // masked: valid rows per group (device)
+    const int* pair_count;        // CTA-pair kernel, contiguous form: number of listed pair rows
+  };
   const __nv_bfloat16* c;         // dense: optional addend [M, N]
   __nv_bfloat16* d;               // output (used by the predicated store path)
   uint32_t* status;               // device status word
@@ -72,8 +75,14 @@ struct Params {
   int sf_num_mb;                  // 128-row blocks of A per K-quad
   int sf_nb;                      // B chunk rows per (group, K-quad): two per tile
   // K-grouped form: K-slice length of each expert (device, multiples of 128) and the number
-  // of packed scale-word rows (the scales of each expert start a new word row)
-  const int32_t* ks;
+  // of packed scale-word rows (the scales of each expert start a new word row). The CTA-pair
+  // kernel's contiguous form instead reads its pair rows, listed per call ({first block,
+  // expert, own blocks} each), from the same slot (the two forms never meet; keeping the
+  // parameter block small keeps every kernel within its register budget).
+  union {
+    const int32_t* ks;
+    const int* pair_list;
+  };
   int sf_k_rows;
 };
 

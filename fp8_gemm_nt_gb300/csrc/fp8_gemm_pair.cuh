@@ -80,51 +80,24 @@ struct PairConfig {
 };
 
 // Walks the pair tiles of the sequence t = cluster, += clusters. A pair row is two
-// consecutive 128-row blocks; in the contiguous form both blocks belong to one expert
-// (an expert with an odd number of blocks ends with a pair whose second block is not its
-// own: that CTA's rows are computed and discarded).
+// consecutive 128-row blocks; in the contiguous form both blocks belong to one expert (an
+// expert with an odd number of blocks ends with a pair whose second block is not its own:
+// that CTA's rows are computed and discarded). The contiguous pair rows are listed once per
+// call by sf_to_utccp_kernel (first block, expert and own-block count per pair row, and
+// their number), so a tile costs one small load.
 template <Kind kKind, int kBN>
 struct PairScheduler {
-  int num_n, num_mb, total;
+  int num_n, total;
   int t, step;
-  // contiguous cursor
-  int cur_pair, cur_block;
-
-  __device__ __forceinline__ int expert_of(const Params& p, int b) const {
-    if (b >= num_mb) return -1;
-    const int g = __ldg(p.m_indices + b * BLOCK_M);
-    return (g >= 0 && g < p.G) ? g : -1;
-  }
-  __device__ __forceinline__ int pair_len(const Params& p, int b, int g) const {
-    return (b + 1 < num_mb && expert_of(p, b + 1) == g) ? 2 : 1;
-  }
 
   __device__ __forceinline__ PairScheduler(const Params& p, int cluster, int clusters) {
     num_n = ceil_div_c(p.N, kBN);
-    num_mb = ceil_div_c(p.M, BLOCK_M);
     t = cluster;
     step = clusters;
-    cur_pair = 0;
-    cur_block = 0;
     if constexpr (kKind == Kind::Contiguous) {
-      int pairs = 0;
-      for (int b = 0; b < num_mb;) {
-        const int g = expert_of(p, b);
-        if (g < 0) {
-          // a block led by an index outside [-1, G) is skipped and reported (once, by CTA 0)
-          if (blockIdx.x == 0 && threadIdx.x == 0) {
-            const int raw = __ldg(p.m_indices + b * BLOCK_M);
-            if (raw < -1 || raw >= p.G) atomicOr(p.status, kStatusBadIndexBit);
-          }
-          ++b;
-          continue;
-        }
-        b += pair_len(p, b, g);
-        ++pairs;
-      }
-      total = pairs * num_n;
+      total = __ldg(p.pair_count) * num_n;
     } else {
-      total = ceil_div_c(num_mb, 2) * num_n;
+      total = ceil_div_c(ceil_div_c(p.M, BLOCK_M), 2) * num_n;
     }
   }
 
@@ -141,27 +114,15 @@ struct PairScheduler {
     s.tile = pair;
     s.valid_m = p.M;
     if constexpr (kKind == Kind::Contiguous) {
-      // advance the cursor to the pair with index `pair` (indices only grow)
-      while (true) {
-        int g = expert_of(p, cur_block);
-        while (g < 0) {
-          if (++cur_block >= num_mb) return false;
-          g = expert_of(p, cur_block);
-        }
-        if (cur_pair == pair) {
-          s.g = g;
-          s.m_blk = cur_block;
-          s.n_contrib = pair_len(p, cur_block, g);   // blocks of this pair that belong to the expert
-          return true;
-        }
-        cur_block += pair_len(p, cur_block, g);
-        ++cur_pair;
-      }
+      const int3 e = *reinterpret_cast<const int3*>(p.pair_list + 3 * pair);
+      s.m_blk = e.x;
+      s.g = e.y;
+      s.n_contrib = e.z;   // blocks of this pair that belong to the expert
     } else {
       s.g = 0;
       s.m_blk = 2 * pair;
-      return true;
     }
+    return true;
   }
 };
 
@@ -592,6 +553,12 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
 // may start inside a scale block. Launched as a programmatic dependent of the previous
 // kernel in the stream (waits for it before reading or writing global memory).
 struct SfPrepArgs {
+  // contiguous form: the pair rows (built by the last block of the launch), else null
+  const int32_t* m_indices;
+  int num_mb, groups_g;
+  int* pair_list;       // [num_mb][3]: first block, expert, own blocks (1 or 2)
+  int* pair_count;
+  uint32_t* status;
   const int32_t* sfa;   // [KP][lda] words
   int32_t* sfa_out;     // [KP][a_blocks][128]
   int a_rows, lda, a_blocks;
@@ -601,13 +568,90 @@ struct SfPrepArgs {
   int kp;
 };
 
+// Pair rows of the contiguous layout, by one block: block b (of 128 rows) belongs to the
+// expert in m_indices[128 b] (outside [0, G): not computed, and reported unless it is -1);
+// runs of consecutive blocks of one expert are cut into pairs from the run's first block. A
+// block starts a pair iff it is valid and an even distance from its run's first block; pair
+// rows are numbered by an exclusive prefix sum of those starts (two block-wide scans per
+// chunk of blockDim.x blocks, carried across chunks).
+__device__ void build_pair_list(const SfPrepArgs& a) {
+  __shared__ int s_g[256 + 1];
+  __shared__ int s_scan[256];
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;   // 256
+  int run_start_carry = -1;    // first block of the run the previous chunk ended in
+  int prev_g = -2;             // expert of the block before this chunk
+  int count_carry = 0;
+  auto expert = [&](int b) {
+    const int g = __ldg(a.m_indices + static_cast<long long>(b) * 128);
+    return (g >= 0 && g < a.groups_g) ? g : -1;
+  };
+  for (int base = 0; base < a.num_mb; base += nt) {
+    const int b = base + tid;
+    const bool in = b < a.num_mb;
+    int raw = -1;
+    if (in) {
+      raw = __ldg(a.m_indices + static_cast<long long>(b) * 128);
+      if (raw < -1 || raw >= a.groups_g) atomicOr(a.status, kStatusBadIndexBit);
+    }
+    const int g = in && raw >= 0 && raw < a.groups_g ? raw : -1;
+    s_g[tid + 1] = g;
+    if (tid == 0) s_g[0] = prev_g;
+    __syncthreads();
+    // run starts: a valid block whose predecessor has another expert
+    int rs = (g >= 0 && s_g[tid] != g) ? b : -1;
+    s_scan[tid] = rs;
+    __syncthreads();
+    for (int off = 1; off < nt; off <<= 1) {           // inclusive prefix max
+      const int v = tid >= off ? s_scan[tid - off] : -1;
+      __syncthreads();
+      s_scan[tid] = max(s_scan[tid], v);
+      __syncthreads();
+    }
+    const int run_start = max(s_scan[tid], run_start_carry);
+    const bool start = g >= 0 && ((b - run_start) % 2 == 0);
+    const int last_rs = s_scan[nt - 1];
+    __syncthreads();
+    s_scan[tid] = start ? 1 : 0;
+    __syncthreads();
+    for (int off = 1; off < nt; off <<= 1) {           // inclusive prefix sum
+      const int v = tid >= off ? s_scan[tid - off] : 0;
+      __syncthreads();
+      s_scan[tid] += v;
+      __syncthreads();
+    }
+    if (start) {
+      const int idx = count_carry + s_scan[tid] - 1;
+      const int own = (b + 1 < a.num_mb && expert(b + 1) == g) ? 2 : 1;
+      a.pair_list[3 * idx + 0] = b;
+      a.pair_list[3 * idx + 1] = g;
+      a.pair_list[3 * idx + 2] = own;
+    }
+    const int chunk_count = s_scan[nt - 1];
+    run_start_carry = max(run_start_carry, last_rs);
+    prev_g = s_g[nt];
+    __syncthreads();
+    count_carry += chunk_count;
+    // a run that ended inside this chunk must not leak into the next one: the next chunk's
+    // first valid block restarts its run whenever its expert differs from prev_g, which the
+    // run-start flags above take care of; run_start_carry only matters for a continuing run
+  }
+  if (tid == 0) *a.pair_count = count_carry;
+}
+
 __global__ void sf_to_utccp_kernel(const SfPrepArgs a) {
   grid_dependency_wait();
   grid_launch_dependents();
+  const bool list_block = a.m_indices != nullptr && blockIdx.x == gridDim.x - 1;
+  if (list_block) {
+    build_pair_list(a);
+    return;
+  }
+  const int sf_blocks = gridDim.x - (a.m_indices != nullptr ? 1 : 0);
   const long long na = static_cast<long long>(a.kp) * a.a_blocks * 128;
   const long long total = na + static_cast<long long>(a.groups) * a.kp * a.b_chunks * 128;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+       idx += static_cast<long long>(sf_blocks) * blockDim.x) {
     int32_t val = 0;
     if (idx < na) {
       const int w = static_cast<int>(idx % 128);

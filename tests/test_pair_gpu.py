@@ -14,7 +14,7 @@ import torch
 
 import oracle as O
 import workloads as W
-from gpu_util import SENTINEL, assert_parity, bf16_bits, bf16_f64, run_contiguous, run_dense
+from gpu_util import SENTINEL, assert_parity, bf16_bits, bf16_f64, dev, run_contiguous, run_dense, sentinel_like
 
 pytestmark = pytest.mark.gpu
 
@@ -118,3 +118,20 @@ def test_pair_contiguous_bad_index_reported(lib, monkeypatch):
     d = run_contiguous(lib, p)
     assert lib.dg_get_device_status() == 6
     assert (bf16_bits(d)[128:] == SENTINEL).all(), "rows of an invalid expert were written"
+
+
+def test_pair_contiguous_repeated_launches(lib, monkeypatch):
+    # the pair rows are listed by the scale-preparation launch before every GEMM; many
+    # back-to-back launches (programmatic dependent launch chains prep -> GEMM -> prep ...)
+    # must all complete without a timeout and leave the same result
+    monkeypatch.setenv("DG_PAIR", "1")
+    p = W.make_contiguous(G=8, tokens=3000, N=512, K=1024, seed=77)
+    a, sfa, b, sfb, idx = dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), dev(p.m_indices)
+    d = sentinel_like((p.M_total, p.N))
+    lib.dg_get_device_status()
+    for _ in range(300):
+        lib.dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, idx)
+    torch.cuda.synchronize()
+    assert lib.dg_get_device_status() == 0
+    ref, valid = O.m_grouped_fp8_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K, p.G)
+    assert_parity(bf16_f64(d)[valid], ref[valid], "after 300 launches")
