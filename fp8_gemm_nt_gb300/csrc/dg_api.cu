@@ -1051,11 +1051,10 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   DeviceState* ds = nullptr;
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
 
-  // The contiguous form runs on single-CTA 128x256 tiles by default (measured faster on
-  // GB300 than the CTA-pair kernel for the G=8 workload: 2856 vs 2730 TFLOPS); DG_PAIR=1
-  // selects the pair kernel.
-  const char* pair_env = std::getenv("DG_PAIR");
-  if (pair_env && pair_env[0] == '1' && !std::getenv("DG_FORCE_BN")) {
+  // The contiguous form runs on CTA pairs (measured on GB300 for the G=8 workload over 100
+  // back-to-back launches: 2860-2950 TFLOPS against 2600-2725 with single-CTA 128 x 256
+  // tiles); DG_PAIR=0 or DG_FORCE_BN selects the single-CTA kernel.
+  if (pair_enabled() && !std::getenv("DG_FORCE_BN")) {
     {
       dg::Params pp{};
       pp.M = M_total;

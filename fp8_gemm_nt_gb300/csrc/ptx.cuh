@@ -60,16 +60,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed. Returns false if that did
-// not happen within timeout_ns (the caller then records DG_ERR_TIMEOUT and unwinds).
+// not happen within timeout_ns of polling (the caller then records DG_ERR_TIMEOUT and
+// unwinds). The time is summed between consecutive polls, each step clamped to 1 ms: polls
+// are microseconds apart, so a larger step is the global timer being re-synchronised (or
+// the context not running), which must not count as waiting time.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  constexpr uint64_t kMaxStepNs = 1000000;
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  uint64_t last = global_timer_ns(), waited = 0;
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(a, parity)) return true;
-    if (global_timer_ns() - t0 > timeout_ns) return false;
+    const uint64_t now = global_timer_ns();
+    const uint64_t step = now - last;   // unsigned: a backwards step is huge and clamped
+    last = now;
+    waited += step < kMaxStepNs ? step : kMaxStepNs;
+    if (waited > timeout_ns) return false;
   }
 }
 
