@@ -88,12 +88,12 @@ def algorithmic(p):
     if isinstance(p, W.Contiguous):
         v = p.valid_rows
         used = sorted(set(int(g) for g in p.m_indices if g >= 0))
-        by = v * p.K + p.sfa.nbytes + len(used) * (p.N * p.K + p.sfb[0].nbytes) + v * p.N * 2
+        by = v * p.K + p.sfa.nbytes + len(used) * (p.b[0].nbytes + p.sfb[0].nbytes) + v * p.N * 2
         return p.flops, by
     mm = np.minimum(p.masked_m, p.max_m)
     used = int((mm > 0).sum())
     v = int(mm.sum())
-    by = v * p.K + p.sfa.nbytes + used * (p.N * p.K + p.sfb[0].nbytes) + v * p.N * 2
+    by = v * p.K + p.sfa.nbytes + used * (p.b[0].nbytes + p.sfb[0].nbytes) + v * p.N * 2
     return p.flops, by
 
 
@@ -154,16 +154,20 @@ class DeviceProblem:
     def launch(self, i):
         c = self.copies[i % self.R]
         L, p = self.lib, self.p
-        if isinstance(p, W.Dense):
+        if isinstance(p, W.Dense) and p.b_format == "e2m1":
+            L.dg_fp8_fp4_gemm_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
+        elif isinstance(p, W.Dense):
             getattr(L, f"dg_fp8_gemm_{p.layout}")(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
         elif isinstance(p, W.Wgrad):
             L.dg_wgrad_gemm_fp8_fp8_fp32_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"])
         elif isinstance(p, W.KGrouped):
             L.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(c["a"], c["sfa"], c["b"], c["sfb"], c["c"], c["d"], c["ks"])
         elif isinstance(p, W.Contiguous):
-            L.dg_m_grouped_fp8_gemm_nt_contiguous(c["a"], c["sfa"], c["b"], c["sfb"], c["d"], c["idx"])
+            fn = L.dg_m_grouped_fp8_fp4_gemm_nt_contiguous if p.b_format == "e2m1" else L.dg_m_grouped_fp8_gemm_nt_contiguous
+            fn(c["a"], c["sfa"], c["b"], c["sfb"], c["d"], c["idx"])
         else:
-            L.dg_m_grouped_fp8_gemm_nt_masked(c["a"], c["sfa"], c["b"], c["sfb"], c["d"], c["mm"])
+            fn = L.dg_m_grouped_fp8_fp4_gemm_nt_masked if p.b_format == "e2m1" else L.dg_m_grouped_fp8_gemm_nt_masked
+            fn(c["a"], c["sfa"], c["b"], c["sfb"], c["d"], c["mm"])
 
 
 def time_steps(torch, prob, steps, warmup, barrier=None):

@@ -39,6 +39,9 @@ SIGNATURES = [
     ("dg_m_grouped_fp8_gemm_nn_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    ("dg_fp8_fp4_gemm_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("dg_m_grouped_fp8_fp4_gemm_nt_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    ("dg_m_grouped_fp8_fp4_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_pack_sf_ue8m0", _I, [_P, _P, _I, _I, _P]),
     ("dg_get_mk_alignment_for_contiguous_layout", _I, []),
     ("dg_set_mk_alignment_for_contiguous_layout", _I, [_I]),
@@ -280,6 +283,74 @@ def dg_m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, d, masked_m, stream=None) ->
     _check("dg_m_grouped_fp8_gemm_nt_masked",
            lib.dg_m_grouped_fp8_gemm_nt_masked(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m),
                                                G, max_m, N, K, _stream(stream)))
+    return d
+
+
+# --------------------------------------------------------------------------------------
+# FP8 x FP4: b holds packed E2M1 (two per byte, the even element in the low nibble), one
+# UE8M0 scale per row per 32 K packed four per int32: sfb [(G,) K/128, ceil4(N)]
+# --------------------------------------------------------------------------------------
+
+_FP4_DTYPES = (torch.uint8,) + ((torch.float4_e2m1fn_x2,) if hasattr(torch, "float4_e2m1fn_x2") else ())
+
+
+def _fp4(t: torch.Tensor, name: str) -> None:
+    _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _need(t.dtype in _FP4_DTYPES, f"{name} must hold packed E2M1 bytes (uint8 or float4_e2m1fn_x2)")
+
+
+def sf_fp4_shape(n: int, k: int, groups: Optional[int] = None):
+    """Shape of the FP4 operand's packed scales: [(G,) K/128, ceil4(n)]."""
+    shape = (k // 128, 4 * (-(-n // 4)))
+    return shape if groups is None else (groups,) + shape
+
+
+def dg_fp8_fp4_gemm_nt(a, sfa, b, sfb, c, d, stream=None) -> torch.Tensor:
+    """D = C + A @ B.T with B in FP4. a [M, K] e4m3, sfa [KP, ceil4(M)] int32, b [N, K/2] packed
+    E2M1 (32-byte aligned), sfb [K/128, ceil4(N)] int32, c [M, N] bf16 or None, d [M, N] bf16."""
+    lib = load_library()
+    _fp8(a, "a"); _fp4(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d")
+    M, K = a.shape
+    N = b.shape[0]
+    _need(b.shape[1] * 2 == K and tuple(d.shape) == (M, N), "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(M, K) and tuple(sfb.shape) == sf_fp4_shape(N, K), "scale shape mismatch")
+    if c is not None:
+        _bf16(c, "c")
+        _need(tuple(c.shape) == (M, N), "c shape mismatch")
+    _check("dg_fp8_fp4_gemm_nt", lib.dg_fp8_fp4_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                                        M, N, K, _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa, b, sfb, d, m_indices, stream=None) -> torch.Tensor:
+    """Contiguous M-grouped FP8 x FP4 GEMM. a [M_total, K], sfa [KP, ceil4(M_total)], b [G, N, K/2]
+    packed E2M1, sfb [G, K/128, ceil4(N)], d [M_total, N] bf16, m_indices [M_total] int32 (-1 = pad)."""
+    lib = load_library()
+    _fp8(a, "a"); _fp4(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d"); _i32(m_indices, "m_indices")
+    M, K = a.shape
+    G, N, Kh = b.shape
+    _need(Kh * 2 == K and tuple(d.shape) == (M, N) and tuple(m_indices.shape) == (M,), "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(M, K) and tuple(sfb.shape) == sf_fp4_shape(N, K, G), "scale shape mismatch")
+    _check("dg_m_grouped_fp8_fp4_gemm_nt_contiguous",
+           lib.dg_m_grouped_fp8_fp4_gemm_nt_contiguous(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d),
+                                                       _ptr(m_indices), M, N, K, G, _stream(stream)))
+    return d
+
+
+def dg_m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, d, masked_m, stream=None) -> torch.Tensor:
+    """Masked M-grouped FP8 x FP4 GEMM. a [G, max_m, K], sfa [G, KP, ceil4(max_m)], b [G, N, K/2]
+    packed E2M1, sfb [G, K/128, ceil4(N)], d [G, max_m, N] bf16, masked_m [G] int32 on the device."""
+    lib = load_library()
+    _fp8(a, "a"); _fp4(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d"); _i32(masked_m, "masked_m")
+    G, max_m, K = a.shape
+    Gb, N, Kh = b.shape
+    _need(Gb == G and Kh * 2 == K and tuple(d.shape) == (G, max_m, N) and tuple(masked_m.shape) == (G,),
+          "shape mismatch")
+    _need(tuple(sfa.shape) == sf_shape(max_m, K, G) and tuple(sfb.shape) == sf_fp4_shape(N, K, G),
+          "scale shape mismatch")
+    _check("dg_m_grouped_fp8_fp4_gemm_nt_masked",
+           lib.dg_m_grouped_fp8_fp4_gemm_nt_masked(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m),
+                                                   G, max_m, N, K, _stream(stream)))
     return d
 
 

@@ -211,14 +211,14 @@ inline int ceil4(int x) { return 4 * ceil_div(x, 4); }
 // Kernel configurations
 // ------------------------------------------------------------------------------------
 template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps_, int kEpiBufs, bool kHasC,
-          int kKG = 1, int kSplit = 0, bool kOutF32 = false, bool kAMN = false, bool kBMN = false>
+          int kKG = 1, int kSplit = 0, bool kOutF32 = false, bool kAMN = false, bool kBMN = false, bool kBF4 = false>
 struct Launcher {
   static constexpr int kEpiWarps = kEpiWarps_;
-  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>;
+  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4>;
   static constexpr int kBN = BN;
   static constexpr auto kernel() {
     return dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG, kSplit, kOutF32,
-                               kAMN, kBMN>;
+                               kAMN, kBMN, kBF4>;
   }
 
   // Largest number of co-resident clusters of kSplit CTAs (0 if the kernel cannot run).
@@ -285,9 +285,9 @@ struct Launcher {
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, p);
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
-      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d BN=%d stages=%d accum=%d epi_warps=%d grid=%d smem=%d stream_k=%d split=%d\n",
+      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d BN=%d stages=%d accum=%d epi_warps=%d grid=%d smem=%d stream_k=%d split=%d kg=%d fp4=%d\n",
                    static_cast<int>(kKind), p.M, p.N, p.K, p.G, BN, kStages, kNumAccum, kEpiWarps, grid,
-                   Cfg::SMEM_BYTES, p.sk_ctas, kSplit);
+                   Cfg::SMEM_BYTES, p.sk_ctas, kSplit, kKG, kBF4 ? 1 : 0);
     return DG_OK;
   }
 };
@@ -296,27 +296,27 @@ struct Launcher {
 // one 128 x BN tile per pair, each CTA half of K, two K-groups per 3-stage ring slot; the
 // partials are summed through distributed shared memory (no workspace, no atomics).
 constexpr int kSplitWays = 2;
-template <bool kHasC, int BN>
-using SplitLauncher = Launcher<dg::Kind::Dense, BN, 3, 1, 4, 1, kHasC, 2, kSplitWays>;
+template <bool kHasC, int BN, bool kBF4 = false>
+using SplitLauncher = Launcher<dg::Kind::Dense, BN, 3, 1, 4, 1, kHasC, 2, kSplitWays, false, false, false, kBF4>;
 
-template <bool kHasC>
+template <bool kHasC, bool kBF4 = false>
 int split_max_clusters(int bn) {
   switch (bn) {
-    case 64: return SplitLauncher<kHasC, 64>::max_clusters();
-    case 96: return SplitLauncher<kHasC, 96>::max_clusters();
-    case 128: return SplitLauncher<kHasC, 128>::max_clusters();
+    case 64: return SplitLauncher<kHasC, 64, kBF4>::max_clusters();
+    case 96: return SplitLauncher<kHasC, 96, kBF4>::max_clusters();
+    case 128: return SplitLauncher<kHasC, 128, kBF4>::max_clusters();
   }
   return 0;
 }
 
-template <bool kHasC>
+template <bool kHasC, bool kBF4 = false>
 dg_status launch_split(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                        const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
                        cudaStream_t stream) {
   switch (bn) {
-    case 64: return SplitLauncher<kHasC, 64>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
-    case 96: return SplitLauncher<kHasC, 96>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
-    case 128: return SplitLauncher<kHasC, 128>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 64: return SplitLauncher<kHasC, 64, kBF4>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 96: return SplitLauncher<kHasC, 96, kBF4>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
+    case 128: return SplitLauncher<kHasC, 128, kBF4>::launch(ta, tb, tsa, tsb, td, p, grid, stream);
   }
   return DG_ERR_INVALID_ARG;
 }
@@ -325,7 +325,7 @@ dg_status launch_split(int bn, const CUtensorMap& ta, const CUtensorMap& tb, con
 // 64 / 96 / 128 whose tiles fit one per co-resident CTA pair, if that keeps at least 3/4
 // of the SMs busy and gives each CTA two or more K-groups; 0 = use stream-K instead.
 // DG_SPLIT=0 disables the split form, DG_SPLIT_BN forces a width (if it fits).
-int pick_split_bn(int M, int N, int K, int sms, bool with_c) {
+int pick_split_bn(int M, int N, int K, int sms, bool with_c, bool fp4 = false) {
   if (const char* f = std::getenv("DG_SPLIT")) {
     if (f[0] == '0') return 0;
   }
@@ -335,7 +335,8 @@ int pick_split_bn(int M, int N, int K, int sms, bool with_c) {
   const long long m_blocks = ceil_div(M, 128);
   for (int bn : {64, 96, 128}) {
     if (forced && bn != forced) continue;
-    const int max_cl = std::min(with_c ? split_max_clusters<true>(bn) : split_max_clusters<false>(bn),
+    const int max_cl = std::min(fp4 ? (with_c ? split_max_clusters<true, true>(bn) : split_max_clusters<false, true>(bn))
+                                    : (with_c ? split_max_clusters<true>(bn) : split_max_clusters<false>(bn)),
                                 sms / kSplitWays);
     const long long tiles = m_blocks * ceil_div(N, bn);
     if (max_cl > 0 && tiles <= max_cl && tiles * kSplitWays * 4 >= 3LL * sms) return bn;
@@ -348,10 +349,33 @@ int pick_split_bn(int M, int N, int K, int sms, bool with_c) {
 //   192: 4-stage ring, double-buffered accumulators (TMEM 2 x 192 columns)
 //   256: 4-stage ring, single accumulator (TMEM 256 columns; 2 x 256 + scales exceeds 512)
 //   128 x 2: two K-groups per stage (64 KB stages, 3 of them), for HBM-bound stream-K shapes
-template <dg::Kind kKind, bool kHasC, bool kOutF32 = false, bool kAMN = false, bool kBMN = false>
+//   FP4 B (kBF4): dense 128, 128 x 2 and 256; contiguous 128 and 256; masked 128 and 192
+template <dg::Kind kKind, bool kHasC, bool kOutF32 = false, bool kAMN = false, bool kBMN = false, bool kBF4 = false>
 dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                     const CUtensorMap& tsb, const CUtensorMap& td, const dg::Params& p, int grid,
                     cudaStream_t stream, int kgroups_per_stage = 1) {
+  if constexpr (kBF4) {
+    static_assert(!kOutF32 && !kAMN && !kBMN, "FP4 B: K-major operands, BF16 output");
+    if constexpr (kKind == dg::Kind::Dense) {
+      if (kgroups_per_stage == 2 && bn == 128)
+        return Launcher<kKind, 128, 3, 2, 4, 1, kHasC, 2, 0, false, false, false, true>::launch(ta, tb, tsa, tsb, td,
+                                                                                                  p, grid, stream);
+    }
+    if constexpr (kKind == dg::Kind::Masked) {
+      if (bn == 192)
+        return Launcher<kKind, 192, 4, 2, 4, 2, kHasC, 1, 0, false, false, false, true>::launch(ta, tb, tsa, tsb, td,
+                                                                                                  p, grid, stream);
+    }
+    if (bn == 128)
+      return Launcher<kKind, 128, 5, 2, 4, 2, kHasC, 1, 0, false, false, false, true>::launch(ta, tb, tsa, tsb, td, p,
+                                                                                                grid, stream);
+    if constexpr (kKind != dg::Kind::Masked) {
+      if (bn == 256)
+        return Launcher<kKind, 256, 4, 1, 4, 1, kHasC, 1, 0, false, false, false, true>::launch(ta, tb, tsa, tsb, td,
+                                                                                                  p, grid, stream);
+    }
+    return DG_ERR_INVALID_ARG;
+  }
   if constexpr (kKind == dg::Kind::Dense) {
     if (kgroups_per_stage == 2 && bn == 128)
       return Launcher<kKind, 128, 3, 2, 4, 1, kHasC, 2, 0, kOutF32, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, p, grid,
@@ -539,6 +563,39 @@ bool map_out_f32(CUtensorMap* m, void* base, int rows, int N) {
   const uint64_t strides[1] = {static_cast<uint64_t>(N) * 4};
   const uint32_t box[2] = {32, 32};
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// FP4 operand ([(G,) rows, K/2] bytes of packed E2M1): 128-element x box_rows boxes of the
+// 16U4_ALIGN16B type (each 8 bytes land in a 16-byte shared-memory chunk), 128-byte swizzle.
+// The base must be 32-byte aligned and K/2 a multiple of 32 bytes.
+bool map_operand_fp4(CUtensorMap* m, const void* base, int G, int rows, int K, int box_rows) {
+  const uint64_t row_bytes = static_cast<uint64_t>(K) / 2;
+  if (G <= 0) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {128, static_cast<uint32_t>(box_rows)};
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows), static_cast<uint64_t>(G)};
+  const uint64_t strides[2] = {row_bytes, row_bytes * rows};
+  const uint32_t box[3] = {128, static_cast<uint32_t>(box_rows), 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// FP4 B scale words [(G,) K/128, ceil4(N)] int32 (word (q, n): the four 32-wide blocks of
+// K-group q of row n), loaded as box_n words x kg K-groups.
+bool map_sf_fp4(CUtensorMap* m, const int32_t* base, int G, int N, int KG, int box_n, int kg) {
+  const uint64_t w = static_cast<uint64_t>(ceil4(N));
+  if (G <= 0) {
+    const uint64_t dims[2] = {w, static_cast<uint64_t>(KG)};
+    const uint64_t strides[1] = {w * 4};
+    const uint32_t box[2] = {static_cast<uint32_t>(box_n), static_cast<uint32_t>(kg)};
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  const uint64_t dims[3] = {w, static_cast<uint64_t>(KG), static_cast<uint64_t>(G)};
+  const uint64_t strides[2] = {w * 4, w * 4 * KG};
+  const uint32_t box[3] = {static_cast<uint32_t>(box_n), static_cast<uint32_t>(kg), 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Dense / contiguous GEMM on CTA pairs: converts the scale words into tcgen05.cp chunks in
@@ -748,15 +805,15 @@ __global__ void pack_sf_kernel(const float* __restrict__ sf, int32_t* __restrict
 
 // Dense GEMM on the single-CTA kernel: whole tiles (tile mode) or, with fewer tiles than
 // SMs, stream-K. kOutF32: FP32 C / D (weight-gradient form), else BF16.
-template <bool kOutF32, bool kAMN = false, bool kBMN = false>
+template <bool kOutF32, bool kAMN = false, bool kBMN = false, bool kBF4 = false>
 dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
                            const void* c, void* d, int M, int N, int K, int BN, int sms, cudaStream_t stream) {
   DeviceState* ds = &dsr;
   const int KP = ceil_div(K / 128, 4);
   CUtensorMap ta, tb, tsa, tsb, td;
   if (!(kAMN ? map_operand_mn(&ta, a, M, K) : map_operand_2d(&ta, a, M, K, 128)) ||
-      !(kBMN ? map_operand_mn(&tb, b, N, K) : map_operand_2d(&tb, b, N, K, BN)) ||
-      !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
+      !(kBF4 ? map_operand_fp4(&tb, b, 0, N, K, BN) : kBMN ? map_operand_mn(&tb, b, N, K) : map_operand_2d(&tb, b, N, K, BN)) ||
+      !map_sf(&tsa, sfa, 0, M, KP, 128) || (!kBF4 && !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8)) ||
       !(kOutF32 ? map_out_f32(&td, d, M, N) : map_out(&td, d, 0, M, N)))
     return DG_ERR_CUDA;
   dg::Params p{};
@@ -804,8 +861,12 @@ dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, 
   } else {
     kg = 1;   // tile mode: whole tiles, one K-group per stage
   }
-  if (c) return launch_bn<dg::Kind::Dense, true, kOutF32, kAMN, kBMN>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
-  return launch_bn<dg::Kind::Dense, false, kOutF32, kAMN, kBMN>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
+  if constexpr (kBF4) {
+    if (!map_sf_fp4(&tsb, sfb, 0, N, K / 128, BN, kg)) return DG_ERR_CUDA;
+  }
+  if (c)
+    return launch_bn<dg::Kind::Dense, true, kOutF32, kAMN, kBMN, kBF4>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
+  return launch_bn<dg::Kind::Dense, false, kOutF32, kAMN, kBMN, kBF4>(BN, ta, tb, tsa, tsb, td, p, grid, stream, kg);
 }
 
 }  // namespace
@@ -1272,6 +1333,141 @@ dg_status dg_set_debug(int fault_mode, unsigned long long wait_timeout_ns) {
   g_fault.store(fault_mode);
   g_timeout_ns.store(wait_timeout_ns);
   return DG_OK;
+}
+
+}  // extern "C"
+
+// ======================================================================================
+// FP8 x FP4: A E4M3 (scales 1 x 128), B packed E2M1 (one UE8M0 scale per row per 32 K)
+// ======================================================================================
+namespace {
+
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+// Tile width for FP4 B: the masked form (short K, HBM-bound) takes 192 when N > 128, the
+// others the wider of 256 / 128 unless it wastes columns. DG_FORCE_BN overrides (128 or
+// 256; 192 for the masked form).
+int pick_bn_fp4(dg::Kind kind, int N) {
+  if (const char* f = std::getenv("DG_FORCE_BN")) {
+    const int v = std::atoi(f);
+    if (v == 128 || (v == 256 && kind != dg::Kind::Masked) || (v == 192 && kind == dg::Kind::Masked)) return v;
+  }
+  if (kind == dg::Kind::Masked) return N > 128 ? 192 : 128;
+  return ceil_div(N, 256) * 256 <= ceil_div(N, 128) * 128 ? 256 : 128;
+}
+
+dg_status check_fp4_pointers(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                             const void* d) {
+  if (!a || !sfa || !b || !sfb || !d) return DG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned32(b) || !aligned16(sfb) || !aligned16(d) || (c && !aligned16(c)))
+    return DG_ERR_MISALIGNED;
+  return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dg_status dg_fp8_fp4_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* c,
+                             void* d, int M, int N, int K, cudaStream_t stream) {
+  if (M < 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (M == 0) return DG_OK;
+  if (dg_status s = check_fp4_pointers(a, sfa, b, sfb, c, d); s != DG_OK) return s;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  const int sms = sms_to_use(*ds);
+  const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
+  if (tiles128 < sms) {
+    // few tiles: split-K over CTA pairs when the tiles fill the GPU that way, else stream-K
+    if (const int sbn = pick_split_bn(M, N, K, sms, c != nullptr, true); sbn > 0) {
+      CUtensorMap ta, tb, tsa, tsb, td;
+      if (!map_operand_2d(&ta, a, M, K, 128) || !map_operand_fp4(&tb, b, 0, N, K, sbn) ||
+          !map_sf(&tsa, sfa, 0, M, ceil_div(K / 128, 4), 128) || !map_sf_fp4(&tsb, sfb, 0, N, K / 128, sbn, 2) ||
+          !map_out(&td, d, 0, M, N))
+        return DG_ERR_CUDA;
+      dg::Params p{};
+      p.M = M;
+      p.N = N;
+      p.K = K;
+      p.G = 1;
+      p.c = static_cast<const __nv_bfloat16*>(c);
+      p.d = static_cast<__nv_bfloat16*>(d);
+      p.status = ds->status;
+      p.timeout_ns = wait_timeout_ns();
+      p.fault = g_fault.load();
+      const int grid = static_cast<int>(static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, sbn)) * kSplitWays;
+      if (c) return launch_split<true, true>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
+      return launch_split<false, true>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
+    }
+    return run_dense_single<false, false, false, true>(*ds, a, sfa, b, sfb, c, d, M, N, K, 128, sms, stream);
+  }
+  return run_dense_single<false, false, false, true>(*ds, a, sfa, b, sfb, c, d, M, N, K,
+                                                     pick_bn_fp4(dg::Kind::Dense, N), sms, stream);
+}
+
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b,
+                                                  const int32_t* sfb, void* d, const int32_t* m_indices, int M_total,
+                                                  int N, int K, int G, cudaStream_t stream) {
+  if (M_total < 0 || G <= 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (M_total == 0) return DG_OK;
+  if (!m_indices) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_fp4_pointers(a, sfa, b, sfb, nullptr, d); s != DG_OK) return s;
+  if (reinterpret_cast<uintptr_t>(m_indices) & 3u) return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  const int BN = pick_bn_fp4(dg::Kind::Contiguous, N);
+  CUtensorMap ta, tb, tsa, tsb, td;
+  if (!map_operand_2d(&ta, a, M_total, K, 128) || !map_operand_fp4(&tb, b, G, N, K, BN) ||
+      !map_sf(&tsa, sfa, 0, M_total, ceil_div(K / 128, 4), 128) || !map_sf_fp4(&tsb, sfb, G, N, K / 128, BN, 1) ||
+      !map_out(&td, d, 0, M_total, N))
+    return DG_ERR_CUDA;
+  dg::Params p{};
+  p.M = M_total;
+  p.N = N;
+  p.K = K;
+  p.G = G;
+  p.m_indices = m_indices;
+  p.d = static_cast<__nv_bfloat16*>(d);
+  p.status = ds->status;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
+  const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
+  const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
+  return launch_bn<dg::Kind::Contiguous, false, false, false, false, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
+}
+
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              void* d, const int32_t* masked_m, int G, int max_m, int N, int K,
+                                              cudaStream_t stream) {
+  if (G <= 0 || max_m < 0) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_common(N, K); s != DG_OK) return s;
+  if (max_m == 0) return DG_OK;
+  if (!masked_m) return DG_ERR_INVALID_ARG;
+  if (dg_status s = check_fp4_pointers(a, sfa, b, sfb, nullptr, d); s != DG_OK) return s;
+  if (reinterpret_cast<uintptr_t>(masked_m) & 3u) return DG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  const int BN = pick_bn_fp4(dg::Kind::Masked, N);
+  CUtensorMap ta, tb, tsa, tsb, td;
+  if (!map_operand_3d(&ta, a, G, max_m, K, 128) || !map_operand_fp4(&tb, b, G, N, K, BN) ||
+      !map_sf(&tsa, sfa, G, max_m, ceil_div(K / 128, 4), 128) || !map_sf_fp4(&tsb, sfb, G, N, K / 128, BN, 1) ||
+      !map_out(&td, d, G, max_m, N))
+    return DG_ERR_CUDA;
+  dg::Params p{};
+  p.M = max_m;
+  p.N = N;
+  p.K = K;
+  p.G = G;
+  p.masked_m = masked_m;
+  p.d = static_cast<__nv_bfloat16*>(d);
+  p.status = ds->status;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
+  const long long tiles = static_cast<long long>(G) * ceil_div(max_m, 128) * ceil_div(N, BN);
+  const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
+  return launch_bn<dg::Kind::Masked, false, false, false, false, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
 }
 
 }  // extern "C"

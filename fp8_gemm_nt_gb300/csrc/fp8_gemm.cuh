@@ -96,7 +96,16 @@ __host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) 
 // kSplit > 0 (dense only): split-K over a cluster of kSplit CTAs. Each cluster computes one
 // tile, CTA r of the cluster K-groups [r, r+1) * K / kSplit of it; the FP32 partials meet
 // in shared memory and CTA r sums (in rank order) and stores columns [r, r+1) * BN / kSplit.
-template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, int kKG = 1, int kSplit = 0>
+//
+// kBF4: B is FP4 (E2M1, two per byte) with one UE8M0 scale per row per 32 K. A TMA load of
+// the 16U4_ALIGN16B type spreads each 8 bytes of B over a 16-byte shared-memory chunk (the
+// upper 8 bytes zero), which is the layout tcgen05.mma reads an E2M1 operand in, so the B
+// stage has the FP8 shape (BN rows x 128 bytes per K-group) while the transaction count is
+// the global bytes read (BN x 64 per K-group; measured on GB300). Every stage then carries
+// the scale words: A's packed word per row (as in FP8) and, per K-group, one word per B row
+// holding the scales of its four 32-wide blocks.
+template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, int kKG = 1, int kSplit = 0,
+          bool kBF4 = false>
 struct Config {
   static_assert(kKG == 1 || kKG == 2, "one or two K-groups per stage");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
@@ -113,13 +122,16 @@ struct Config {
   static constexpr int B_SUB = BN * BLOCK_K;                    // one K-group of B
   static constexpr int A_BYTES = kKG * A_SUB;                   // per stage
   static constexpr int B_BYTES = kKG * B_SUB;
+  static constexpr int B_TX = kBF4 ? B_BYTES / 2 : B_BYTES;     // global bytes of a stage's B boxes
   static constexpr int SFB_CHUNKS = ceil_div_c(BN, 128);        // 128-row chunks of B scale rows
+  static constexpr int SFB_SETS = kBF4 ? kKG : 1;               // B scale sets in TMEM per scale stage
+  static constexpr int SF_RAW_B_BYTES = kBF4 ? BN * 4 * kKG : 8 * 4;   // FP4: BN row words per K-group
   static constexpr int SF_RAW_A = 0;                            // 128 words as loaded (row-major)
-  static constexpr int SF_RAW_B = 512;                          // 8 block words as loaded
-  static constexpr int SF_UT_A = 1024;                          // 32 rows x 16 B tcgen05.cp source
-  static constexpr int SF_UT_B = 1536;                          // SFB_CHUNKS x (32 rows x 16 B)
-  static constexpr int SF_BYTES = SF_UT_B + SFB_CHUNKS * 512;
-  static constexpr int SF_TX_BYTES = BLOCK_M * 4 + 8 * 4;       // SFA box {128,1} + SFB box {8,1}
+  static constexpr int SF_RAW_B = 512;                          // B words as loaded
+  static constexpr int SF_UT_A = 512 + ceil_div_c(SF_RAW_B_BYTES > 512 ? SF_RAW_B_BYTES : 512, 128) * 128;
+  static constexpr int SF_UT_B = SF_UT_A + 512;                 // SFB_SETS x SFB_CHUNKS x (32 rows x 16 B)
+  static constexpr int SF_BYTES = SF_UT_B + SFB_SETS * SFB_CHUNKS * 512;
+  static constexpr int SF_TX_BYTES = BLOCK_M * 4 + SF_RAW_B_BYTES;   // SFA box {128,1} + SFB box
   static constexpr int EPI_BUF_BYTES = 32 * 128;                // 32 rows x 64 BF16 columns
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + kStages * A_BYTES;
@@ -134,8 +146,8 @@ struct Config {
   // tensor memory columns
   static constexpr int ACC_COLS = kNumAccum * BN;
   static constexpr int SFA_COL = ACC_COLS;                      // 2 buffers x 4 columns
-  static constexpr int SFB_COL = SFA_COL + 8;                   // 2 buffers x 4*SFB_CHUNKS columns
-  static constexpr int TMEM_USED = SFB_COL + 2 * 4 * SFB_CHUNKS;
+  static constexpr int SFB_COL = SFA_COL + 8;                   // 2 buffers x SFB_SETS x 4*SFB_CHUNKS columns
+  static constexpr int TMEM_USED = SFB_COL + 2 * SFB_SETS * 4 * SFB_CHUNKS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                  : TMEM_USED <= 256 ? 256 : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
@@ -392,12 +404,14 @@ __device__ __forceinline__ float4 ld_global_cg_v4f(const float* p) {
 // between 128-byte atoms along M/N) and SBO = 1024 (stride between 8-row groups along K),
 // and each 32-deep K step of the MMA advances it by 32 rows = 4 KB.
 template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC, int kKG = 1,
-          int kSplit = 0, bool kOutF32 = false, bool kAMN = false, bool kBMN = false>
-__global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>::kThreads, 1)
+          int kSplit = 0, bool kOutF32 = false, bool kAMN = false, bool kBMN = false, bool kBF4 = false>
+__global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_d, const Params p) {
-  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit>;
+  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4>;
+  static_assert(!kBF4 || (!kAMN && !kBMN && !kOutF32 && kKind != Kind::KGrouped),
+                "FP4 B: K-major operands, BF16 output, dense / contiguous / masked forms");
   static_assert(kSplit == 0 || kKind == Kind::Dense, "split-K clusters: dense form only");
   static_assert(!kOutF32 || ((kKind == Kind::Dense || kKind == Kind::KGrouped) && kSplit == 0),
                 "FP32 output: dense (tile mode / stream-K) and K-grouped forms only");
@@ -505,9 +519,9 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
             on_timeout();
             goto producer_done;
           }
-          const bool with_sf = kb == seg.kb_begin || (kb % 4) == 0;
+          const bool with_sf = kBF4 || kb == seg.kb_begin || (kb % 4) == 0;
           uint64_t* fb = &full_bar[stage];
-          mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + (with_sf ? C::SF_TX_BYTES : 0));
+          mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_TX + (with_sf ? C::SF_TX_BYTES : 0));
           uint8_t* sa = smem + C::OFF_A + stage * C::A_BYTES;
           uint8_t* sb = smem + C::OFF_B + stage * C::B_BYTES;
           uint8_t* ssf = smem + C::OFF_SF + stage * C::SF_BYTES;
@@ -544,7 +558,14 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
             } else {
               tma_load_2d(ssf + C::SF_RAW_A, &tm_sfa, fb, row0, seg.sf_row + kb / 4);
             }
-            if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
+            if constexpr (kBF4) {
+              // kKG rows (K-groups) of BN per-row words
+              if constexpr (kKind == Kind::Dense) {
+                tma_load_2d(ssf + C::SF_RAW_B, &tm_sfb, fb, n0, kb);
+              } else {
+                tma_load_3d(ssf + C::SF_RAW_B, &tm_sfb, fb, n0, kb, seg.g);
+              }
+            } else if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
               tma_load_2d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, seg.sf_row + kb / 4);
             } else {
               tma_load_3d(ssf + C::SF_RAW_B, &tm_sfb, fb, sfb_x, kb / 4, seg.g);
@@ -573,8 +594,9 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     // GB300: each tcgen05.mma issue costs ~75 cycles and a warp-wide wait path ~400, so the
     // loop, not the tensor pipe, set the pace).
     if (lane == 0) {
-      constexpr uint32_t kIdesc =
-          make_idesc_mxf8_e4m3(BLOCK_M, BN) | (kAMN ? 1u << 15 : 0u) | (kBMN ? 1u << 16 : 0u);
+      // B format field [10,13): 0 = E4M3, 5 = E2M1
+      constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(BLOCK_M, BN) | (kAMN ? 1u << 15 : 0u) |
+                                  (kBMN ? 1u << 16 : 0u) | (kBF4 ? 5u << 10 : 0u);
       const uint64_t a_desc0 =
           make_smem_desc(smem_addr(smem + C::OFF_A), kAMN ? 128 * BLOCK_K : 16, 1024, kLayoutSwizzle128B);
       const uint64_t b_desc0 =
@@ -601,7 +623,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
               on_timeout();
               goto mma_done;
             }
-            if (kb == seg.kb_begin || kb % 4 == 0) {
+            if (kBF4 || kb == seg.kb_begin || kb % 4 == 0) {
               // the scale warp has rearranged this stage's scale words for tcgen05.cp
               if (!mbar_wait(&sf_ready_bar[stage], (sf_parity >> stage) & 1u, p.timeout_ns)) {
                 on_timeout();
@@ -612,11 +634,11 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
               const uint32_t buf = sf_iter & 1;
               ++sf_iter;
               sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
-              sfb_tmem = tmem_base + C::SFB_COL + 4 * C::SFB_CHUNKS * buf;
+              sfb_tmem = tmem_base + C::SFB_COL + 4 * C::SFB_SETS * C::SFB_CHUNKS * buf;
               const uint64_t sf_desc = sf_desc0 + ((stage * C::SF_BYTES) >> 4);
               tmem_copy_32x128b_warpx4(sfa_tmem, sf_desc + (C::SF_UT_A >> 4));
 #pragma unroll
-              for (int ch = 0; ch < C::SFB_CHUNKS; ++ch)
+              for (int ch = 0; ch < C::SFB_SETS * C::SFB_CHUNKS; ++ch)
                 tmem_copy_32x128b_warpx4(sfb_tmem + 4 * ch, sf_desc + ((C::SF_UT_B + 512 * ch) >> 4));
             } else {
               tc_fence_after();
@@ -627,11 +649,15 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
               if (kb + j < seg.kb_end) {
                 const uint64_t adesc = a_desc0 + ((stage * C::A_BYTES + j * C::A_SUB) >> 4);
                 const uint64_t bdesc = b_desc0 + ((stage * C::B_BYTES + j * C::B_SUB) >> 4);
-                const uint32_t idesc = idesc_with_sf_id(kIdesc, (kb + j) % 4, (kb + j) % 4);
 #pragma unroll
-                for (int k = 0; k < BLOCK_K / 32; ++k)
-                  mma_mxf8_block_scale(d_tmem, adesc + kAStep * k, bdesc + kBStep * k, idesc, sfa_tmem, sfb_tmem,
+                for (int k = 0; k < BLOCK_K / 32; ++k) {
+                  // A: byte (kb + j) % 4 of its packed word; B (FP8): the same byte of the block
+                  // word, (FP4): byte k of K-group j's row word (the k-th 32-wide block)
+                  const uint32_t idesc = idesc_with_sf_id(kIdesc, (kb + j) % 4, kBF4 ? k : (kb + j) % 4);
+                  mma_mxf8_block_scale(d_tmem, adesc + kAStep * k, bdesc + kBStep * k, idesc, sfa_tmem,
+                                       sfb_tmem + (kBF4 ? 4 * C::SFB_CHUNKS * j : 0),
                                        (kb + j != seg.kb_begin || k != 0) ? 1u : 0u);
+                }
               }
             }
             tc_commit(&empty_bar[stage]);
@@ -666,22 +692,41 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
           if (lane == 0) on_timeout();
           goto sf_done;
         }
-        if (kb == seg.kb_begin || kb % 4 == 0) {
+        if (kBF4 || kb == seg.kb_begin || kb % 4 == 0) {
           const uint32_t sf_base = smem_addr(smem + C::OFF_SF + stage * C::SF_BYTES);
           const uint32_t a0 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * lane);
           const uint32_t a1 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 32));
           const uint32_t a2 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 64));
           const uint32_t a3 = ld_shared_u32(sf_base + C::SF_RAW_A + 4 * (lane + 96));
           st_shared_v4(sf_base + C::SF_UT_A + 16 * lane, a0, a1, a2, a3);
+          if constexpr (kBF4) {
+            // K-group s of the stage: tile row r's word at raw word s * BN + r (rows past BN
+            // read as 0: their columns are never stored)
 #pragma unroll
-          for (int ch = 0; ch < C::SFB_CHUNKS; ++ch) {
-            uint32_t w[4];
+            for (int s = 0; s < C::SFB_SETS; ++s) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int n = n0 + 128 * ch + static_cast<int>(lane) + 32 * j;
-              w[j] = ld_shared_u32(sf_base + C::SF_RAW_B + 4 * (n / SF_BLOCK_N - sfb_x));
+              for (int ch = 0; ch < C::SFB_CHUNKS; ++ch) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int r = 128 * ch + static_cast<int>(lane) + 32 * j;
+                  w[j] = r < BN ? ld_shared_u32(sf_base + C::SF_RAW_B + 4 * (s * BN + r)) : 0u;
+                }
+                st_shared_v4(sf_base + C::SF_UT_B + 512 * (s * C::SFB_CHUNKS + ch) + 16 * lane, w[0], w[1], w[2],
+                             w[3]);
+              }
             }
-            st_shared_v4(sf_base + C::SF_UT_B + 512 * ch + 16 * lane, w[0], w[1], w[2], w[3]);
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < C::SFB_CHUNKS; ++ch) {
+              uint32_t w[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int n = n0 + 128 * ch + static_cast<int>(lane) + 32 * j;
+                w[j] = ld_shared_u32(sf_base + C::SF_RAW_B + 4 * (n / SF_BLOCK_N - sfb_x));
+              }
+              st_shared_v4(sf_base + C::SF_UT_B + 512 * ch + 16 * lane, w[0], w[1], w[2], w[3]);
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();

@@ -193,6 +193,45 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa,
                                           cudaStream_t stream);
 
 /*
+ * FP8 x FP4 GEMMs: D = C + A @ B.T with A in E4M3 and B in FP4 (DeepGEMM news entry of
+ * 2026.04.16, "FP8xFP4 GEMM"; the Mega MoE section of the same README runs its linear layers
+ * as "FP8xFP4" on weights given as "FP4 with UE8M0 SF"). The pages say no more; the readings
+ * taken here:
+ *   - B is OCP MX FP4 (E2M1: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}), two codes per byte, element 2j
+ *     of a row in the low nibble of byte j: b is uint8 [N, K/2] row-major.
+ *   - B has one UE8M0 scale per row per 32 consecutive K-elements (the MX block), packed four
+ *     per int32 along K and stored MN-major: sfb is int32 [KG, ceil4(N)], word (q, n) holding
+ *     the scales of K-elements 128q + 32j .. 128q + 32j + 31 of row n in byte j.
+ *   - A, sfa, c and d are exactly as in dg_fp8_gemm_nt (A scales 1 x 128, BF16 C and D).
+ *     D[m, n] = C[m, n] + sum_k sA[m, k / 128] * sB[n, k / 32] * A[m, k] * B[n, k].
+ * b must be 32-byte aligned (the 16U4 tensor-map type's rule), every other pointer 16-byte
+ * aligned (DG_ERR_MISALIGNED otherwise). Shape limits and errors as dg_fp8_gemm_nt.
+ */
+dg_status dg_fp8_fp4_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                             const void* c, void* d, int M, int N, int K, cudaStream_t stream);
+
+/*
+ * Contiguous M-grouped FP8 x FP4 GEMM: dg_m_grouped_fp8_gemm_nt_contiguous with each expert's
+ * B in FP4 as above.
+ *   b   : uint8 [G, N, K/2] (packed E2M1), 32-byte aligned.
+ *   sfb : int32 [G, KG, ceil4(N)] (per-row, per-32 scales packed as for dg_fp8_fp4_gemm_nt).
+ *   a, sfa, d, m_indices, M_total, N, K, G : as dg_m_grouped_fp8_gemm_nt_contiguous.
+ */
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b,
+                                                  const int32_t* sfb, void* d, const int32_t* m_indices,
+                                                  int M_total, int N, int K, int G, cudaStream_t stream);
+
+/*
+ * Masked M-grouped FP8 x FP4 GEMM: dg_m_grouped_fp8_gemm_nt_masked with each expert's B in FP4.
+ *   b   : uint8 [G, N, K/2] (packed E2M1), 32-byte aligned.
+ *   sfb : int32 [G, KG, ceil4(N)].
+ *   a, sfa, d, masked_m, G, max_m, N, K : as dg_m_grouped_fp8_gemm_nt_masked.
+ */
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b,
+                                              const int32_t* sfb, void* d, const int32_t* masked_m,
+                                              int G, int max_m, int N, int K, cudaStream_t stream);
+
+/*
  * Scale-factor packing ("Utilities": get_mn_major_tma_aligned_packed_ue8m0_tensor /
  * transform_sf_into_required_layout). Converts FP32 scales into the packed, MN-major,
  * TMA-aligned UE8M0 words the GEMMs consume.

@@ -42,6 +42,9 @@ Pins: tests/test_oracle_pins.py checks this module against the OCP code tables,
 torch's own FP8/BF16 decoders, brute-force rational arithmetic on tiny inputs,
 identity/one-hot operands, exact power-of-two scale invariance, the C-only case and
 the grouped-equals-per-expert-dense identity; planted mistakes must fail a pin.
+The FP8 x FP4 forms (end of the module) are pinned the same way: the OCP E2M1 table,
+exact rationals with an independent nibble unpacking, one-hot closed forms, and the
+identity with the FP8 form when every FP4 value and scale is also an FP8 one.
 """
 from __future__ import annotations
 
@@ -297,6 +300,128 @@ def m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, masked_m, G: int, max_m: int, N
             sa = unpack_sf(sfa[g], max_m, KG)[:m]
             D[i, :m] = _scaled_gemm(np.asarray(a[g])[:m], sa, np.asarray(b[g]),
                                     unpack_sf(sfb[g], NB, KG), K)
+    return D, valid
+
+
+# --------------------------------------------------------------------------------------
+# FP8 x FP4: E4M3 activations against E2M1 weights
+# --------------------------------------------------------------------------------------
+# The pages name the GEMM only (the DeepGEMM news entry of 2026.04.16, "FP8xFP4 GEMM", and
+# the Mega MoE section, whose linear layers are "FP8xFP4" with weights "FP4 with UE8M0 SF").
+# Readings, each the plainest one the pages allow:
+# * the FP4 operand is OCP MX FP4 (E2M1: sign, 2 exponent bits with bias 1, 1 mantissa
+#   bit; +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}; no infinities or NaN), two codes per byte, element
+#   2j in the low nibble of byte j of its row (B stored [N, K/2] bytes, K-major as in NT);
+# * its UE8M0 scales follow the MX block: one per row per 32 consecutive K-elements, packed
+#   four per int32 along K (block 4q + j in byte j of word q) and stored MN-major
+#   [K/128, ceil4(N)] words, the same "packed, transposed" format as A's scales;
+# * A, its scales, C and D are exactly as in fp8_gemm_nt.
+# Exactness: E4M3 x E2M1 products are multiples of 2**-10 below 2**12, so each 32-term block
+# sum is exact in FP64 and the only rounding is the FP64 sum over blocks.
+
+FP4_BLOCK_K = 32
+
+
+def _e2m1_table() -> np.ndarray:
+    """All 16 E2M1 codes decoded from the format's definition."""
+    t = np.empty(16, np.float64)
+    for code in range(16):
+        s = -1.0 if code & 0x8 else 1.0
+        e = (code >> 1) & 0x3
+        m = code & 0x1
+        t[code] = s * (0.5 * m if e == 0 else (1.0 + 0.5 * m) * 2.0 ** (e - 1))
+    return t
+
+
+_E2M1 = _e2m1_table()
+
+
+def decode_e2m1(codes: np.ndarray) -> np.ndarray:
+    """E2M1 codes (0..15) -> float64."""
+    return _E2M1[np.asarray(codes, dtype=np.uint8) & 0xF]
+
+
+def unpack_e2m1(packed: np.ndarray, K: int) -> np.ndarray:
+    """Packed FP4 bytes [..., K/2] -> codes [..., K]: element 2j is the low nibble of byte j."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (K,), np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def _scaled_gemm_fp4(a_codes, sa_codes, b_codes, sb_codes, K: int) -> np.ndarray:
+    """sum_j sA[:, j // 4] * sB[:, j] * (A_j @ B_j.T) over the 32-wide blocks j, in FP64.
+
+    a_codes: E4M3 [R, K]; sa_codes: UE8M0 [R, K/128]; b_codes: E2M1 [N, K];
+    sb_codes: UE8M0 [N, K/32] (one per row per 32-wide block of B).
+    """
+    A = decode_e4m3(a_codes)
+    B = decode_e2m1(b_codes)
+    sA = decode_ue8m0(sa_codes)
+    sB = decode_ue8m0(sb_codes)
+    D = np.zeros((A.shape[0], B.shape[0]), np.float64)
+    for j in range(K // FP4_BLOCK_K):
+        ks = slice(j * FP4_BLOCK_K, (j + 1) * FP4_BLOCK_K)
+        D += sA[:, j * FP4_BLOCK_K // GROUP_K, None] * (A[:, ks] @ B[:, ks].T) * sB[None, :, j]
+    return D
+
+
+def fp8_fp4_gemm_nt(a, sfa, b, sfb, c: Optional[np.ndarray], M: int, N: int, K: int,
+                    rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """D = C + A @ B.T with A E4M3 (scales 1 x 128) and B E2M1 (scales 1 x 32), in FP64
+    (DeepGEMM news 2026.04.16 "FP8xFP4 GEMM"; README "Interfaces / Notices" for A, C, D and
+    the scale packing; the readings above for B).
+
+    a: uint8 [M, K]; sfa: int32 [ceil(K/512), ceil4(M)]; b: uint8 [N, K/2] (packed E2M1);
+    sfb: int32 [K/128, ceil4(N)]; c: bf16 bits [M, N] or None. Returns FP64 [len(rows), N].
+    """
+    assert K % GROUP_K == 0
+    rows = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    sa = unpack_sf(sfa, M, K // GROUP_K)[rows]
+    sb = unpack_sf(sfb, N, K // FP4_BLOCK_K)
+    D = _scaled_gemm_fp4(np.asarray(a)[rows], sa, unpack_e2m1(b, K), sb, K)
+    if c is not None:
+        D = decode_bf16(np.asarray(c)[rows]) + D
+    return D
+
+
+def m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa, b, sfb, m_indices, M_total: int, N: int, K: int, G: int,
+                                         rows: Optional[Sequence[int]] = None):
+    """Contiguous M-grouped FP8 x FP4 GEMM (README "Grouped GEMMs (contiguous layout)" with the
+    FP4 weights read as in fp8_fp4_gemm_nt): row r uses expert m_indices[r]'s B [N, K/2] and
+    scales [K/128, ceil4(N)]; padding rows (-1) produce nothing.
+    Returns (D [R, N] float64 with NaN on padding rows, valid [R] bool)."""
+    rows = np.arange(M_total) if rows is None else np.asarray(rows, dtype=np.int64)
+    idx = np.asarray(m_indices)[rows]
+    D = np.full((len(rows), N), np.nan)
+    sa = unpack_sf(sfa, M_total, K // GROUP_K)
+    for g in range(G):
+        sel = np.nonzero(idx == g)[0]
+        if len(sel) == 0:
+            continue
+        r = rows[sel]
+        D[sel] = _scaled_gemm_fp4(np.asarray(a)[r], sa[r], unpack_e2m1(b[g], K),
+                                  unpack_sf(sfb[g], N, K // FP4_BLOCK_K), K)
+    return D, idx >= 0
+
+
+def m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, masked_m, G: int, max_m: int, N: int, K: int,
+                                     groups: Optional[Sequence[int]] = None):
+    """Masked M-grouped FP8 x FP4 GEMM (README "Grouped GEMMs (masked layout)" with the FP4
+    weights read as in fp8_fp4_gemm_nt): group g computes rows r < masked_m[g] (clamped to
+    [0, max_m]) of A[g] against B[g].
+    Returns (D [len(groups), max_m, N] with NaN on masked rows, valid [len(groups), max_m])."""
+    groups = list(range(G)) if groups is None else list(groups)
+    D = np.full((len(groups), max_m, N), np.nan)
+    valid = np.zeros((len(groups), max_m), bool)
+    for i, g in enumerate(groups):
+        m = int(min(max(int(masked_m[g]), 0), max_m))
+        valid[i, :m] = True
+        if m:
+            sa = unpack_sf(sfa[g], max_m, K // GROUP_K)[:m]
+            D[i, :m] = _scaled_gemm_fp4(np.asarray(a[g])[:m], sa, unpack_e2m1(b[g], K),
+                                        unpack_sf(sfb[g], N, K // FP4_BLOCK_K), K)
     return D, valid
 
 

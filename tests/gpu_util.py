@@ -38,7 +38,8 @@ def run_dense(lib, p: W.Dense, c_alias: bool = False) -> torch.Tensor:
         d = c
     else:
         d = sentinel_like((p.M, p.N))
-    lib.dg_fp8_gemm_nt(a, sfa, b, sfb, c, d)
+    fn = lib.dg_fp8_fp4_gemm_nt if p.b_format == "e2m1" else lib.dg_fp8_gemm_nt
+    fn(a, sfa, b, sfb, c, d)
     torch.cuda.synchronize()
     return d
 
@@ -70,14 +71,16 @@ def run_k_grouped(lib, p: W.KGrouped, in_place: bool = False) -> torch.Tensor:
 
 def run_contiguous(lib, p: W.Contiguous) -> torch.Tensor:
     d = sentinel_like((p.M_total, p.N))
-    lib.dg_m_grouped_fp8_gemm_nt_contiguous(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d, dev(p.m_indices))
+    fn = lib.dg_m_grouped_fp8_fp4_gemm_nt_contiguous if p.b_format == "e2m1" else lib.dg_m_grouped_fp8_gemm_nt_contiguous
+    fn(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d, dev(p.m_indices))
     torch.cuda.synchronize()
     return d
 
 
 def run_masked(lib, p: W.Masked) -> torch.Tensor:
     d = sentinel_like((p.G, p.max_m, p.N))
-    lib.dg_m_grouped_fp8_gemm_nt_masked(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d, dev(p.masked_m))
+    fn = lib.dg_m_grouped_fp8_fp4_gemm_nt_masked if p.b_format == "e2m1" else lib.dg_m_grouped_fp8_gemm_nt_masked
+    fn(dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), d, dev(p.masked_m))
     torch.cuda.synchronize()
     return d
 

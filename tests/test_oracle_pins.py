@@ -366,10 +366,141 @@ def pin_grouped_layouts(O_):
     np.testing.assert_allclose(D2[1], brute_force(a2[:, 128:], ea2[:, 1:], b2[:, 128:], eb2[:, 1:]), rtol=1e-14)
 
 
+# --------------------------------------------------------------------------------------
+# FP8 x FP4 pins
+# --------------------------------------------------------------------------------------
+
+# E2M1 magnitudes of codes 0..7 as tabulated in the OCP Microscaling Formats (MX) v1.0
+# specification (FP4 E2M1: 0, 0.5 subnormal, then 1, 1.5, 2, 3, 4, 6); codes 8..15 negate.
+E2M1_OCP = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4),
+            Fraction(6)]
+
+
+def e2m1_value(code: int) -> Fraction:
+    return -E2M1_OCP[code & 7] if code & 8 else E2M1_OCP[code & 7]
+
+
+def fp4_code(packed: np.ndarray, n: int, k: int) -> int:
+    """Element k of row n of a packed FP4 matrix: the low nibble holds the even element."""
+    return (int(packed[n, k // 2]) >> (4 * (k % 2))) & 0xF
+
+
+def brute_force_fp4(a, ea, b_packed, eb, c_bits=None):
+    """Exact rational D = C + sum_k sA[m, k//128] * sB[n, k//32] * A[m, k] * B[n, k]."""
+    M, K = a.shape
+    N = b_packed.shape[0]
+    A = [[Fraction(float(v)) for v in row] for row in torch_e4m3(a)]
+    two = Fraction(2)
+    D = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += (A[m][k] * e2m1_value(fp4_code(b_packed, n, k)) * two ** (int(ea[m, k // 128]) - 127)
+                        * two ** (int(eb[n, k // 32]) - 127))
+            if c_bits is not None:
+                cv = torch.tensor([int(c_bits[m, n])], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+                acc += Fraction(float(cv.to(torch.float64).item()))
+            D[m, n] = float(acc)
+    return D
+
+
+def pin_e2m1_table(O_):
+    got = O_.decode_e2m1(np.arange(16))
+    expect = np.array([float(e2m1_value(c)) for c in range(16)])
+    assert np.array_equal(got, expect)
+    assert np.signbit(got[8]) and not np.signbit(got[0])
+
+
+def pin_fp4_brute_force(O_):
+    rng = np.random.default_rng(31)
+    M, N, K = 3, 5, 256
+    a = random_codes(rng, (M, K))
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    ea = rng.integers(120, 135, size=(M, K // 128)).astype(np.uint8)
+    eb = rng.integers(120, 135, size=(N, K // 32)).astype(np.uint8)
+    c = W.to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    got = O_.fp8_fp4_gemm_nt(a, words_from_codes(ea), b, words_from_codes(eb), c, M, N, K)
+    np.testing.assert_allclose(got, brute_force_fp4(a, ea, b, eb, c), rtol=1e-14, atol=0)
+
+
+def pin_fp4_one_hot(O_):
+    # B row n holds a single 1.0 (code 2) at column k0[n]: D[m, n] = sA * sB * A[m, k0[n]]
+    rng = np.random.default_rng(32)
+    M, N, K = 4, 8, 512
+    k0 = np.array([0, 1, 33, 94, 127, 128, 301, 511])
+    b = np.zeros((N, K // 2), np.uint8)
+    for n, k in enumerate(k0):
+        b[n, k // 2] = 2 << (4 * (k % 2))
+    a = random_codes(rng, (M, K))
+    ea = rng.integers(120, 135, size=(M, K // 128)).astype(np.uint8)
+    eb = rng.integers(120, 135, size=(N, K // 32)).astype(np.uint8)
+    got = O_.fp8_fp4_gemm_nt(a, words_from_codes(ea), b, words_from_codes(eb), None, M, N, K)
+    A = torch_e4m3(a)
+    for m in range(M):
+        for n, k in enumerate(k0):
+            want = A[m, k] * 2.0 ** (int(ea[m, k // 128]) - 127) * 2.0 ** (int(eb[n, k // 32]) - 127)
+            assert got[m, n] == want, (m, n, got[m, n], want)
+
+
+def pin_fp4_matches_fp8_route(O_):
+    # Every E2M1 value is an E4M3 value: with B's scales constant over each 128 x 128 block the
+    # FP8 x FP4 GEMM is the FP8 GEMM of the same numbers (B re-encoded by value lookup in
+    # torch's E4M3 decoding).
+    rng = np.random.default_rng(33)
+    M, N, K = 6, 136, 384
+    a = random_codes(rng, (M, K))
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    e4m3_of = {}
+    for code in range(256):
+        v = torch_e4m3(np.array([code], np.uint8))[0]
+        if not np.isnan(v):
+            e4m3_of.setdefault(float(v), code)
+    e4m3_of[0.0] = 0
+    b8 = np.array([[e4m3_of[float(e2m1_value(fp4_code(b, n, k)))] for k in range(K)] for n in range(N)], np.uint8)
+    ea = rng.integers(122, 133, size=(M, K // 128)).astype(np.uint8)
+    eb_blocks = rng.integers(122, 133, size=(2, K // 128)).astype(np.uint8)
+    eb_rows = np.repeat(np.repeat(eb_blocks, 128, axis=0)[:N], 4, axis=1)     # [N, K/32]
+    c = W.to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    got = O_.fp8_fp4_gemm_nt(a, words_from_codes(ea), b, words_from_codes(eb_rows), c, M, N, K)
+    want = O_.fp8_gemm_nt(a, words_from_codes(ea), b8, words_from_codes(eb_blocks), c, M, N, K)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def pin_fp4_grouped_equals_dense(O_):
+    rng = np.random.default_rng(34)
+    G, N, K = 3, 40, 256
+    b = rng.integers(0, 256, size=(G, N, K // 2), dtype=np.uint8)
+    eb = rng.integers(122, 133, size=(G, N, K // 32)).astype(np.uint8)
+    sfb = np.stack([words_from_codes(eb[g]) for g in range(G)])
+    m_idx = np.array([2] * 3 + [-1] * 125 + [0] * 2 + [-1] * 126, np.int32)
+    R = len(m_idx)
+    a = random_codes(rng, (R, K))
+    ea = rng.integers(122, 133, size=(R, K // 128)).astype(np.uint8)
+    D, valid = O_.m_grouped_fp8_fp4_gemm_nt_contiguous(a, words_from_codes(ea), b, sfb, m_idx, R, N, K, G)
+    assert np.array_equal(valid, m_idx >= 0)
+    assert np.isnan(D[~valid]).all()
+    for r in np.nonzero(m_idx >= 0)[0]:
+        g = m_idx[r]
+        want = brute_force_fp4(a[r:r + 1], ea[r:r + 1], b[g], eb[g])
+        np.testing.assert_allclose(D[r:r + 1], want, rtol=1e-14)
+    max_m = 5
+    am = random_codes(rng, (G, max_m, K))
+    eam = rng.integers(122, 133, size=(G, max_m, K // 128)).astype(np.uint8)
+    sfam = np.stack([words_from_codes(eam[g]) for g in range(G)])
+    masked = np.array([2, 0, 7], np.int32)          # the last is clamped to max_m
+    Dm, vm = O_.m_grouped_fp8_fp4_gemm_nt_masked(am, sfam, b, sfb, masked, G, max_m, N, K)
+    assert vm.sum() == 2 + 0 + max_m
+    np.testing.assert_allclose(Dm[0, :2], brute_force_fp4(am[0, :2], eam[0, :2], b[0], eb[0]), rtol=1e-14)
+    np.testing.assert_allclose(Dm[2], brute_force_fp4(am[2], eam[2], b[2], eb[2]), rtol=1e-14)
+    assert np.isnan(Dm[1]).all() and np.isnan(Dm[0, 2:]).all()
+
+
 PINS = [pin_e4m3_table, pin_ue8m0_table, pin_bf16, pin_unpack, pin_brute_force, pin_identity,
         pin_one_hot, pin_pow2_invariance, pin_c_only, pin_dequantised_route,
         pin_contiguous_equals_dense, pin_masked_equals_dense, pin_wgrad_brute_force, pin_wgrad_c_only,
-        pin_k_grouped_equals_per_expert, pin_layouts, pin_grouped_layouts]
+        pin_k_grouped_equals_per_expert, pin_layouts, pin_grouped_layouts, pin_e2m1_table, pin_fp4_brute_force,
+        pin_fp4_one_hot, pin_fp4_matches_fp8_route, pin_fp4_grouped_equals_dense]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -526,6 +657,52 @@ def _tn_forgets_to_transpose_a(old):
     return f
 
 
+def _mut_e2m1(table_fn):
+    @contextlib.contextmanager
+    def ctx():
+        old = O._E2M1.copy()
+        O._E2M1[:] = table_fn(old)
+        try:
+            yield
+        finally:
+            O._E2M1[:] = old
+    return ctx
+
+
+def _e2m1_subnormal_as_normal(t):
+    t = t.copy()
+    t[1], t[9] = 1.0, -1.0      # code 1 read with an implicit leading one
+    return t
+
+
+def _fp4_high_nibble_first(old):
+    def f(packed, K):
+        p = np.asarray(packed, dtype=np.uint8)
+        out = np.empty(p.shape[:-1] + (K,), np.uint8)
+        out[..., 0::2] = p >> 4
+        out[..., 1::2] = p & 0xF
+        return out
+    return f
+
+
+def _make_scaled_fp4(mode):
+    def factory(old):
+        def f(a_codes, sa_codes, b_codes, sb_codes, K):
+            A = O.decode_e4m3(a_codes)
+            B = O.decode_e2m1(b_codes)
+            sA = O.decode_ue8m0(sa_codes)
+            sB = O.decode_ue8m0(sb_codes)
+            D = np.zeros((A.shape[0], B.shape[0]))
+            for j in range(K // 32):
+                ks = slice(32 * j, 32 * j + 32)
+                jb = 4 * (j // 4) if mode == "b_scale_per_128" else j
+                ja = min(j, sA.shape[1] - 1) if mode == "a_scale_per_32" else j // 4
+                D += sA[:, ja, None] * (A[:, ks] @ B[:, ks].T) * sB[None, :, jb]
+            return D
+        return f
+    return factory
+
+
 MUTANTS = {
     "subnormal_implicit_one": _mut_table(_subnormal_with_implicit_one),
     "sign_ignored": _mut_table(lambda t: np.abs(t)),
@@ -542,6 +719,11 @@ MUTANTS = {
     "wgrad_c_dropped": _mut_attr("wgrad_gemm_fp8_fp8_fp32_nt", _wgrad_c_dropped),
     "k_grouped_scales_packed_globally": _mut_attr("k_grouped_wgrad_gemm_fp8_fp8_fp32_nt", _k_grouped_global_packing),
     "tn_reads_a_as_k_major": _mut_attr("fp8_gemm_tn", _tn_forgets_to_transpose_a),
+    "fp4_subnormal_as_normal": _mut_e2m1(_e2m1_subnormal_as_normal),
+    "fp4_sign_ignored": _mut_e2m1(lambda t: np.abs(t)),
+    "fp4_high_nibble_first": _mut_attr("unpack_e2m1", _fp4_high_nibble_first),
+    "fp4_b_scale_per_128": _mut_attr("_scaled_gemm_fp4", _make_scaled_fp4("b_scale_per_128")),
+    "fp4_a_scale_per_32": _mut_attr("_scaled_gemm_fp4", _make_scaled_fp4("a_scale_per_32")),
 }
 
 

@@ -116,3 +116,44 @@ def test_layout_workload(lib):
     ref = O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, None, p.M, p.N, p.K, rows=rows)
     assert_parity(bf16_f64(d)[rows], ref, name)
     assert lib.dg_get_device_status() == 0
+
+
+def test_fp4_dense_workload(lib):
+    name = "fp4_dense_decode_128x7168x16384_c"
+    p = W.make_workload(name)
+    d = run_dense(lib, p)
+    ref = O.fp8_fp4_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K)
+    assert_parity(bf16_f64(d), ref, name)
+    assert lib.dg_get_device_status() == 0
+
+
+def test_fp4_masked_workload(lib):
+    name = "fp4_masked_g32_m256_n7168_k2048"
+    p = W.make_workload(name)
+    d = run_masked(lib, p)
+    bits = bf16_bits(d)
+    valid = np.arange(p.max_m)[None, :] < p.masked_m[:, None]
+    assert (bits[~valid] == SENTINEL).all()
+    groups = sorted(set([0, p.G - 1] + np.random.default_rng(4).choice(p.G, 6, replace=False).tolist()))
+    ref, v = O.m_grouped_fp8_fp4_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, p.masked_m, p.G, p.max_m, p.N, p.K,
+                                                groups=groups)
+    assert_parity(bf16_f64(d)[groups][v], ref[v], name)
+    assert lib.dg_get_device_status() == 0
+
+
+def test_fp4_contiguous_workload(lib):
+    name = "fp4_contiguous_g8_t32768_n4096_k7168"
+    p = W.make_workload(name)
+    d = run_contiguous(lib, p)
+    bits = bf16_bits(d)
+    pad = p.m_indices < 0
+    assert (bits[pad] == SENTINEL).all()
+    starts = [int(np.nonzero(p.m_indices == g)[0][0]) for g in range(p.G) if (p.m_indices == g).any()]
+    ends = [int(np.nonzero(p.m_indices == g)[0][-1]) for g in range(p.G) if (p.m_indices == g).any()]
+    rows = np.unique(np.concatenate([_rows(p.M_total, 64, 5), starts, ends]))
+    rows = rows[p.m_indices[rows] >= 0]
+    ref, valid = O.m_grouped_fp8_fp4_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K,
+                                                        p.G, rows=rows)
+    assert valid.all()
+    assert_parity(bf16_f64(d)[rows], ref, name)
+    assert lib.dg_get_device_status() == 0

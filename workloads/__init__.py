@@ -52,14 +52,14 @@ def _to_e4m3_bytes(x: np.ndarray) -> np.ndarray:
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
 
 
-def _scale_exponents(amax: np.ndarray) -> np.ndarray:
-    """Smallest UE8M0 code e (1..254) with amax / 2**(e-127) <= 448; amax == 0 -> 127."""
+def _scale_exponents(amax: np.ndarray, vmax: float = E4M3_MAX) -> np.ndarray:
+    """Smallest UE8M0 code e (1..254) with amax / 2**(e-127) <= vmax; amax == 0 -> 127."""
     amax = np.asarray(amax, dtype=np.float64)
     with np.errstate(divide="ignore"):
-        s = np.ceil(np.log2(np.where(amax > 0, amax, 1.0) / E4M3_MAX))
+        s = np.ceil(np.log2(np.where(amax > 0, amax, 1.0) / vmax))
     # fix any off-by-one from log2 rounding so that s is the least valid exponent
-    s = np.where(np.ldexp(amax, -s.astype(np.int64)) > E4M3_MAX, s + 1, s)
-    s = np.where(np.ldexp(amax, -(s - 1).astype(np.int64)) <= E4M3_MAX, s - 1, s)
+    s = np.where(np.ldexp(amax, -s.astype(np.int64)) > vmax, s + 1, s)
+    s = np.where(np.ldexp(amax, -(s - 1).astype(np.int64)) <= vmax, s - 1, s)
     e = np.clip(s + 127, 1, 254)
     e = np.where(amax > 0, e, 127)
     return e.astype(np.uint8)
@@ -88,6 +88,40 @@ def quantize_blocks(x: np.ndarray):
     xg = x.reshape(N, K // GROUP_K, GROUP_K).astype(np.float64)
     scaled = np.ldexp(xg, -(rows_e.astype(np.int64) - 127)[:, :, None])
     return _to_e4m3_bytes(scaled.reshape(N, K).astype(np.float32)), e
+
+
+E2M1_MAX = 6.0
+FP4_BLOCK_K = 32       # K extent of one FP4 scale (the MX block)
+_E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _to_e2m1_codes(x: np.ndarray) -> np.ndarray:
+    """Round values (already inside +-6) to the nearest E2M1 magnitude, ties to the even
+    code; the sign goes to bit 3 (zero magnitudes stay +0)."""
+    x = np.asarray(x)
+    mag = np.abs(x.astype(np.float64))
+    mid = (_E2M1_MAGNITUDES[:-1] + _E2M1_MAGNITUDES[1:]) / 2          # 0.25, 0.75, ..., 5
+    idx = np.searchsorted(mid, mag, side="left")                          # a tie lands on the lower code
+    tie = (idx < len(mid)) & (mag == mid[np.minimum(idx, len(mid) - 1)]) & (idx % 2 == 1)
+    idx = (idx + tie).astype(np.uint8)                                    # odd lower code: take the even one
+    return np.where((x < 0) & (idx > 0), idx | 8, idx).astype(np.uint8)
+
+
+def pack_fp4(codes: np.ndarray) -> np.ndarray:
+    """E2M1 codes [..., K] -> bytes [..., K/2], element 2j in the low nibble of byte j."""
+    c = np.asarray(codes, np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def quantize_fp4_rows(x: np.ndarray):
+    """Per-row, per-32-K-block FP4 quantisation (the MX recipe): x fp32 [N, K] ->
+    (packed E2M1 bytes [N, K/2], exps [N, K/32])."""
+    N, K = x.shape
+    assert K % GROUP_K == 0
+    xb = x.reshape(N, K // FP4_BLOCK_K, FP4_BLOCK_K)
+    e = _scale_exponents(np.abs(xb).max(axis=2), E2M1_MAX)
+    scaled = np.ldexp(xb.astype(np.float64), -(e.astype(np.int64) - 127)[:, :, None])
+    return pack_fp4(_to_e2m1_codes(scaled.reshape(N, K))), e
 
 
 def pack_sf(exps: np.ndarray) -> np.ndarray:
@@ -122,6 +156,7 @@ class Dense:
     N: int
     K: int
     layout: str = "nt"         # how a and b are stored on the device (the arrays here are always NT)
+    b_format: str = "e4m3"     # "e2m1": b is packed FP4 [N, K/2], sfb per row per 32 K [K/128, ceil4(N)]
 
     @property
     def flops(self) -> float:
@@ -181,6 +216,7 @@ class Contiguous:
     N: int
     K: int
     G: int
+    b_format: str = "e4m3"     # "e2m1": b is packed FP4 [G, N, K/2], sfb [G, K/128, ceil4(N)]
 
     @property
     def valid_rows(self) -> int:
@@ -202,6 +238,7 @@ class Masked:
     max_m: int
     N: int
     K: int
+    b_format: str = "e4m3"     # "e2m1": b is packed FP4 [G, N, K/2], sfb [G, K/128, ceil4(N)]
 
     @property
     def flops(self) -> float:
@@ -231,6 +268,15 @@ def make_dense(M: int, N: int, K: int, seed: int, with_c: bool = False,
     b, eb = quantize_blocks(_normal(rng, (N, K), row_magnitude))
     c = to_bf16_bits(rng.standard_normal((M, N), dtype=np.float32)) if with_c else None
     return Dense(a, pack_sf(ea), b, pack_sf(eb), c, M, N, K)
+
+
+def make_dense_fp4(M: int, N: int, K: int, seed: int, with_c: bool = False) -> Dense:
+    """A quantised like make_dense; B [N, K] quantised to FP4 with one scale per row per 32 K."""
+    rng = _rng(seed)
+    a, ea = quantize_rows(_normal(rng, (M, K)))
+    b, eb = quantize_fp4_rows(_normal(rng, (N, K)))
+    c = to_bf16_bits(rng.standard_normal((M, N), dtype=np.float32)) if with_c else None
+    return Dense(a, pack_sf(ea), b, pack_sf(eb), c, M, N, K, b_format="e2m1")
 
 
 def make_wgrad(M: int, N: int, K: int, seed: int, with_c: bool = True) -> Wgrad:
@@ -275,17 +321,20 @@ def make_k_grouped(G: int, M: int, N: int, tokens: int, seed: int, with_c: bool 
                     pack_sf_k_grouped(eb, ks), c, ks, M, N)
 
 
-def _make_b_grouped(rng, G, N, K):
+def _make_b_grouped(rng, G, N, K, b_format="e4m3"):
     bs, sfbs = [], []
     for _ in range(G):
-        b, eb = quantize_blocks(_normal(rng, (N, K)))
+        if b_format == "e2m1":
+            b, eb = quantize_fp4_rows(_normal(rng, (N, K)))
+        else:
+            b, eb = quantize_blocks(_normal(rng, (N, K)))
         bs.append(b)
         sfbs.append(pack_sf(eb))
     return np.stack(bs), np.stack(sfbs)
 
 
 def make_contiguous(G: int, tokens: int, N: int, K: int, seed: int,
-                    counts: Optional[np.ndarray] = None) -> Contiguous:
+                    counts: Optional[np.ndarray] = None, b_format: str = "e4m3") -> Contiguous:
     """Token rows split among G experts by a uniform multinomial (or given counts); each
     expert segment padded to a multiple of 128 rows with m_indices = -1 on the padding."""
     rng = _rng(seed)
@@ -301,12 +350,12 @@ def make_contiguous(G: int, tokens: int, N: int, K: int, seed: int,
         off += s
     a, ea = quantize_rows(_normal(rng, (max(M_total, 1), K)))
     a, ea = a[:M_total], ea[:M_total]
-    b, sfb = _make_b_grouped(rng, G, N, K)
-    return Contiguous(a, pack_sf(ea), b, sfb, m_indices, M_total, N, K, G)
+    b, sfb = _make_b_grouped(rng, G, N, K, b_format)
+    return Contiguous(a, pack_sf(ea), b, sfb, m_indices, M_total, N, K, G, b_format)
 
 
 def make_masked(G: int, max_m: int, N: int, K: int, seed: int,
-                masked_m: Optional[np.ndarray] = None) -> Masked:
+                masked_m: Optional[np.ndarray] = None, b_format: str = "e4m3") -> Masked:
     """A [G, max_m, K]; masked_m ~ U{0..max_m} per expert (or given); rows past masked_m
     hold ordinary random data that the GEMM must ignore."""
     rng = _rng(seed)
@@ -318,8 +367,8 @@ def make_masked(G: int, max_m: int, N: int, K: int, seed: int,
         a, ea = quantize_rows(_normal(rng, (max_m, K)))
         a_list.append(a)
         sfa_list.append(pack_sf(ea))
-    b, sfb = _make_b_grouped(rng, G, N, K)
-    return Masked(np.stack(a_list), np.stack(sfa_list), b, sfb, masked_m, G, max_m, N, K)
+    b, sfb = _make_b_grouped(rng, G, N, K, b_format)
+    return Masked(np.stack(a_list), np.stack(sfa_list), b, sfb, masked_m, G, max_m, N, K, b_format)
 
 
 # --------------------------------------------------------------------------------------
@@ -341,6 +390,11 @@ WORKLOADS = {
     "dense_nn_4096x7168x2048": dict(kind="dense_layout", layout="nn", M=4096, N=7168, K=2048, with_c=False),
     # MoE weight gradient: 4 experts, 4096 x 7168 each, 16384 tokens split among them
     "k_grouped_wgrad_g4_m4096_n7168_t16384": dict(kind="k_grouped", G=4, M=4096, N=7168, tokens=16384),
+    # FP8 x FP4 (weights in FP4 with per-32 UE8M0 scales): the decode and MoE shapes above
+    "fp4_dense_decode_128x7168x16384_c": dict(kind="dense_fp4", M=128, N=7168, K=16384, with_c=True),
+    "fp4_masked_g32_m256_n7168_k2048": dict(kind="masked", G=32, max_m=256, N=7168, K=2048, b_format="e2m1"),
+    "fp4_contiguous_g8_t32768_n4096_k7168": dict(kind="contiguous", G=8, tokens=32768, N=4096, K=7168,
+                                                 b_format="e2m1"),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -351,6 +405,8 @@ def make_workload(name: str):
     kind = spec.pop("kind")
     if kind == "dense":
         return make_dense(seed=seed, **spec)
+    if kind == "dense_fp4":
+        return make_dense_fp4(seed=seed, **spec)
     if kind == "contiguous":
         return make_contiguous(seed=seed, **spec)
     if kind == "wgrad":
