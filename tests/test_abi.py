@@ -108,3 +108,24 @@ def test_weight_gradient_forms_reject_bad_arguments(lib):
     assert lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, None, x, None, 2, 128, 128, 128, 1, None) == INVALID
     assert lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(x, x, x, x, None, x, P(0x10002), 2, 128, 128, 128, 1,
                                                        None) == MISALIGNED
+
+
+def test_fp8_fp4_forms_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    x = P(0x10000)
+    INVALID, MISALIGNED = 1, 3
+    assert lib.dg_fp8_fp4_gemm_nt(None, x, x, x, None, x, 128, 128, 128, None) == INVALID
+    assert lib.dg_fp8_fp4_gemm_nt(x, x, x, x, None, x, 128, 128, 64, None) == INVALID      # K % 128
+    assert lib.dg_fp8_fp4_gemm_nt(x, x, x, x, None, x, 128, 120, 128, None) == INVALID     # N % 16
+    # the packed FP4 operand must be 32-byte aligned; 16 is not enough
+    assert lib.dg_fp8_fp4_gemm_nt(x, x, P(0x10010), x, None, x, 128, 128, 128, None) == MISALIGNED
+    assert lib.dg_fp8_fp4_gemm_nt(x, x, x, x, P(0x10008), x, 128, 128, 128, None) == MISALIGNED
+    assert lib.dg_m_grouped_fp8_fp4_gemm_nt_contiguous(x, x, x, x, x, x, 128, 128, 128, 0, None) == INVALID
+    assert lib.dg_m_grouped_fp8_fp4_gemm_nt_contiguous(x, x, x, x, x, None, 128, 128, 128, 2, None) == INVALID
+    assert lib.dg_m_grouped_fp8_fp4_gemm_nt_contiguous(x, x, P(0x10010), x, x, x, 128, 128, 128, 2,
+                                                       None) == MISALIGNED
+    assert lib.dg_m_grouped_fp8_fp4_gemm_nt_masked(x, x, x, x, x, x, 0, 128, 128, 128, None) == INVALID
+    assert lib.dg_m_grouped_fp8_fp4_gemm_nt_masked(x, x, x, x, x, P(0x10002), 2, 128, 128, 128, None) == MISALIGNED
+    # empty problems launch nothing and accept null pointers
+    assert lib.dg_fp8_fp4_gemm_nt(None, None, None, None, None, None, 0, 128, 128, None) == 0
+    assert lib.dg_m_grouped_fp8_fp4_gemm_nt_masked(None, None, None, None, None, None, 2, 0, 128, 128, None) == 0
