@@ -727,15 +727,22 @@ MUTANTS = {
 }
 
 
+# pins that build exact rationals over grouped problems take ~1-2 s each: tried last
+_SLOW_PINS = {"pin_k_grouped_equals_per_expert", "pin_grouped_layouts", "pin_masked_equals_dense",
+              "pin_contiguous_equals_dense", "pin_brute_force", "pin_fp4_grouped_equals_dense",
+              "pin_wgrad_brute_force", "pin_layouts"}
+
+
 @pytest.mark.parametrize("name", list(MUTANTS))
 def test_planted_mistake_is_caught(name):
-    caught = []
+    caught = None
     with MUTANTS[name]():
-        for pin in PINS:
+        for pin in sorted(PINS, key=lambda f: f.__name__ in _SLOW_PINS):
             try:
                 pin(O)
             except (AssertionError, ValueError, IndexError):
-                caught.append(pin.__name__)
+                caught = pin.__name__
+                break
     assert caught, f"planted mistake {name} passed every pin"
 
 
