@@ -170,6 +170,29 @@ class DeviceProblem:
             fn(c["a"], c["sfa"], c["b"], c["sfb"], c["d"], c["mm"])
 
 
+def copy_bandwidth(torch, nbytes=1 << 30, reps=10):
+    """Harness check: a device-to-device copy of a known size (larger than L2), timed with the
+    same CUDA events on the launching stream; returns GB/s counting the read and the write."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda").fill_(1)
+    dst = torch.empty_like(src)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            dst.copy_(src)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            dst.copy_(src)
+        end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    del src, dst
+    torch.cuda.empty_cache()
+    return 2.0 * nbytes * reps / (ms * 1e-3) / 1e9
+
+
 def time_steps(torch, prob, steps, warmup, barrier=None):
     """Warm up, then time exactly `steps` launches back to back.
 
@@ -328,8 +351,8 @@ print(json.dumps(dict(seconds=el, flops=flops, rows=done_rows, calls=calls, rows
 """
 
 
-def cpu_baseline(name, budget_s=10.0, rows_per_call=16):
-    cores = os.cpu_count() or 1
+def cpu_baseline(name, budget_s=10.0, rows_per_call=16, cores=None):
+    cores = cores or os.cpu_count() or 1
     env = dict(os.environ, OPENBLAS_NUM_THREADS=str(cores), OMP_NUM_THREADS=str(cores), CUDA_VISIBLE_DEVICES="")
     try:
         out = subprocess.run([sys.executable, "-c", CPU_CHILD, ROOT, name, str(budget_s), str(rows_per_call)],
@@ -400,6 +423,7 @@ def main():
     # measured FP8 tensor ceiling (MMA-only kernel on every SM), reported beside the peak;
     # skipped with --headline-only so that profiles of that command show only the timed path
     mma_ceiling = None if args.headline_only else L.dg_measure_fp8_mma_tflops(4096)[0]
+    copy_gbs = None if args.headline_only else copy_bandwidth(torch)
     ms_per_step = t_max / args.steps
     value = job_tflops(world, flops, args.steps, t_max)
     kern_ms = region_ms / args.steps
@@ -444,6 +468,10 @@ def main():
         return
 
     cpu = cpu_baseline(HEADLINE, args.cpu_budget)
+    if not args.headline_only:
+        one = cpu_baseline(HEADLINE, args.cpu_budget / 2, rows_per_call=4, cores=1)
+        cpu["value_1thread"] = one["value"]
+        cpu["sample_1thread"] = one["sample"]
     line = {
         "metric": METRIC,
         "value": value,
@@ -467,6 +495,9 @@ def main():
         "fp8_mma_ceiling_tflops": mma_ceiling,
         "fp8_mma_ceiling_how": "dg_measure_fp8_mma_tflops: block-scaled 128x256x32 tcgen05.mma back to back from "
                                "shared memory, one CTA per SM, CUDA events (no data movement)",
+        "harness_check": {"copy_gbs": copy_gbs, "hbm_peak_gbs": peaks["hbm_gbs"],
+                          "how": "1 GiB device-to-device copy (torch), 10 reps, CUDA events on the launching "
+                                 "stream, read + write bytes: the timing method against a known-size transfer"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": HEADLINE_TRAFFIC["bytes_per_launch"],
                      "traffic_source": HEADLINE_TRAFFIC["source"],

@@ -407,12 +407,12 @@ constexpr int kEpilogueWarps = 4;
 // with one accumulator, BN = 240 or 192 with two.
 constexpr int kPairStages = 5;
 
-template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false>
+template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false, bool kBF4 = false>
 struct PairLauncher {
   static constexpr int kNumAccum = kBN == 256 ? 1 : 2;
-  using Cfg = dg::PairConfig<kPairStages, kBN, kNumAccum>;
+  using Cfg = dg::PairConfig<kPairStages, kBN, kNumAccum, kBF4>;
   static constexpr auto kernel() {
-    return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kBN, kNumAccum, kHasC, kOutF32>;
+    return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kBN, kNumAccum, kHasC, kOutF32, kBF4>;
   }
 
   // Largest number of co-resident CTA pairs (0 if the device cannot run the kernel).
@@ -465,9 +465,9 @@ struct PairLauncher {
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, td_tail, p);
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
-      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d pair 256x%d accum=%d stages=%d clusters=%d smem=%d\n",
+      std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d pair 256x%d accum=%d stages=%d clusters=%d smem=%d fp4=%d\n",
                    static_cast<int>(kKind), p.M, p.N, p.K, p.G, kBN, kNumAccum, kPairStages, clusters,
-                   Cfg::SMEM_BYTES);
+                   Cfg::SMEM_BYTES, kBF4 ? 1 : 0);
     return DG_OK;
   }
 };
@@ -600,7 +600,7 @@ bool map_sf_fp4(CUtensorMap* m, const int32_t* base, int G, int N, int KG, int b
 
 // Dense / contiguous GEMM on CTA pairs: converts the scale words into tcgen05.cp chunks in
 // the stream workspace (two small kernels), then launches the pair kernel.
-template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false>
+template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false, bool kBF4 = false>
 dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d,
                    dg::Params p, int clusters, cudaStream_t stream) {
   const int KP = ceil_div(p.K / 128, 4);
@@ -608,9 +608,10 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   const int NB = ceil_div(p.N, 128);
   const int sfb_rows = 2 * ceil_div(p.N, kBN);     // two chunks per tile
   const int G = kKind == dg::Kind::Dense ? 1 : p.G;
+  const int b_kp = kBF4 ? p.K / 128 : KP;           // B chunk rows per K-group (FP4) or per K-quad
   const size_t sfa_words = static_cast<size_t>(KP) * num_mb * 128;
-  const size_t sfb_words = static_cast<size_t>(G) * KP * sfb_rows * 128;
-  if (static_cast<size_t>(KP) * num_mb > (1u << 30) || static_cast<size_t>(G) * KP * sfb_rows > (1u << 30))
+  const size_t sfb_words = static_cast<size_t>(G) * b_kp * sfb_rows * 128;
+  if (static_cast<size_t>(KP) * num_mb > (1u << 30) || static_cast<size_t>(G) * b_kp * sfb_rows > (1u << 30))
     return DG_ERR_UNSUPPORTED;
   // contiguous form: the pair-row list (3 ints per pair row, at most one per block) and its length
   const size_t list_words = kKind == dg::Kind::Contiguous ? 4 + 4 * static_cast<size_t>(ceil_div(3 * num_mb, 4)) : 0;
@@ -632,10 +633,12 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
     pa.sfb_out = sfb_t;
     pa.groups = G;
     pa.b_rows = p.N;
-    pa.ldb = ceil4(NB);
+    pa.ldb = kBF4 ? ceil4(p.N) : ceil4(NB);
     pa.b_chunks = sfb_rows;
     pa.tile_bn = kBN;
     pa.kp = KP;
+    pa.b_kp = b_kp;
+    pa.b_per_row = kBF4 ? 1 : 0;
     if constexpr (kKind == dg::Kind::Contiguous) {
       pa.m_indices = p.m_indices;
       pa.num_mb = num_mb;
@@ -678,13 +681,15 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
     td_tail = td;
   }
   // each CTA of the pair loads BN/2 rows of the B tile
-  if (kKind == dg::Kind::Dense)
+  if (kBF4)
+    ok = ok && map_operand_fp4(&tb, b, kKind == dg::Kind::Dense ? 0 : G, p.N, p.K, kBN / 2);
+  else if (kKind == dg::Kind::Dense)
     ok = ok && map_operand_2d(&tb, b, p.N, p.K, kBN / 2);
   else
     ok = ok && map_operand_3d(&tb, b, G, p.N, p.K, kBN / 2);
   {
     const uint64_t dims_a[2] = {128, static_cast<uint64_t>(KP) * num_mb};
-    const uint64_t dims_b[2] = {128, static_cast<uint64_t>(G) * KP * sfb_rows};
+    const uint64_t dims_b[2] = {128, static_cast<uint64_t>(G) * b_kp * sfb_rows};
     const uint64_t strides[1] = {512};
     const uint32_t box_a[2] = {128, 1}, box_b[2] = {128, 2};
     ok = ok && make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa_t, dims_a, strides, box_a, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -693,7 +698,7 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   if (!ok) return DG_ERR_CUDA;
   p.sf_num_mb = num_mb;
   p.sf_nb = sfb_rows;
-  return PairLauncher<kKind, kHasC, kBN, kOutF32>::launch(ta, tb, tsa, tsb, td, td_tail, p, clusters, stream);
+  return PairLauncher<kKind, kHasC, kBN, kOutF32, kBF4>::launch(ta, tb, tsa, tsb, td, td_tail, p, clusters, stream);
 }
 
 // Pair tile width: DG_PAIR_BN (192, 240 or 256) overrides; 240 is offered for the dense
@@ -724,7 +729,7 @@ int pick_pair_bn(long long pair_rows, int N, int K, int clusters, bool dense) {
 }
 
 // Launches the pair kernel for kKind if the device can run it; *launched tells whether it did.
-template <dg::Kind kKind, bool kOutF32 = false>
+template <dg::Kind kKind, bool kOutF32 = false, bool kBF4 = false>
 dg_status try_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
                    const void* c, void* d, dg::Params pp, long long pair_rows, int sms, cudaStream_t stream,
                    bool* launched) {
@@ -735,12 +740,12 @@ dg_status try_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   constexpr bool kDense = kKind == dg::Kind::Dense;
   constexpr int kWideBN = kDense ? 240 : 192;     // the 240-wide configuration is dense-only
   const bool with_c = kDense && c != nullptr;
-  const int max_cl = std::min({with_c ? PairLauncher<kKind, kDense, 256, kOutF32>::max_clusters()
-                                      : PairLauncher<kKind, false, 256, kOutF32>::max_clusters(),
-                               with_c ? PairLauncher<kKind, kDense, 192, kOutF32>::max_clusters()
-                                      : PairLauncher<kKind, false, 192, kOutF32>::max_clusters(),
-                               with_c ? PairLauncher<kKind, kDense, kWideBN, kOutF32>::max_clusters()
-                                      : PairLauncher<kKind, false, kWideBN, kOutF32>::max_clusters()});
+  const int max_cl = std::min({with_c ? PairLauncher<kKind, kDense, 256, kOutF32, kBF4>::max_clusters()
+                                      : PairLauncher<kKind, false, 256, kOutF32, kBF4>::max_clusters(),
+                               with_c ? PairLauncher<kKind, kDense, 192, kOutF32, kBF4>::max_clusters()
+                                      : PairLauncher<kKind, false, 192, kOutF32, kBF4>::max_clusters(),
+                               with_c ? PairLauncher<kKind, kDense, kWideBN, kOutF32, kBF4>::max_clusters()
+                                      : PairLauncher<kKind, false, kWideBN, kOutF32, kBF4>::max_clusters()});
   if (max_cl <= 0) return DG_OK;
   const int cl_cap = std::min(max_cl, sms / 2);
   const int bn = pick_pair_bn(pair_rows, pp.N, pp.K, cl_cap, kDense);
@@ -748,15 +753,15 @@ dg_status try_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   const int clusters = static_cast<int>(std::min<long long>(cl_cap, pair_tiles));
   *launched = true;
   if (bn == 240) {
-    if (with_c) return run_pair<kKind, kDense, kWideBN, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
-    return run_pair<kKind, false, kWideBN, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    if (with_c) return run_pair<kKind, kDense, kWideBN, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    return run_pair<kKind, false, kWideBN, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
   }
   if (bn == 256) {
-    if (with_c) return run_pair<kKind, kDense, 256, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
-    return run_pair<kKind, false, 256, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    if (with_c) return run_pair<kKind, kDense, 256, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    return run_pair<kKind, false, 256, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
   }
-  if (with_c) return run_pair<kKind, kDense, 192, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
-  return run_pair<kKind, false, 192, kOutF32>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+  if (with_c) return run_pair<kKind, kDense, 192, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+  return run_pair<kKind, false, 192, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
 }
 
 dg_status check_common(int N, int K) {
@@ -1378,6 +1383,22 @@ dg_status dg_fp8_fp4_gemm_nt(const void* a, const int32_t* sfa, const void* b, c
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
   const int sms = sms_to_use(*ds);
   const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
+  if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
+    dg::Params pp{};
+    pp.M = M;
+    pp.N = N;
+    pp.K = K;
+    pp.G = 1;
+    pp.c = static_cast<const __nv_bfloat16*>(c);
+    pp.d = static_cast<__nv_bfloat16*>(d);
+    pp.status = ds->status;
+    pp.timeout_ns = wait_timeout_ns();
+    pp.fault = g_fault.load();
+    bool launched = false;
+    const dg_status s = try_pair<dg::Kind::Dense, false, true>(*ds, a, sfa, b, sfb, c, d, pp, ceil_div(M, 256), sms,
+                                                               stream, &launched);
+    if (launched) return s;
+  }
   if (tiles128 < sms) {
     // few tiles: split-K over CTA pairs when the tiles fill the GPU that way, else stream-K
     if (const int sbn = pick_split_bn(M, N, K, sms, c != nullptr, true); sbn > 0) {
@@ -1417,6 +1438,23 @@ dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void* a, const int32_t* 
   if (reinterpret_cast<uintptr_t>(m_indices) & 3u) return DG_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  if (pair_enabled() && !std::getenv("DG_FORCE_BN")) {
+    dg::Params pp{};
+    pp.M = M_total;
+    pp.N = N;
+    pp.K = K;
+    pp.G = G;
+    pp.m_indices = m_indices;
+    pp.d = static_cast<__nv_bfloat16*>(d);
+    pp.status = ds->status;
+    pp.timeout_ns = wait_timeout_ns();
+    pp.fault = g_fault.load();
+    bool launched = false;
+    const dg_status s = try_pair<dg::Kind::Contiguous, false, true>(*ds, a, sfa, b, sfb, nullptr, d, pp,
+                                                                    ceil_div(M_total, 128), sms_to_use(*ds), stream,
+                                                                    &launched);
+    if (launched) return s;
+  }
   const int BN = pick_bn_fp4(dg::Kind::Contiguous, N);
   CUtensorMap ta, tb, tsa, tsb, td;
   if (!map_operand_2d(&ta, a, M_total, K, 128) || !map_operand_fp4(&tb, b, G, N, K, BN) ||

@@ -189,7 +189,7 @@ struct Scheduler {
   bool stream_k;
 
   __device__ __forceinline__ int clamped_mask(const Params& p, int g) const {
-    int m = __ldg(p.masked_m + g);
+    int m = ld_cg_s32(p.masked_m + g);
     return m < 0 ? 0 : (m > p.M ? p.M : m);
   }
 
@@ -223,7 +223,7 @@ struct Scheduler {
         long long kg_sum = 0, rows = 0;
         bool bad = false;
         for (int g = 0; g < p.G; ++g) {
-          const int k = __ldg(p.ks + g);
+          const int k = ld_cg_s32(p.ks + g);
           if (k < 0 || k % BLOCK_K != 0) bad = true;
           if (k > 0) {
             kg_sum += k / BLOCK_K;
@@ -240,7 +240,7 @@ struct Scheduler {
       g_tiles = p.G > 0 ? ceil_div_c(clamped_mask(p, 0), BLOCK_M) * num_n : 0;
       if (blockIdx.x == 0 && threadIdx.x == 0) {
         for (int g = 0; g < p.G; ++g) {
-          const int m = __ldg(p.masked_m + g);
+          const int m = ld_cg_s32(p.masked_m + g);
           if (m < 0 || m > p.M) atomicOr(p.status, kStatusBadIndexBit);
         }
       }
@@ -274,7 +274,7 @@ struct Scheduler {
       const int tpg = num_m * num_n;
       const int g = cur / tpg;
       while (g_cur < g) {   // experts are visited in increasing order
-        const int k = __ldg(p.ks + g_cur);
+        const int k = ld_cg_s32(p.ks + g_cur);
         if (k > 0) {
           kbase_cur += k / BLOCK_K;
           sfrow_cur += (k + 4 * BLOCK_K - 1) / (4 * BLOCK_K);
@@ -282,7 +282,7 @@ struct Scheduler {
         ++g_cur;
       }
       const int local = cur - g * tpg;
-      const int k = __ldg(p.ks + g);
+      const int k = ld_cg_s32(p.ks + g);
       s.tile = cur;
       s.g = g;
       s.m_blk = local / num_n;
@@ -360,7 +360,7 @@ struct Scheduler {
         s.valid_m = p.M;
         s.g = 0;
         if constexpr (kKind == Kind::Contiguous) {
-          const int g = __ldg(p.m_indices + s.m_blk * BLOCK_M);
+          const int g = ld_cg_s32(p.m_indices + s.m_blk * BLOCK_M);
           if (g < 0 || g >= p.G) {
             // a block led by an out-of-range index is reported once (by its n = 0 tile)
             if ((g < -1 || g >= p.G) && s.n_blk == 0 && threadIdx.x == 64) atomicOr(p.status, kStatusBadIndexBit);
@@ -764,7 +764,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
 #pragma unroll
         for (int u = 0; u < kUnits; ++u) {
           const int gcol = seg.n_blk * BN + rank * kSliceCols + 8 * u;
-          cv[u] = (row_ok && gcol < p.N) ? ld_global_nc_v4(p.c + static_cast<long long>(row) * p.N + gcol)
+          cv[u] = (row_ok && gcol < p.N) ? ld_cg_v4(p.c + static_cast<long long>(row) * p.N + gcol)
                                          : make_uint4(0, 0, 0, 0);
         }
       }
@@ -870,7 +870,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
         row_ok = row < p.M;
         d_row = row;
       } else if constexpr (kKind == Kind::Contiguous) {
-        const int gi = row < p.M ? __ldg(p.m_indices + row) : -1;
+        const int gi = row < p.M ? ld_cg_s32(p.m_indices + row) : -1;
         row_ok = gi == seg.g;
         if (gi != seg.g && gi != -1 && seg.n_blk == 0 && col_part == 0) atomicOr(p.status, kStatusBadIndexBit);
         d_row = row;
@@ -896,7 +896,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                   if (n0 + hcol + 4 * q < p.N) {
-                    const uint4 cv = ld_global_nc_v4(crow + 4 * q);
+                    const uint4 cv = ld_cg_v4(crow + 4 * q);
                     f[32 * h + 4 * q + 0] = __uint_as_float(cv.x) + f[32 * h + 4 * q + 0];
                     f[32 * h + 4 * q + 1] = __uint_as_float(cv.y) + f[32 * h + 4 * q + 1];
                     f[32 * h + 4 * q + 2] = __uint_as_float(cv.z) + f[32 * h + 4 * q + 2];
@@ -934,7 +934,7 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               if (n0 + col + 8 * q < p.N) {
-                const uint4 cv = ld_global_nc_v4(crow + 8 * q);
+                const uint4 cv = ld_cg_v4(crow + 8 * q);
                 const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {

@@ -27,7 +27,8 @@
 //               dense (an issuing thread's own shared-memory accesses stall it).
 // The scale words are consumed in the tcgen05.cp source layout, produced beforehand in a
 // workspace by sf_to_utccp_kernel: one 512-byte chunk per 128 rows of A per 4 K-groups,
-// and two per BN-wide tile of B per 4 K-groups (tile columns 0..127 and 128..255).
+// and two per BN-wide tile of B per 4 K-groups (tile columns 0..127 and 128..255), or per
+// K-group for FP4 B (one word per row: the scales of its four 32-wide blocks).
 // Operation: D = C + A @ B.T (DeepGEMM README "Interfaces / Notices", "Normal dense GEMMs",
 // "Grouped GEMMs (contiguous layout)", as reproduced on the page "Weight gradient kernels
 // for dense and MoE models #95").
@@ -37,7 +38,10 @@
 
 namespace dg {
 
-template <int kStages, int kBN, int kNumAccum>
+// kBF4: B is FP4 (E2M1 with one UE8M0 per row per 32 K), loaded through 16U4_ALIGN16B maps into
+// the same shared-memory shape as E4M3 (the barrier counts half the bytes); every stage then
+// carries scale chunks (A's K-quad chunk and this K-group's B chunks).
+template <int kStages, int kBN, int kNumAccum, bool kBF4 = false>
 struct PairConfig {
   static constexpr int BN = kBN;                 // tile width of the pair; each CTA loads BN/2 B rows
   static_assert(BN % 16 == 0 && BN >= 128 && BN <= 256, "tile width: a multiple of 16 in [128, 256]");
@@ -65,8 +69,8 @@ struct PairConfig {
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-  static constexpr int TX_AB = 2 * (A_BYTES + B_BYTES);           // both CTAs, every stage
-  static constexpr int TX_SF = 2 * (SFA_BYTES + SFB_BYTES);       // both CTAs, every 4th stage
+  static constexpr int TX_AB = 2 * (A_BYTES + (kBF4 ? B_BYTES / 2 : B_BYTES));   // both CTAs, every stage
+  static constexpr int TX_SF = 2 * (SFA_BYTES + SFB_BYTES);       // both CTAs, every scale stage
   // TMEM: kNumAccum BN-column accumulators and 2 x 4 SFA / 2 x 8 SFB columns, packed when
   // they fit; otherwise (two 240-column accumulators) the accumulators start at columns 0
   // and 256 and the scale columns sit in the 16 columns after each
@@ -95,7 +99,7 @@ struct PairScheduler {
     t = cluster;
     step = clusters;
     if constexpr (kKind == Kind::Contiguous) {
-      total = __ldg(p.pair_count) * num_n;
+      total = ld_cg_s32(p.pair_count) * num_n;
     } else {
       total = ceil_div_c(ceil_div_c(p.M, BLOCK_M), 2) * num_n;
     }
@@ -114,10 +118,9 @@ struct PairScheduler {
     s.tile = pair;
     s.valid_m = p.M;
     if constexpr (kKind == Kind::Contiguous) {
-      const int3 e = *reinterpret_cast<const int3*>(p.pair_list + 3 * pair);
-      s.m_blk = e.x;
-      s.g = e.y;
-      s.n_contrib = e.z;   // blocks of this pair that belong to the expert
+      s.m_blk = ld_cg_s32(p.pair_list + 3 * pair);
+      s.g = ld_cg_s32(p.pair_list + 3 * pair + 1);
+      s.n_contrib = ld_cg_s32(p.pair_list + 3 * pair + 2);   // blocks of the pair that are the expert's
     } else {
       s.g = 0;
       s.m_blk = 2 * pair;
@@ -126,9 +129,9 @@ struct PairScheduler {
   }
 };
 
-// kOutF32: FP32 C / D (the dense weight-gradient form), else BF16.
-template <Kind kKind, int kStages, int kBN, int kNumAccum, bool kHasC, bool kOutF32 = false>
-__global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads, 1)
+// kOutF32: FP32 C / D (the dense weight-gradient form), else BF16. kBF4: B in FP4.
+template <Kind kKind, int kStages, int kBN, int kNumAccum, bool kHasC, bool kOutF32 = false, bool kBF4 = false>
+__global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                          const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_d_tail,
@@ -136,7 +139,8 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
   static_assert(kKind != Kind::Masked, "the masked form uses the single-CTA kernel");
   static_assert(kKind == Kind::Dense || kBN % 64 == 0, "narrow last chunks: dense form only");
   static_assert(!kOutF32 || kKind == Kind::Dense, "FP32 output: dense form only");
-  using C = PairConfig<kStages, kBN, kNumAccum>;
+  static_assert(!kBF4 || !kOutF32, "FP4 B: BF16 output");
+  using C = PairConfig<kStages, kBN, kNumAccum, kBF4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -214,7 +218,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
             on_timeout();
             goto producer_done;
           }
-          const bool with_sf = (kb % 4) == 0;
+          const bool with_sf = kBF4 || (kb % 4) == 0;
           const uint32_t fb = map_to_rank(&full_bar[stage], 0);
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], C::TX_AB + (with_sf ? C::TX_SF : 0));
           uint8_t* sa = smem + C::OFF_A + stage * C::A_BYTES;
@@ -228,9 +232,11 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
           }
           if (with_sf) {
             const int q = kb / 4;
-            // SFA chunk row: (q, m_blk); SFB chunk rows: (g, q, n-block) and the next one
+            // SFA chunk row: (q, m_blk); SFB chunk rows: (g, q, n-block) and the next one, or
+            // with FP4 B (g, kb, n-block): one pair of chunks per K-group
             tma_load_2d_pair(ssf, &tm_sfa, fb, 0, q * p.sf_num_mb + m_blk);
-            tma_load_2d_pair(ssf + C::SFA_BYTES, &tm_sfb, fb, 0, (seg.g * KP + q) * p.sf_nb + 2 * seg.n_blk);
+            const int b_row = kBF4 ? seg.g * num_kb + kb : seg.g * KP + q;
+            tma_load_2d_pair(ssf + C::SFA_BYTES, &tm_sfb, fb, 0, b_row * p.sf_nb + 2 * seg.n_blk);
           }
           ++issued;
           if (++stage == kStages) {
@@ -252,7 +258,8 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
     // ================================ MMA issuer (leader) ===========================
     // One thread of the leader runs the whole loop (no warp-wide synchronisation per K-group).
     if (leader && lane == 0) {
-      constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(2 * BLOCK_M, C::BN);
+      // B format field [10,13): 0 = E4M3, 5 = E2M1
+      constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(2 * BLOCK_M, C::BN) | (kBF4 ? 5u << 10 : 0u);
       const uint64_t a_desc0 = make_smem_desc(smem_addr(smem + C::OFF_A), 16, 1024, kLayoutSwizzle128B);
       const uint64_t b_desc0 = make_smem_desc(smem_addr(smem + C::OFF_B), 16, 1024, kLayoutSwizzle128B);
       uint32_t stage = 0, phase = 0, tile_iter = 0, sf_iter = 0;
@@ -272,8 +279,8 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
               goto mma_done;
             }
             tc_fence_after();
-            if (kb % 4 == 0) {
-              // the scales of this K-quad are in TMEM buffer (sf_iter & 1); the other
+            if (kBF4 || kb % 4 == 0) {
+              // the scales of this K-quad (K-group, FP4 B) are in TMEM buffer (sf_iter & 1); the other
               // buffer's readers are all issued: it may be refilled once they complete
               if (sf_iter > 0) tc_commit_pair(&sf_free_bar[(sf_iter - 1) & 1]);
               const uint32_t buf = sf_iter & 1;
@@ -283,11 +290,13 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
             }
             const uint64_t adesc = a_desc0 + ((stage * C::A_BYTES) >> 4);
             const uint64_t bdesc = b_desc0 + ((stage * C::B_BYTES) >> 4);
-            const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kb % 4);
 #pragma unroll
-            for (int k = 0; k < BLOCK_K / 32; ++k)
+            for (int k = 0; k < BLOCK_K / 32; ++k) {
+              // B's scale byte: the K-group's (FP8) or the k-th 32-wide block's (FP4)
+              const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kBF4 ? k : kb % 4);
               mma_mxf8_block_scale_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
                                         (kb | k) != 0);
+            }
             tc_commit_pair(&empty_bar[stage]);
             if (++stage == kStages) {
               stage = 0;
@@ -317,7 +326,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
             on_timeout();
             goto ready_done;
           }
-          if (kb % 4 == 0) {
+          if (kBF4 || kb % 4 == 0) {
             if (sf_iter >= 2 && !mbar_wait(&sf_free_bar[sf_iter & 1], ((sf_iter >> 1) - 1) & 1, p.timeout_ns)) {
               on_timeout();
               goto ready_done;
@@ -399,7 +408,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
       if constexpr (kKind == Kind::Dense) {
         row_ok = row < p.M;
       } else {
-        const int gi = row < p.M ? __ldg(p.m_indices + row) : -1;
+        const int gi = row < p.M ? ld_cg_s32(p.m_indices + row) : -1;
         row_ok = gi == seg.g;
         // a row of the expert's own blocks that names another expert violates the layout
         if (gi != seg.g && gi != -1 && static_cast<int>(rank) < seg.n_contrib && seg.n_blk == 0 && wq == 0)
@@ -444,7 +453,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                   if (4 * q < hw && n0 + hcol + 4 * q < p.N) {
-                    const uint4 cv = ld_global_nc_v4(crow + 4 * q);
+                    const uint4 cv = ld_cg_v4(crow + 4 * q);
                     f[32 * h + 4 * q + 0] = __uint_as_float(cv.x) + f[32 * h + 4 * q + 0];
                     f[32 * h + 4 * q + 1] = __uint_as_float(cv.y) + f[32 * h + 4 * q + 1];
                     f[32 * h + 4 * q + 2] = __uint_as_float(cv.z) + f[32 * h + 4 * q + 2];
@@ -479,7 +488,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum>::kThreads,
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               if (q < units && n0 + col + 8 * q < p.N) {
-                const uint4 cv = ld_global_nc_v4(crow + 8 * q);
+                const uint4 cv = ld_cg_v4(crow + 8 * q);
                 const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -562,10 +571,12 @@ struct SfPrepArgs {
   const int32_t* sfa;   // [KP][lda] words
   int32_t* sfa_out;     // [KP][a_blocks][128]
   int a_rows, lda, a_blocks;
-  const int32_t* sfb;   // [G][KP][ldb] words
-  int32_t* sfb_out;     // [G][KP][b_chunks][128]
+  const int32_t* sfb;   // [G][b_kp][ldb] words
+  int32_t* sfb_out;     // [G][b_kp][b_chunks][128]
   int groups, b_rows, ldb, b_chunks, tile_bn;
-  int kp;
+  int kp;               // A's word rows (K-quads)
+  int b_kp;             // B's word rows: K-quads (one word per 128-row block), or K-groups with
+  int b_per_row;        // b_per_row set (FP4 B: one word per row, its four 32-wide blocks)
 };
 
 // Pair rows of the contiguous layout, by one block: block b (of 128 rows) belongs to the
@@ -583,7 +594,7 @@ __device__ void build_pair_list(const SfPrepArgs& a) {
   int prev_g = -2;             // expert of the block before this chunk
   int count_carry = 0;
   auto expert = [&](int b) {
-    const int g = __ldg(a.m_indices + static_cast<long long>(b) * 128);
+    const int g = ld_cg_s32(a.m_indices + static_cast<long long>(b) * 128);
     return (g >= 0 && g < a.groups_g) ? g : -1;
   };
   for (int base = 0; base < a.num_mb; base += nt) {
@@ -591,7 +602,7 @@ __device__ void build_pair_list(const SfPrepArgs& a) {
     const bool in = b < a.num_mb;
     int raw = -1;
     if (in) {
-      raw = __ldg(a.m_indices + static_cast<long long>(b) * 128);
+      raw = ld_cg_s32(a.m_indices + static_cast<long long>(b) * 128);
       if (raw < -1 || raw >= a.groups_g) atomicOr(a.status, kStatusBadIndexBit);
     }
     const int g = in && raw >= 0 && raw < a.groups_g ? raw : -1;
@@ -649,7 +660,7 @@ __global__ void sf_to_utccp_kernel(const SfPrepArgs a) {
   }
   const int sf_blocks = gridDim.x - (a.m_indices != nullptr ? 1 : 0);
   const long long na = static_cast<long long>(a.kp) * a.a_blocks * 128;
-  const long long total = na + static_cast<long long>(a.groups) * a.kp * a.b_chunks * 128;
+  const long long total = na + static_cast<long long>(a.groups) * a.b_kp * a.b_chunks * 128;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<long long>(sf_blocks) * blockDim.x) {
     int32_t val = 0;
@@ -659,16 +670,16 @@ __global__ void sf_to_utccp_kernel(const SfPrepArgs a) {
       const int b = static_cast<int>(chunk % a.a_blocks);
       const long long q = chunk / a.a_blocks;
       const int row = b * 128 + 32 * (w % 4) + w / 4;
-      if (row < a.a_rows) val = __ldg(a.sfa + q * a.lda + row);
+      if (row < a.a_rows) val = ld_cg_s32(a.sfa + q * a.lda + row);
       a.sfa_out[idx] = val;
     } else {
       const long long j = idx - na;
       const int w = static_cast<int>(j % 128);
-      const long long chunk = j / 128;                // (g * kp + q) * b_chunks + c
+      const long long chunk = j / 128;                // (g * b_kp + q) * b_chunks + c
       const int c = static_cast<int>(chunk % a.b_chunks);
       const long long gq = chunk / a.b_chunks;
       const int row = (c / 2) * a.tile_bn + (c % 2) * 128 + 32 * (w % 4) + w / 4;
-      if (row < a.b_rows) val = __ldg(a.sfb + gq * a.ldb + row / 128);
+      if (row < a.b_rows) val = ld_cg_s32(a.sfb + gq * a.ldb + (a.b_per_row ? row : row / 128));
       a.sfb_out[j] = val;
     }
   }

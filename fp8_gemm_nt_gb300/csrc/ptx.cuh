@@ -289,11 +289,23 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
+// Loads of kernel inputs. With programmatic dependent launch a kernel's lifetime overlaps the
+// grid that produced its inputs (our scale/pair-list preparation, or the caller's previous
+// kernel), so the read-only (.nc) path's contract does not hold; and an SM's L1 may keep
+// lines from before the producer finished. Inputs are therefore read at L2 (.cg), the GPU's
+// point of coherence, after griddepcontrol.wait.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.cg.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_cg_s32(const int* p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 

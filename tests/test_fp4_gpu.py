@@ -4,9 +4,10 @@ the FP64 oracle, through the C ABI.
 Bar as for the FP8 forms: per element |d - ref| <= 1e-2*|ref| + 1e-2*rms(ref) and the
 cosine-style difference below 1e-3; bit-exact where the result is exact in BF16 (one-hot
 B) and for everything integer indexing decides (padding and masked rows keep the sentinel).
-The dense shapes are chosen to reach every launch form the dispatcher has for FP4 B:
-tile mode with 128- and 256-wide tiles, stream-K with two K-groups per stage (an odd
-K-group count leaves the last stage half past K), and split-K over CTA pairs.
+The shapes are chosen to reach every launch form the dispatcher has for FP4 B: the CTA-pair
+kernel at each width (256, 240, 192), single-CTA tile mode with 128- and 256-wide tiles,
+stream-K with two K-groups per stage (an odd K-group count leaves the last stage half past
+K), and split-K over CTA pairs.
 """
 from __future__ import annotations
 
@@ -46,8 +47,8 @@ DENSE_SHAPES = [
     (256, 384, 1152, False),     # stream-K, two K-groups per stage, KG = 9
     (130, 1040, 2048, True),     # split-K, wider
     (513, 272, 256, False),      # tile mode, KG = 2
-    (1024, 2560, 256, False),    # tile mode, 256-wide tiles (>= one tile per SM)
-    (1280, 2432, 384, True),     # tile mode, 128-wide tiles (256 would waste columns), with C
+    (1024, 2560, 256, False),    # >= one tile per SM: the CTA-pair kernel
+    (1280, 2432, 384, True),     # the CTA-pair kernel, with C
 ]
 
 
@@ -169,3 +170,69 @@ def test_fp4_misaligned_b_rejected(lib):
         lib.dg_fp8_fp4_gemm_nt(dev(p.a), dev(p.sfa), b, dev(p.sfb), None, d)
     assert e.value.status == 3
     assert (bf16_bits(d) == SENTINEL).all()
+
+
+# --------------------------------------------------------------------------------------
+# FP4 B on the CTA-pair kernel (with 8 SMs in use, small problems have enough tiles)
+# --------------------------------------------------------------------------------------
+
+@pytest.fixture
+def few_sms(lib):
+    lib.dg_set_num_sms(8)
+    yield
+    lib.dg_set_num_sms(0)
+
+
+@pytest.fixture(params=[256, 240, 192])
+def pair_bn(request, monkeypatch):
+    monkeypatch.setenv("DG_PAIR_BN", str(request.param))
+    return request.param
+
+
+@pytest.mark.parametrize("M,N,K,with_c", [
+    (256, 256, 128, False),
+    (384, 512, 640, True),       # odd number of 128-row blocks
+    (300, 400, 1152, True),      # ragged M and N, K-groups not a multiple of 4
+    (1024, 768, 2048, False),    # several pair tiles per CTA pair
+    (512, 496, 640, True),       # N = 2 x 240 + 16: the last tile's narrow chunk lies past N
+])
+def test_fp4_pair_dense(lib, few_sms, pair_bn, M, N, K, with_c):
+    p = W.make_dense_fp4(M, N, K, seed=3000 + M + N + K, with_c=with_c)
+    d = run_dense(lib, p)
+    ref = O.fp8_fp4_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, M, N, K)
+    assert_parity(bf16_f64(d), ref, f"fp4 pair dense {M}x{N}x{K}")
+
+
+def test_fp4_pair_one_hot_exact(lib, few_sms, pair_bn):
+    M, N, K = 512, 512, 640
+    rng = np.random.default_rng(pair_bn)
+    p = W.make_dense_fp4(M, N, K, seed=17)
+    k0 = rng.integers(0, K, size=N)
+    b = np.zeros((N, K // 2), np.uint8)
+    for n, k in enumerate(k0):
+        b[n, k // 2] = 2 << (4 * (k % 2))
+    p.b, p.sfb = b, W.pack_sf(rng.integers(120, 135, size=(N, K // 32)).astype(np.uint8))
+    d = bf16_f64(run_dense(lib, p))
+    assert np.array_equal(d, O.fp8_fp4_gemm_nt(p.a, p.sfa, p.b, p.sfb, None, M, N, K))
+
+
+@pytest.mark.parametrize("counts,N,K", [([300, 0, 129], 256, 512), ([1, 255, 200, 77], 384, 896)])
+def test_fp4_contiguous_single_cta(lib, counts, N, K, monkeypatch):
+    monkeypatch.setenv("DG_PAIR", "0")
+    p = W.make_contiguous(G=len(counts), tokens=sum(counts), N=N, K=K, seed=81 + N, counts=counts,
+                          b_format="e2m1")
+    d = run_contiguous(lib, p)
+    ref, valid = O.m_grouped_fp8_fp4_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K,
+                                                        p.G)
+    assert (bf16_bits(d)[~valid] == SENTINEL).all()
+    assert_parity(bf16_f64(d)[valid], ref[valid], f"fp4 contiguous single-CTA {counts}")
+
+
+@pytest.mark.parametrize("M,N,K,with_c", [(1024, 2560, 256, False), (1280, 2432, 384, True)])
+def test_fp4_dense_single_cta_tile_mode(lib, M, N, K, with_c, monkeypatch):
+    # 256- and 128-wide single-CTA tiles (the pair kernel takes these shapes by default)
+    monkeypatch.setenv("DG_PAIR", "0")
+    p = W.make_dense_fp4(M, N, K, seed=4000 + M + N + K, with_c=with_c)
+    d = run_dense(lib, p)
+    ref = O.fp8_fp4_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, M, N, K)
+    assert_parity(bf16_f64(d), ref, f"fp4 single-CTA tile mode {M}x{N}x{K}")

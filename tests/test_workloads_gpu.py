@@ -6,6 +6,8 @@ bit-exactly over the whole output.
 """
 from __future__ import annotations
 
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -25,6 +27,11 @@ def lib():
     import fp8_gemm_nt_gb300 as L
     L.load_library()
     return L
+
+
+@functools.lru_cache(maxsize=1)
+def _workload(name):
+    return W.make_workload(name)
 
 
 def _rows(n, k, seed):
@@ -143,7 +150,7 @@ def test_fp4_masked_workload(lib):
 
 def test_fp4_contiguous_workload(lib):
     name = "fp4_contiguous_g8_t32768_n4096_k7168"
-    p = W.make_workload(name)
+    p = _workload(name)
     d = run_contiguous(lib, p)
     bits = bf16_bits(d)
     pad = p.m_indices < 0
@@ -157,3 +164,21 @@ def test_fp4_contiguous_workload(lib):
     assert valid.all()
     assert_parity(bf16_f64(d)[rows], ref, name)
     assert lib.dg_get_device_status() == 0
+
+
+def test_contiguous_pair_fresh_streams(lib):
+    # Batches of back-to-back launches, each batch on a new stream (a new, freshly zeroed
+    # workspace for the preparation kernel's pair list). A CTA that read a stale pair count
+    # (an L1 line from before the preparation kernel wrote it) once left its cluster partner
+    # waiting: 9 of 60 such batches of this workload timed out on GB300 before the kernels
+    # read their inputs at L2.
+    p = _workload("fp4_contiguous_g8_t32768_n4096_k7168")
+    a, sfa, b, sfb, idx = dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb), dev(p.m_indices)
+    d = sentinel_like((p.M_total, p.N))
+    for batch in range(24):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for _ in range(25):
+                lib.dg_m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa, b, sfb, d, idx)
+        torch.cuda.synchronize()
+        assert lib.dg_get_device_status() == 0, f"batch {batch}"
