@@ -214,7 +214,7 @@ template <dg::Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps_, in
           int kKG = 1, int kSplit = 0, bool kOutF32 = false, bool kAMN = false, bool kBMN = false, bool kBF4 = false>
 struct Launcher {
   static constexpr int kEpiWarps = kEpiWarps_;
-  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4>;
+  using Cfg = dg::Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4, dg::count_cache_for(kKind)>;
   static constexpr int kBN = BN;
   static constexpr auto kernel() {
     return dg::fp8_gemm_kernel<kKind, BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kHasC, kKG, kSplit, kOutF32,
@@ -446,7 +446,7 @@ struct PairLauncher {
 
   static dg_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                           const CUtensorMap& tsb, const CUtensorMap& td, const CUtensorMap& td_tail,
-                          const dg::Params& p, int clusters, cudaStream_t stream) {
+                          const CUtensorMap& tc, const dg::Params& p, int clusters, cudaStream_t stream) {
     auto kern = kernel();
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -462,7 +462,7 @@ struct PairLauncher {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, td_tail, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, td, td_tail, tc, p);
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
       std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d pair 256x%d accum=%d stages=%d clusters=%d smem=%d fp4=%d\n",
@@ -666,8 +666,14 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
     if (e != cudaSuccess) return cuda_fail(e);
   }
 
-  CUtensorMap ta, tb, tsa, tsb, td, td_tail;
+  CUtensorMap ta, tb, tsa, tsb, td, td_tail, tc;
   bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) && (kOutF32 ? map_out_f32(&td, d, p.M, p.N) : map_out(&td, d, 0, p.M, p.N));
+  // C is read by TMA in boxes of the output's geometry (the map of D over C's memory)
+  void* c_mem = const_cast<void*>(static_cast<const void*>(p.c));
+  if (kHasC)
+    ok = ok && (kOutF32 ? map_out_f32(&tc, c_mem, p.M, p.N) : map_out(&tc, c_mem, 0, p.M, p.N));
+  else
+    tc = td;
   if constexpr (kBN % 64 != 0) {
     // the narrower end of each tile, 32 rows high, no swizzle: BF16 its last kBN % 64
     // columns; FP32 its last (kBN % 64) % 32 columns (the rest goes out as 32-column boxes)
@@ -698,7 +704,7 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   if (!ok) return DG_ERR_CUDA;
   p.sf_num_mb = num_mb;
   p.sf_nb = sfb_rows;
-  return PairLauncher<kKind, kHasC, kBN, kOutF32, kBF4>::launch(ta, tb, tsa, tsb, td, td_tail, p, clusters, stream);
+  return PairLauncher<kKind, kHasC, kBN, kOutF32, kBF4>::launch(ta, tb, tsa, tsb, td, td_tail, tc, p, clusters, stream);
 }
 
 // Pair tile width: DG_PAIR_BN (192, 240 or 256) overrides; 240 is offered for the dense

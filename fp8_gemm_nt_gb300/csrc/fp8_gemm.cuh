@@ -50,6 +50,9 @@ constexpr int BLOCK_M = 128;
 constexpr int BLOCK_K = 128;   // one scale group per pipeline stage
 constexpr int SF_BLOCK_N = 128;
 constexpr int kPrefetchKGroups = 4;   // K-groups of the first segment prefetched into L2 at launch
+constexpr int kMaskCountCache = 1024;   // masked form: group counts cached in shared memory (more: read at L2)
+
+__host__ __device__ constexpr int count_cache_for(Kind k) { return k == Kind::Masked ? kMaskCountCache : 0; }
 
 struct Params {
   int M;   // dense: M; contiguous: M_total; masked: max_m (rows per group)
@@ -104,8 +107,10 @@ __host__ __device__ constexpr int ceil_div_c(int a, int b) { return (a + b - 1) 
 // the global bytes read (BN x 64 per K-group; measured on GB300). Every stage then carries
 // the scale words: A's packed word per row (as in FP8) and, per K-group, one word per B row
 // holding the scales of its four 32-wide blocks.
+// kCountCache: per-group row counts (the masked form's device-side counts) held in shared
+// memory, read once per CTA, so that the schedule walk of every role reads them there.
 template <int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, int kKG = 1, int kSplit = 0,
-          bool kBF4 = false>
+          bool kBF4 = false, int kCountCache = 0>
 struct Config {
   static_assert(kKG == 1 || kKG == 2, "one or two K-groups per stage");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
@@ -140,7 +145,8 @@ struct Config {
   static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * kEpiBufs * EPI_BUF_BYTES;
   static constexpr int NUM_BARS = 3 * kStages + 2 * kNumAccum + 1;   // + scale-ready per stage
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;       // + slack for manual alignment
+  static constexpr int OFF_COUNTS = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = OFF_COUNTS + 4 * kCountCache + 1024;   // + slack for manual alignment
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 
   // tensor memory columns
@@ -187,13 +193,19 @@ struct Scheduler {
   int t;                         // tile mode: next tile index
   long long u, u_end, U;         // stream-K: this CTA's K-group range, total K-groups
   bool stream_k;
+  const int* counts;             // masked: the group counts cached in shared memory (or null)
+
+  __device__ __forceinline__ int raw_mask(const Params& p, int g) const {
+    return (counts != nullptr && g < kMaskCountCache) ? counts[g] : ld_cg_s32(p.masked_m + g);
+  }
 
   __device__ __forceinline__ int clamped_mask(const Params& p, int g) const {
-    int m = ld_cg_s32(p.masked_m + g);
+    const int m = raw_mask(p, g);
     return m < 0 ? 0 : (m > p.M ? p.M : m);
   }
 
-  __device__ __forceinline__ explicit Scheduler(const Params& p) {
+  __device__ __forceinline__ explicit Scheduler(const Params& p, const int* cached_counts = nullptr) {
+    counts = cached_counts;
     num_n = ceil_div_c(p.N, BN);
     num_m = ceil_div_c(p.M, BLOCK_M);
     num_kb = p.K / BLOCK_K;
@@ -240,7 +252,7 @@ struct Scheduler {
       g_tiles = p.G > 0 ? ceil_div_c(clamped_mask(p, 0), BLOCK_M) * num_n : 0;
       if (blockIdx.x == 0 && threadIdx.x == 0) {
         for (int g = 0; g < p.G; ++g) {
-          const int m = ld_cg_s32(p.masked_m + g);
+          const int m = raw_mask(p, g);
           if (m < 0 || m > p.M) atomicOr(p.status, kStatusBadIndexBit);
         }
       }
@@ -383,6 +395,35 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
+// C of one output chunk (32 rows x 128 bytes: 64 BF16 or 32 FP32 columns) into a warp's
+// staging buffer, in the layout the output staging uses (row r's 16-byte piece j at
+// r * 128 + (j ^ (r & 7)) * 16). The warp loads it together, four 128-byte rows per
+// instruction (a lane per row would touch 32 lines per instruction), at L2. c0 points at
+// lane 0's row and the chunk's first column; rows whose bit in ok_mask is clear and pieces
+// at or past `cols` elements (or past `pieces`) read as zero.
+template <typename T, int kPieces = 8>
+__device__ __forceinline__ void warp_stage_c(uint32_t sbuf, const T* c0, long long ld, uint32_t ok_mask, int cols,
+                                             uint32_t lane) {
+  constexpr int kPer = 16 / static_cast<int>(sizeof(T));   // elements per 16-byte piece
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {   // two rounds of four loads in flight (register budget)
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = (4 * half + i) * 32 + static_cast<int>(lane);
+      const int r = idx >> 3, j = idx & 7;
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (j < kPieces && ((ok_mask >> r) & 1u) && kPer * j < cols) v[i] = ld_cg_v4(c0 + r * ld + kPer * j);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = (4 * half + i) * 32 + static_cast<int>(lane);
+      const int r = idx >> 3, j = idx & 7;
+      if (j < kPieces) st_shared_v4(sbuf + r * 128 + ((j ^ (r & 7)) * 16), v[i].x, v[i].y, v[i].z, v[i].w);
+    }
+  }
+}
+
 __device__ __forceinline__ void st_global_v4f(float* p, float a, float b, float c, float d) {
   asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
@@ -405,11 +446,12 @@ __device__ __forceinline__ float4 ld_global_cg_v4f(const float* p) {
 // and each 32-deep K step of the MMA advances it by 32 rows = 4 KB.
 template <Kind kKind, int BN, int kStages, int kNumAccum, int kEpiWarps, int kEpiBufs, bool kHasC, int kKG = 1,
           int kSplit = 0, bool kOutF32 = false, bool kAMN = false, bool kBMN = false, bool kBF4 = false>
-__global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4>::kThreads, 1)
+__global__ void __launch_bounds__(
+    Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4, count_cache_for(kKind)>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_d, const Params p) {
-  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4>;
+  using C = Config<BN, kStages, kNumAccum, kEpiWarps, kEpiBufs, kKG, kSplit, kBF4, count_cache_for(kKind)>;
   static_assert(!kBF4 || (!kAMN && !kBMN && !kOutF32 && kKind != Kind::KGrouped),
                 "FP4 B: K-major operands, BF16 output, dense / contiguous / masked forms");
   static_assert(kSplit == 0 || kKind == Kind::Dense, "split-K clusters: dense form only");
@@ -503,7 +545,17 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
     *abort_flag = 1;
   };
 
-  Scheduler<kKind, BN, kKG, kSplit> sched(p);
+  const int* cached_counts = nullptr;
+  if constexpr (kKind == Kind::Masked) {
+    // the group counts, read once at L2 (they may come from the previous kernel) into
+    // shared memory for every role's schedule walk
+    int* cache = reinterpret_cast<int*>(smem + C::OFF_COUNTS);
+    const int n = p.G < kMaskCountCache ? p.G : kMaskCountCache;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) cache[i] = ld_cg_s32(p.masked_m + i);
+    __syncthreads();
+    cached_counts = cache;
+  }
+  Scheduler<kKind, BN, kKG, kSplit> sched(p, cached_counts);
   Segment seg;
 
   if (warp == 0) {
@@ -758,15 +810,15 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
       const int rank = seg.slot;
       const int row = seg.m_blk * BLOCK_M + row_in_tile;
       const bool row_ok = ok && row < p.M;
-      // C of this CTA's output slice, loaded while the MMAs run
-      uint4 cv[kHasC ? kUnits : 1];
+      // C of this CTA's output slice, staged (coalesced) in the warp's epilogue buffer, which
+      // this path does not otherwise use, while the MMAs run
+      const uint32_t cstage = smem_addr(smem + C::OFF_EPI + (warp - 2) * C::EPI_BUF_BYTES);
       if constexpr (kHasC) {
-#pragma unroll
-        for (int u = 0; u < kUnits; ++u) {
-          const int gcol = seg.n_blk * BN + rank * kSliceCols + 8 * u;
-          cv[u] = (row_ok && gcol < p.N) ? ld_cg_v4(p.c + static_cast<long long>(row) * p.N + gcol)
-                                         : make_uint4(0, 0, 0, 0);
-        }
+        const int gcol0 = seg.n_blk * BN + rank * kSliceCols;
+        const uint32_t ok_rows = __ballot_sync(0xffffffffu, row_ok);
+        const int row0 = seg.m_blk * BLOCK_M + quad * 32;
+        warp_stage_c<__nv_bfloat16, kUnits>(cstage, p.c + static_cast<long long>(row0) * p.N + gcol0, p.N, ok_rows,
+                                            p.N - gcol0, lane);
       }
       if (ok) {
         ok = warp_wait(&tfull_bar[0], 0, p.timeout_ns, abort_flag);
@@ -824,7 +876,8 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
           }
           if (row_ok && gcol < p.N) {
             if constexpr (kHasC) {
-              const uint32_t cw[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
+              const uint4 cvu = ld_shared_v4(cstage + lane * 128 + ((u ^ (lane & 7)) * 16));
+              const uint32_t cw[4] = {cvu.x, cvu.y, cvu.z, cvu.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cw[e]));
@@ -890,26 +943,26 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int hcol = col + 32 * h;
-            if constexpr (kHasC) {
-              if (row_ok && !c_added) {
-                const float* crow = cbase + d_row * p.N + n0 + hcol;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  if (n0 + hcol + 4 * q < p.N) {
-                    const uint4 cv = ld_cg_v4(crow + 4 * q);
-                    f[32 * h + 4 * q + 0] = __uint_as_float(cv.x) + f[32 * h + 4 * q + 0];
-                    f[32 * h + 4 * q + 1] = __uint_as_float(cv.y) + f[32 * h + 4 * q + 1];
-                    f[32 * h + 4 * q + 2] = __uint_as_float(cv.z) + f[32 * h + 4 * q + 2];
-                    f[32 * h + 4 * q + 3] = __uint_as_float(cv.w) + f[32 * h + 4 * q + 3];
-                  }
-                }
-              }
-            }
             uint8_t* sbuf = stage_base + (buf_iter % kEpiBufs) * C::EPI_BUF_BYTES;
             ++buf_iter;
             if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
             __syncwarp();
             const uint32_t srow = smem_addr(sbuf) + lane * 128;
+            if constexpr (kHasC) {
+              if (!c_added) {
+                const long long row0 = __shfl_sync(0xffffffffu, d_row, 0);
+                warp_stage_c(smem_addr(sbuf), cbase + row0 * p.N + n0 + hcol, p.N, ok_mask, p.N - (n0 + hcol), lane);
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const uint4 cv = ld_shared_v4(srow + ((q ^ (lane & 7)) * 16));
+                  f[32 * h + 4 * q + 0] = __uint_as_float(cv.x) + f[32 * h + 4 * q + 0];
+                  f[32 * h + 4 * q + 1] = __uint_as_float(cv.y) + f[32 * h + 4 * q + 1];
+                  f[32 * h + 4 * q + 2] = __uint_as_float(cv.z) + f[32 * h + 4 * q + 2];
+                  f[32 * h + 4 * q + 3] = __uint_as_float(cv.w) + f[32 * h + 4 * q + 3];
+                }
+              }
+            }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
               st_shared_v4(srow + ((u ^ (lane & 7)) * 16), __float_as_uint(f[32 * h + 4 * u]),
@@ -928,30 +981,30 @@ __global__ void __launch_bounds__(Config<BN, kStages, kNumAccum, kEpiWarps, kEpi
           }
           return;
         }
-        if constexpr (kHasC) {
-          if (row_ok && !c_added) {
-            const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              if (n0 + col + 8 * q < p.N) {
-                const uint4 cv = ld_cg_v4(crow + 8 * q);
-                const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162*>(&cw[e]);
-                  const float2 cf = __bfloat1622float2(c2);
-                  f[8 * q + 2 * e] = cf.x + f[8 * q + 2 * e];
-                  f[8 * q + 2 * e + 1] = cf.y + f[8 * q + 2 * e + 1];
-                }
-              }
-            }
-          }
-        }
         uint8_t* sbuf = stage_base + (buf_iter % kEpiBufs) * C::EPI_BUF_BYTES;
         ++buf_iter;
         if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
         __syncwarp();
         const uint32_t srow = smem_addr(sbuf) + lane * 128;
+        if constexpr (kHasC) {
+          if (!c_added) {
+            const long long row0 = __shfl_sync(0xffffffffu, d_row, 0);
+            warp_stage_c(smem_addr(sbuf), p.c + row0 * p.N + n0 + col, p.N, ok_mask, p.N - (n0 + col), lane);
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint4 cv = ld_shared_v4(srow + ((q ^ (lane & 7)) * 16));
+              const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162*>(&cw[e]);
+                const float2 cf = __bfloat1622float2(c2);
+                f[8 * q + 2 * e] = cf.x + f[8 * q + 2 * e];
+                f[8 * q + 2 * e + 1] = cf.y + f[8 * q + 2 * e + 1];
+              }
+            }
+          }
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           uint32_t w[4];

@@ -64,8 +64,8 @@ struct PairConfig {
   static constexpr int OFF_EPI = ((OFF_SF + kStages * SF_STRIDE + 1023) / 1024) * 1024;
   static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_BUF_BYTES;
   // full / empty / ready per stage, tfull / tempty per accumulator, MMA drain, copy drain,
-  // one "scale buffer free" barrier per TMEM scale buffer
-  static constexpr int NUM_BARS = 3 * kStages + 2 * kNumAccum + 4;
+  // one "scale buffer free" barrier per TMEM scale buffer, one "C landed" per epilogue warp
+  static constexpr int NUM_BARS = 3 * kStages + 2 * kNumAccum + 4 + kEpiWarps;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                          const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_d_tail,
-                         const Params p) {
+                         const __grid_constant__ CUtensorMap tm_c, const Params p) {
   static_assert(kKind != Kind::Masked, "the masked form uses the single-CTA kernel");
   static_assert(kKind == Kind::Dense || kBN % 64 == 0, "narrow last chunks: dense form only");
   static_assert(!kOutF32 || kKind == Kind::Dense, "FP32 output: dense form only");
@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
   uint64_t* ready_bar = drain_bar + 1;          // [kStages] leader: stage handed to the MMA thread
   uint64_t* sf_drain_bar = ready_bar + kStages;
   uint64_t* sf_free_bar = sf_drain_bar + 1;     // [2] leader: MMAs reading TMEM scale buffer b completed
+  uint64_t* c_bar = sf_free_bar + 2;            // [kEpiWarps] this CTA: a C box landed in warp w's staging
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
     mbar_init(sf_drain_bar, 1);
     mbar_init(&sf_free_bar[0], 1);
     mbar_init(&sf_free_bar[1], 1);
+    for (int w = 0; w < C::kEpiWarps; ++w) mbar_init(&c_bar[w], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -187,6 +189,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
     tma_prefetch_desc(&tm_sfa);
     tma_prefetch_desc(&tm_sfb);
     tma_prefetch_desc(&tm_d);
+    if constexpr (kHasC) tma_prefetch_desc(&tm_c);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
@@ -365,12 +368,34 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
     const int col0 = kCols * wq;                     // first tile column of this warp
     uint8_t* sbuf = smem + C::OFF_EPI + ew * C::EPI_BUF_BYTES;
     uint32_t tile_iter = 0;
+    uint32_t c_loads = 0;   // C boxes loaded into sbuf (parity of c_bar[ew])
+    // C of one staging box (32 rows x 128 bytes at column x of the tile's rows, the layout of
+    // the output box) by TMA into sbuf, for the warp to add from shared memory. A tile's first
+    // box is issued before the accumulator is ready (it lands while the MMAs run).
+    auto issue_c_box = [&](int x) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&c_bar[ew], 32 * 128);
+        tma_load_2d(sbuf, &tm_c, &c_bar[ew], x, (seg.m_blk + static_cast<int>(rank)) * BLOCK_M + quad * 32);
+      }
+    };
+    auto wait_c_box = [&]() {
+      const bool ok = warp_wait(&c_bar[ew], c_loads & 1, p.timeout_ns, abort_flag);
+      ++c_loads;
+      if (!ok && lane == 0) on_timeout();
+    };
     while (sched.next(p, seg)) {
       const uint32_t acc = tile_iter % kNumAccum;
+      if constexpr (kHasC) {
+        if (lane == 0) bulk_wait_group_read<0>();   // the previous tile's last store has read sbuf
+        __syncwarp();
+        issue_c_box(seg.n_blk * C::BN + col0);
+      }
       if (!warp_wait(&tfull_bar[acc], (tile_iter / kNumAccum) & 1, p.timeout_ns, abort_flag)) {
         if (lane == 0) on_timeout();
+        if constexpr (kHasC) wait_c_box();   // no copy may still be landing at exit
         break;
       }
+      if constexpr (kHasC) wait_c_box();
       ++tile_iter;
       tc_fence_after();
       const uint32_t taddr =
@@ -440,30 +465,33 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
         if constexpr (kOutF32) {
           // FP32: 32-column halves, one 128-byte swizzled TMA box each (tm_d); a 16-column
           // half (the end of a 240-wide tile) as plain 64-byte rows (tm_d_tail)
-          const float* cbase = reinterpret_cast<const float*>(p.c);
           const int width = tail ? C::kTail : 64;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int hw = width - 32 * h < 32 ? width - 32 * h : 32;
             if (hw <= 0) break;
             const int hcol = col + 32 * h;
-            if constexpr (kHasC) {
-              if (row_ok) {
-                const float* crow = cbase + d_row * p.N + n0 + hcol;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  if (4 * q < hw && n0 + hcol + 4 * q < p.N) {
-                    const uint4 cv = ld_cg_v4(crow + 4 * q);
-                    f[32 * h + 4 * q + 0] = __uint_as_float(cv.x) + f[32 * h + 4 * q + 0];
-                    f[32 * h + 4 * q + 1] = __uint_as_float(cv.y) + f[32 * h + 4 * q + 1];
-                    f[32 * h + 4 * q + 2] = __uint_as_float(cv.z) + f[32 * h + 4 * q + 2];
-                    f[32 * h + 4 * q + 3] = __uint_as_float(cv.w) + f[32 * h + 4 * q + 3];
-                  }
-                }
-              }
-            }
             if (lane == 0) bulk_wait_group_read<0>();
             __syncwarp();
+            if constexpr (kHasC) {
+              // C arrives by TMA in the swizzled layout, each lane adds its row; the output
+              // may use another layout: sync in between
+              if (ch != 0 || h != 0) {
+                issue_c_box(n0 + hcol);
+                wait_c_box();
+              }
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                if (n0 + hcol + 4 * q < p.N) {   // (past N nothing is stored)
+                  const uint4 cv = ld_shared_v4(smem_addr(sbuf) + lane * 128 + ((q ^ (lane & 7)) * 16));
+                  f[32 * h + 4 * q + 0] = __uint_as_float(cv.x) + f[32 * h + 4 * q + 0];
+                  f[32 * h + 4 * q + 1] = __uint_as_float(cv.y) + f[32 * h + 4 * q + 1];
+                  f[32 * h + 4 * q + 2] = __uint_as_float(cv.z) + f[32 * h + 4 * q + 2];
+                  f[32 * h + 4 * q + 3] = __uint_as_float(cv.w) + f[32 * h + 4 * q + 3];
+                }
+              }
+              __syncwarp();
+            }
             const bool narrow = hw < 32;
             const uint32_t srow = smem_addr(sbuf) + lane * (narrow ? 64 : 128);
 #pragma unroll
@@ -482,26 +510,30 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
           }
           continue;
         }
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
         if constexpr (kHasC) {
-          if (row_ok) {
-            const __nv_bfloat16* crow = p.c + d_row * p.N + n0 + col;
+          // C arrives by TMA (a full 64-column box, also for the narrow last chunk), each lane
+          // adds its row; the narrow chunk's output layout differs: sync before it is written
+          if (ch != 0) {
+            issue_c_box(n0 + col);
+            wait_c_box();
+          }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              if (q < units && n0 + col + 8 * q < p.N) {
-                const uint4 cv = ld_cg_v4(crow + 8 * q);
-                const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+          for (int q = 0; q < 8; ++q) {
+            if (q < units && n0 + col + 8 * q < p.N) {   // (past the tile or N nothing is stored)
+              const uint4 cv = ld_shared_v4(smem_addr(sbuf) + lane * 128 + ((q ^ (lane & 7)) * 16));
+              const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cw[e]));
-                  f[8 * q + 2 * e] = cf.x + f[8 * q + 2 * e];
-                  f[8 * q + 2 * e + 1] = cf.y + f[8 * q + 2 * e + 1];
-                }
+              for (int e = 0; e < 4; ++e) {
+                const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cw[e]));
+                f[8 * q + 2 * e] = cf.x + f[8 * q + 2 * e];
+                f[8 * q + 2 * e + 1] = cf.y + f[8 * q + 2 * e + 1];
               }
             }
           }
+          __syncwarp();
         }
-        if (lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
         // staging: 64-column chunks in the 128-byte-swizzled layout of tm_d; the narrower
         // last chunk as plain rows of kTail * 2 bytes (tm_d_tail, no swizzle)
         const uint32_t srow = smem_addr(sbuf) + lane * (tail ? C::kTail * 2 : 128);

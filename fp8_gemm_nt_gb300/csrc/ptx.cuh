@@ -298,14 +298,13 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p)
-               : "memory");
+               : "l"(p));
   return v;
 }
 
 __device__ __forceinline__ int ld_cg_s32(const int* p) {
   int v;
-  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 

@@ -201,6 +201,25 @@ def test_masked_parity_and_mask(lib, masked_m, max_m, N, K):
     assert_parity(bf16_f64(d)[valid], ref[valid], f"masked {masked_m}")
 
 
+def test_masked_many_groups_beyond_count_cache(lib):
+    # more groups than the kernel caches in shared memory (1024): the counts past the cache
+    # are read from global memory; a few non-empty groups on both sides of the boundary
+    G, max_m, N, K = 1100, 16, 32, 128
+    masked_m = np.zeros(G, np.int32)
+    masked_m[[0, 5, 1023, 1024, 1060, 1099]] = [3, 16, 1, 7, 16, 2]
+    p = W.make_masked(G=G, max_m=max_m, N=N, K=K, seed=77, masked_m=masked_m)
+    d = run_masked(lib, p)
+    groups = [0, 5, 1023, 1024, 1060, 1099, 1, 1050]
+    ref, valid = O.m_grouped_fp8_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, p.masked_m, p.G, p.max_m, p.N, p.K,
+                                                groups=groups)
+    got = bf16_f64(d)[groups]
+    assert (bf16_bits(d)[groups][~valid] == SENTINEL).all()
+    assert_parity(got[valid], ref[valid], "masked, 1100 groups")
+    untouched = np.ones(G, bool)
+    untouched[[0, 5, 1023, 1024, 1060, 1099]] = False
+    assert (bf16_bits(d)[untouched] == SENTINEL).all()
+
+
 def test_masked_count_above_max_is_clamped(lib):
     p = W.make_masked(G=2, max_m=64, N=64, K=128, seed=3, masked_m=[100, 10])
     d = run_masked(lib, p)
