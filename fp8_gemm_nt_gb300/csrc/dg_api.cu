@@ -565,6 +565,14 @@ bool map_out_f32(CUtensorMap* m, void* base, int rows, int N) {
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// FP32 output D (and C) of the K-grouped form, [G][rows][N]: 32 x 32 boxes, 128-byte swizzle.
+bool map_out_f32_3d(CUtensorMap* m, void* base, int G, int rows, int N) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(rows), static_cast<uint64_t>(G)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(N) * 4, static_cast<uint64_t>(N) * rows * 4};
+  const uint32_t box[3] = {32, 32, 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // FP4 operand ([(G,) rows, K/2] bytes of packed E2M1): 128-element x box_rows boxes of the
 // 16U4_ALIGN16B type (each 8 bytes land in a 16-byte shared-memory chunk), 128-byte swizzle.
 // The base must be 32-byte aligned and K/2 a multiple of 32 bytes.
@@ -603,11 +611,13 @@ bool map_sf_fp4(CUtensorMap* m, const int32_t* base, int G, int N, int KG, int b
 template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false, bool kBF4 = false>
 dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d,
                    dg::Params p, int clusters, cudaStream_t stream) {
-  const int KP = ceil_div(p.K / 128, 4);
+  constexpr bool kKG = kKind == dg::Kind::KGrouped;
+  // scale word rows: K-quads, or (K-grouped) the per-expert packed rows of all experts
+  const int KP = kKG ? p.sf_k_rows : ceil_div(p.K / 128, 4);
   const int num_mb = ceil_div(p.M, 128);
   const int NB = ceil_div(p.N, 128);
   const int sfb_rows = 2 * ceil_div(p.N, kBN);     // two chunks per tile
-  const int G = kKind == dg::Kind::Dense ? 1 : p.G;
+  const int G = (kKind == dg::Kind::Dense || kKG) ? 1 : p.G;   // groups of B (and its scales)
   const int b_kp = kBF4 ? p.K / 128 : KP;           // B chunk rows per K-group (FP4) or per K-quad
   const size_t sfa_words = static_cast<size_t>(KP) * num_mb * 128;
   const size_t sfb_words = static_cast<size_t>(G) * b_kp * sfb_rows * 128;
@@ -667,11 +677,14 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   }
 
   CUtensorMap ta, tb, tsa, tsb, td, td_tail, tc;
-  bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) && (kOutF32 ? map_out_f32(&td, d, p.M, p.N) : map_out(&td, d, 0, p.M, p.N));
+  bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) &&
+            (kKG ? map_out_f32_3d(&td, d, p.G, p.M, p.N)
+                 : kOutF32 ? map_out_f32(&td, d, p.M, p.N) : map_out(&td, d, 0, p.M, p.N));
   // C is read by TMA in boxes of the output's geometry (the map of D over C's memory)
   void* c_mem = const_cast<void*>(static_cast<const void*>(p.c));
   if (kHasC)
-    ok = ok && (kOutF32 ? map_out_f32(&tc, c_mem, p.M, p.N) : map_out(&tc, c_mem, 0, p.M, p.N));
+    ok = ok && (kKG ? map_out_f32_3d(&tc, c_mem, p.G, p.M, p.N)
+                    : kOutF32 ? map_out_f32(&tc, c_mem, p.M, p.N) : map_out(&tc, c_mem, 0, p.M, p.N));
   else
     tc = td;
   if constexpr (kBN % 64 != 0) {
@@ -689,7 +702,7 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   // each CTA of the pair loads BN/2 rows of the B tile
   if (kBF4)
     ok = ok && map_operand_fp4(&tb, b, kKind == dg::Kind::Dense ? 0 : G, p.N, p.K, kBN / 2);
-  else if (kKind == dg::Kind::Dense)
+  else if (kKind == dg::Kind::Dense || kKG)
     ok = ok && map_operand_2d(&tb, b, p.N, p.K, kBN / 2);
   else
     ok = ok && map_operand_3d(&tb, b, G, p.N, p.K, kBN / 2);
@@ -740,33 +753,37 @@ dg_status try_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
                    const void* c, void* d, dg::Params pp, long long pair_rows, int sms, cudaStream_t stream,
                    bool* launched) {
   *launched = false;
-  if constexpr (kKind != dg::Kind::Dense) {
-    if (c) return DG_ERR_INVALID_ARG;   // only the dense form takes C
+  // C: the dense and K-grouped forms
+  constexpr bool kTakesC = kKind == dg::Kind::Dense || kKind == dg::Kind::KGrouped;
+  if constexpr (!kTakesC) {
+    if (c) return DG_ERR_INVALID_ARG;
   }
   constexpr bool kDense = kKind == dg::Kind::Dense;
   constexpr int kWideBN = kDense ? 240 : 192;     // the 240-wide configuration is dense-only
-  const bool with_c = kDense && c != nullptr;
-  const int max_cl = std::min({with_c ? PairLauncher<kKind, kDense, 256, kOutF32, kBF4>::max_clusters()
+  const bool with_c = kTakesC && c != nullptr;
+  const int max_cl = std::min({with_c ? PairLauncher<kKind, kTakesC, 256, kOutF32, kBF4>::max_clusters()
                                       : PairLauncher<kKind, false, 256, kOutF32, kBF4>::max_clusters(),
-                               with_c ? PairLauncher<kKind, kDense, 192, kOutF32, kBF4>::max_clusters()
+                               with_c ? PairLauncher<kKind, kTakesC, 192, kOutF32, kBF4>::max_clusters()
                                       : PairLauncher<kKind, false, 192, kOutF32, kBF4>::max_clusters(),
-                               with_c ? PairLauncher<kKind, kDense, kWideBN, kOutF32, kBF4>::max_clusters()
+                               with_c ? PairLauncher<kKind, kTakesC, kWideBN, kOutF32, kBF4>::max_clusters()
                                       : PairLauncher<kKind, false, kWideBN, kOutF32, kBF4>::max_clusters()});
   if (max_cl <= 0) return DG_OK;
   const int cl_cap = std::min(max_cl, sms / 2);
-  const int bn = pick_pair_bn(pair_rows, pp.N, pp.K, cl_cap, kDense);
+  // K-grouped: a tile spans one expert's K slice (their mean stands for the makespan estimate)
+  const int k_tile = kKind == dg::Kind::KGrouped ? 128 * std::max(1, pp.K / 128 / std::max(pp.G, 1)) : pp.K;
+  const int bn = pick_pair_bn(pair_rows, pp.N, k_tile, cl_cap, kDense);
   const long long pair_tiles = pair_rows * ceil_div(pp.N, bn);
   const int clusters = static_cast<int>(std::min<long long>(cl_cap, pair_tiles));
   *launched = true;
   if (bn == 240) {
-    if (with_c) return run_pair<kKind, kDense, kWideBN, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    if (with_c) return run_pair<kKind, kTakesC, kWideBN, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
     return run_pair<kKind, false, kWideBN, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
   }
   if (bn == 256) {
-    if (with_c) return run_pair<kKind, kDense, 256, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+    if (with_c) return run_pair<kKind, kTakesC, 256, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
     return run_pair<kKind, false, 256, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
   }
-  if (with_c) return run_pair<kKind, kDense, 192, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
+  if (with_c) return run_pair<kKind, kTakesC, 192, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
   return run_pair<kKind, false, 192, kOutF32, kBF4>(ds, a, sfa, b, sfb, d, pp, clusters, stream);
 }
 
@@ -1062,6 +1079,29 @@ dg_status k_grouped_entry(const void* a, const int32_t* sfa, const void* b,
     return e == cudaSuccess ? DG_OK : cuda_fail(e);
   }
   const int sms = sms_to_use(*ds);
+  if constexpr (!kMN) {
+    // CTA pairs when the tiles fill the GPU (K-major operands only)
+    const long long tiles128 = static_cast<long long>(G) * ceil_div(M, 128) * ceil_div(N, 128);
+    if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
+      dg::Params pp{};
+      pp.M = M;
+      pp.N = N;
+      pp.K = K_total;
+      pp.G = G;
+      pp.c = reinterpret_cast<const __nv_bfloat16*>(c);   // FP32 in this form
+      pp.d = reinterpret_cast<__nv_bfloat16*>(d);
+      pp.ks = ks;
+      pp.sf_k_rows = sf_k_rows;
+      pp.status = ds->status;
+      pp.timeout_ns = wait_timeout_ns();
+      pp.fault = g_fault.load();
+      bool launched = false;
+      const dg_status s = try_pair<dg::Kind::KGrouped, true>(*ds, a, sfa, b, sfb, c, d, pp,
+                                                             static_cast<long long>(G) * ceil_div(M, 256), sms,
+                                                             stream, &launched);
+      if (launched) return s;
+    }
+  }
   int BN = std::getenv("DG_FORCE_BN") || N <= 128 ? pick_bn(dg::Kind::Dense, N) : 192;
   if (kMN && BN == 192) BN = 256;   // an N-major B tile is whole 128-column atoms
   CUtensorMap ta, tb, tsa, tsb, td;

@@ -89,34 +89,82 @@ struct PairConfig {
 // that CTA's rows are computed and discarded). The contiguous pair rows are listed once per
 // call by sf_to_utccp_kernel (first block, expert and own-block count per pair row, and
 // their number), so a tile costs one small load.
+// K-grouped form: tiles are (expert, pair row, n); every role visits the experts in increasing
+// order and carries the running K-group and scale-row offsets of the current one.
 template <Kind kKind, int kBN>
 struct PairScheduler {
   int num_n, total;
   int t, step;
+  int pairs_per_g, g_cur, kbase_cur, sfrow_cur;   // K-grouped walk
 
   __device__ __forceinline__ PairScheduler(const Params& p, int cluster, int clusters) {
     num_n = ceil_div_c(p.N, kBN);
     t = cluster;
     step = clusters;
+    pairs_per_g = ceil_div_c(ceil_div_c(p.M, BLOCK_M), 2);
+    g_cur = kbase_cur = sfrow_cur = 0;
     if constexpr (kKind == Kind::Contiguous) {
       total = ld_cg_s32(p.pair_count) * num_n;
+    } else if constexpr (kKind == Kind::KGrouped) {
+      total = p.G * pairs_per_g * num_n;
+      if (blockIdx.x == 0 && threadIdx.x == 0) {
+        // every slice a non-negative multiple of 128, the slices covering K, the scale rows
+        // matching the per-expert packing; otherwise the layout is violated (reported)
+        long long kg_sum = 0, rows = 0;
+        bool bad = false;
+        for (int g = 0; g < p.G; ++g) {
+          const int k = ld_cg_s32(p.ks + g);
+          if (k < 0 || k % BLOCK_K != 0) bad = true;
+          if (k > 0) {
+            kg_sum += k / BLOCK_K;
+            rows += (k + 4 * BLOCK_K - 1) / (4 * BLOCK_K);
+          }
+        }
+        if (bad || kg_sum != p.K / BLOCK_K || rows != p.sf_k_rows) atomicOr(p.status, kStatusBadIndexBit);
+      }
     } else {
-      total = ceil_div_c(ceil_div_c(p.M, BLOCK_M), 2) * num_n;
+      total = pairs_per_g * num_n;
     }
   }
 
   // seg.m_blk is the pair's first block; the CTA of rank r works on block m_blk + r.
   __device__ __forceinline__ bool next(const Params& p, Segment& s) {
     if (t >= total) return false;
-    const int pair = t / num_n;
-    s.n_blk = t % num_n;
-    t += step;
+    s.k_base = 0;
+    s.sf_row = 0;
     s.kb_begin = 0;
     s.kb_end = p.K / BLOCK_K;
     s.n_contrib = 1;
     s.slot = 0;
-    s.tile = pair;
     s.valid_m = p.M;
+    if constexpr (kKind == Kind::KGrouped) {
+      const int cur = t;
+      t += step;
+      const int tpg = pairs_per_g * num_n;
+      const int g = cur / tpg;
+      while (g_cur < g) {
+        const int k = ld_cg_s32(p.ks + g_cur);
+        if (k > 0) {
+          kbase_cur += k / BLOCK_K;
+          sfrow_cur += (k + 4 * BLOCK_K - 1) / (4 * BLOCK_K);
+        }
+        ++g_cur;
+      }
+      const int local = cur - g * tpg;
+      const int k = ld_cg_s32(p.ks + g);
+      s.g = g;
+      s.m_blk = 2 * (local / num_n);
+      s.n_blk = local % num_n;
+      s.tile = cur;
+      s.kb_end = k > 0 ? k / BLOCK_K : 0;   // 0: an expert without tokens (D = C)
+      s.k_base = kbase_cur;
+      s.sf_row = sfrow_cur;
+      return true;
+    }
+    const int pair = t / num_n;
+    s.n_blk = t % num_n;
+    t += step;
+    s.tile = pair;
     if constexpr (kKind == Kind::Contiguous) {
       s.m_blk = ld_cg_s32(p.pair_list + 3 * pair);
       s.g = ld_cg_s32(p.pair_list + 3 * pair + 1);
@@ -138,7 +186,8 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
                          const __grid_constant__ CUtensorMap tm_c, const Params p) {
   static_assert(kKind != Kind::Masked, "the masked form uses the single-CTA kernel");
   static_assert(kKind == Kind::Dense || kBN % 64 == 0, "narrow last chunks: dense form only");
-  static_assert(!kOutF32 || kKind == Kind::Dense, "FP32 output: dense form only");
+  static_assert(!kOutF32 || kKind == Kind::Dense || kKind == Kind::KGrouped, "FP32 output: dense and K-grouped");
+  static_assert(kKind != Kind::KGrouped || (kOutF32 && !kBF4), "the K-grouped form: FP8 operands, FP32 output");
   static_assert(!kBF4 || !kOutF32, "FP4 B: BF16 output");
   using C = PairConfig<kStages, kBN, kNumAccum, kBF4>;
   extern __shared__ uint8_t smem_raw[];
@@ -216,7 +265,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
       while (sched.next(p, seg)) {
         const int m_blk = seg.m_blk + static_cast<int>(rank);
         const int n0 = seg.n_blk * C::BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < seg.kb_end; ++kb) {
           if (*abort_flag || !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns)) {
             on_timeout();
             goto producer_done;
@@ -227,18 +276,19 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
           uint8_t* sa = smem + C::OFF_A + stage * C::A_BYTES;
           uint8_t* sb = smem + C::OFF_B + stage * C::B_BYTES;
           uint8_t* ssf = smem + C::OFF_SF + stage * C::SF_STRIDE;
-          tma_load_2d_pair(sa, &tm_a, fb, kb * BLOCK_K, m_blk * BLOCK_M);
-          if constexpr (kKind == Kind::Dense) {
-            tma_load_2d_pair(sb, &tm_b, fb, kb * BLOCK_K, n0 + static_cast<int>(rank) * (C::BN / 2));
+          tma_load_2d_pair(sa, &tm_a, fb, (seg.k_base + kb) * BLOCK_K, m_blk * BLOCK_M);
+          if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
+            tma_load_2d_pair(sb, &tm_b, fb, (seg.k_base + kb) * BLOCK_K, n0 + static_cast<int>(rank) * (C::BN / 2));
           } else {
             tma_load_3d_pair(sb, &tm_b, fb, kb * BLOCK_K, n0 + static_cast<int>(rank) * (C::BN / 2), seg.g);
           }
           if (with_sf) {
-            const int q = kb / 4;
+            const int q = seg.sf_row + kb / 4;
             // SFA chunk row: (q, m_blk); SFB chunk rows: (g, q, n-block) and the next one, or
-            // with FP4 B (g, kb, n-block): one pair of chunks per K-group
+            // with FP4 B (g, kb, n-block): one pair of chunks per K-group; the K-grouped form's
+            // word rows q run over all experts (B is not grouped)
             tma_load_2d_pair(ssf, &tm_sfa, fb, 0, q * p.sf_num_mb + m_blk);
-            const int b_row = kBF4 ? seg.g * num_kb + kb : seg.g * KP + q;
+            const int b_row = kBF4 ? seg.g * num_kb + kb : (kKind == Kind::KGrouped ? q : seg.g * KP + q);
             tma_load_2d_pair(ssf + C::SFA_BYTES, &tm_sfb, fb, 0, b_row * p.sf_nb + 2 * seg.n_blk);
           }
           ++issued;
@@ -276,7 +326,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
         {
           const uint32_t d_tmem = tmem_base + acc * C::ACC_STRIDE;
           uint32_t sfa_tmem = 0, sfb_tmem = 0;
-          for (int kb = 0; kb < num_kb; ++kb) {
+          for (int kb = 0; kb < seg.kb_end; ++kb) {
             if (!mbar_wait(&ready_bar[stage], phase, p.timeout_ns)) {
               on_timeout();
               goto mma_done;
@@ -324,7 +374,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
       const uint64_t sf_desc0 = make_smem_desc(smem_addr(smem + C::OFF_SF), 0, 128, kLayoutNone);
       uint32_t stage = 0, phase = 0, sf_iter = 0;
       while (sched.next(p, seg)) {
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < seg.kb_end; ++kb) {
           if (*abort_flag || !mbar_wait(&full_bar[stage], phase, p.timeout_ns)) {
             on_timeout();
             goto ready_done;
@@ -375,7 +425,12 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
     auto issue_c_box = [&](int x) {
       if (lane == 0) {
         mbar_arrive_expect_tx(&c_bar[ew], 32 * 128);
-        tma_load_2d(sbuf, &tm_c, &c_bar[ew], x, (seg.m_blk + static_cast<int>(rank)) * BLOCK_M + quad * 32);
+        const int y = (seg.m_blk + static_cast<int>(rank)) * BLOCK_M + quad * 32;
+        if constexpr (kKind == Kind::KGrouped) {
+          tma_load_3d(sbuf, &tm_c, &c_bar[ew], x, y, seg.g);
+        } else {
+          tma_load_2d(sbuf, &tm_c, &c_bar[ew], x, y);
+        }
       }
     };
     auto wait_c_box = [&]() {
@@ -405,9 +460,14 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
       // handed back after the last chunk is loaded.
       constexpr int kHeld = kNumAccum == 1 ? kCols : 64;
       uint32_t v[kHeld];
+      // an expert of the K-grouped form without tokens had no MMAs: its accumulator is zero
+      const bool empty = kKind == Kind::KGrouped && seg.kb_end == 0;
       auto load_chunk = [&](int ch, uint32_t* dst) {
         const int col = col0 + 64 * ch;
-        if (C::kTail == 0 || col + 64 <= C::BN) {
+        if (empty) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) dst[i] = 0u;
+        } else if (C::kTail == 0 || col + 64 <= C::BN) {
           tmem_load_32x32b_x32(taddr + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(dst));
           tmem_load_32x32b_x32(taddr + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(dst + 32));
         } else {
@@ -430,7 +490,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
       const int m_blk = seg.m_blk + static_cast<int>(rank);
       const int row = m_blk * BLOCK_M + quad * 32 + static_cast<int>(lane);
       bool row_ok;
-      if constexpr (kKind == Kind::Dense) {
+      if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
         row_ok = row < p.M;
       } else {
         const int gi = row < p.M ? ld_cg_s32(p.m_indices + row) : -1;
@@ -504,7 +564,11 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(narrow ? &tm_d_tail : &tm_d, sbuf, n0 + hcol, m_blk * BLOCK_M + quad * 32);
+              if constexpr (kKind == Kind::KGrouped) {
+                tma_store_3d(&tm_d, sbuf, n0 + hcol, m_blk * BLOCK_M + quad * 32, seg.g);
+              } else {
+                tma_store_2d(narrow ? &tm_d_tail : &tm_d, sbuf, n0 + hcol, m_blk * BLOCK_M + quad * 32);
+              }
               bulk_commit_group();
             }
           }

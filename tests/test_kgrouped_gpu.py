@@ -101,3 +101,57 @@ def test_k_grouped_bad_slices_reported(lib, bad_ks):
     run_k_grouped(lib, p)
     assert lib.dg_get_device_status() == 6
     assert lib.dg_get_device_status() == 0
+
+
+# --------------------------------------------------------------------------------------
+# CTA-pair kernel (with 8 SMs in use, small problems have enough tiles to take it)
+# --------------------------------------------------------------------------------------
+
+@pytest.fixture
+def few_sms(lib):
+    lib.dg_set_num_sms(8)
+    yield
+    lib.dg_set_num_sms(0)
+
+
+@pytest.mark.parametrize("bn", ["256", "192"])
+@pytest.mark.parametrize("ks,M,N,with_c", [
+    ([256, 0, 384], 256, 384, True),
+    ([128, 512, 0, 640], 300, 272, False),    # ragged M (an odd number of 128-row blocks) and N, an empty expert
+    ([1152], 384, 256, True),                 # one expert, K-groups not a multiple of 4
+    ([384, 128, 256], 512, 512, True),
+])
+def test_k_grouped_pair(lib, few_sms, monkeypatch, bn, ks, M, N, with_c):
+    monkeypatch.setenv("DG_PAIR_BN", bn)
+    p = W.make_k_grouped(G=len(ks), M=M, N=N, tokens=0, seed=700 + M + N, with_c=with_c, ks=np.array(ks))
+    d = run_k_grouped(lib, p).cpu().numpy().astype(np.float64)
+    ref = _ref(p)
+    for g in range(p.G):
+        rep = assert_parity(d[g], ref[g], f"pair expert {g} ks={ks}")
+        assert rep["max_err"] <= 1e-5 * max(rep["rms"], 1e-30), rep
+    assert lib.dg_get_device_status() == 0
+
+
+def test_k_grouped_pair_in_place_with_empty_expert(lib, few_sms):
+    p = W.make_k_grouped(G=3, M=384, N=512, tokens=0, seed=17, with_c=True, ks=np.array([256, 0, 640]))
+    c0 = p.c.astype(np.float64)
+    d = dev(p.c)
+    args = (dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb))
+    ks = dev(np.asarray(p.ks, np.int32))
+    for _ in range(2):
+        lib.dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(*args, d, d, ks)
+    torch.cuda.synchronize()
+    prod = O.k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(p.a, p.sfa, p.b, p.sfb, None, p.ks, p.M, p.N)
+    got = d.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got[1], c0[1])          # the empty expert keeps its addend exactly
+    for g in (0, 2):
+        assert_parity(got[g], c0[g] + 2.0 * prod[g], f"pair in place, expert {g}")
+    assert lib.dg_get_device_status() == 0
+
+
+def test_k_grouped_pair_bad_slices_reported(lib, few_sms):
+    p = W.make_k_grouped(G=2, M=256, N=512, tokens=0, seed=18, with_c=False, ks=np.array([256, 256]))
+    p.ks = np.array([256, 200], np.int32)
+    run_k_grouped(lib, p)
+    assert lib.dg_get_device_status() == 6
+    assert lib.dg_get_device_status() == 0
