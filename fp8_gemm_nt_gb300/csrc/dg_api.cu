@@ -407,12 +407,13 @@ constexpr int kEpilogueWarps = 4;
 // with one accumulator, BN = 240 or 192 with two.
 constexpr int kPairStages = 5;
 
-template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false, bool kBF4 = false>
+template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false, bool kBF4 = false, bool kAMN = false,
+          bool kBMN = false>
 struct PairLauncher {
   static constexpr int kNumAccum = kBN == 256 ? 1 : 2;
   using Cfg = dg::PairConfig<kPairStages, kBN, kNumAccum, kBF4>;
   static constexpr auto kernel() {
-    return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kBN, kNumAccum, kHasC, kOutF32, kBF4>;
+    return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kBN, kNumAccum, kHasC, kOutF32, kBF4, kAMN, kBMN>;
   }
 
   // Largest number of co-resident CTA pairs (0 if the device cannot run the kernel).
@@ -608,7 +609,8 @@ bool map_sf_fp4(CUtensorMap* m, const int32_t* base, int G, int N, int KG, int b
 
 // Dense / contiguous GEMM on CTA pairs: converts the scale words into tcgen05.cp chunks in
 // the stream workspace (two small kernels), then launches the pair kernel.
-template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false, bool kBF4 = false>
+template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false, bool kBF4 = false, bool kAMN = false,
+          bool kBMN = false>
 dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d,
                    dg::Params p, int clusters, cudaStream_t stream) {
   constexpr bool kKG = kKind == dg::Kind::KGrouped;
@@ -677,7 +679,7 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   }
 
   CUtensorMap ta, tb, tsa, tsb, td, td_tail, tc;
-  bool ok = map_operand_2d(&ta, a, p.M, p.K, 128) &&
+  bool ok = (kAMN ? map_operand_mn(&ta, a, p.M, p.K) : map_operand_2d(&ta, a, p.M, p.K, 128)) &&
             (kKG ? map_out_f32_3d(&td, d, p.G, p.M, p.N)
                  : kOutF32 ? map_out_f32(&td, d, p.M, p.N) : map_out(&td, d, 0, p.M, p.N));
   // C is read by TMA in boxes of the output's geometry (the map of D over C's memory)
@@ -700,7 +702,9 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
     td_tail = td;
   }
   // each CTA of the pair loads BN/2 rows of the B tile
-  if (kBF4)
+  if (kBMN)
+    ok = ok && map_operand_mn(&tb, b, p.N, p.K);   // 128-column boxes: one per CTA at width 256
+  else if (kBF4)
     ok = ok && map_operand_fp4(&tb, b, kKind == dg::Kind::Dense ? 0 : G, p.N, p.K, kBN / 2);
   else if (kKind == dg::Kind::Dense || kKG)
     ok = ok && map_operand_2d(&tb, b, p.N, p.K, kBN / 2);
@@ -717,7 +721,8 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   if (!ok) return DG_ERR_CUDA;
   p.sf_num_mb = num_mb;
   p.sf_nb = sfb_rows;
-  return PairLauncher<kKind, kHasC, kBN, kOutF32, kBF4>::launch(ta, tb, tsa, tsb, td, td_tail, tc, p, clusters, stream);
+  return PairLauncher<kKind, kHasC, kBN, kOutF32, kBF4, kAMN, kBMN>::launch(ta, tb, tsa, tsb, td, td_tail, tc, p,
+                                                                               clusters, stream);
 }
 
 // Pair tile width: DG_PAIR_BN (192, 240 or 256) overrides; 240 is offered for the dense
@@ -989,6 +994,30 @@ dg_status dense_layout_entry(const void* a, const int32_t* sfa, const void* b, c
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
   const int sms = sms_to_use(*ds);
   const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
+  if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
+    // CTA pairs, 256-wide tiles (each CTA's half of an N-major B tile is one 128-column atom)
+    const int max_cl = c ? PairLauncher<dg::Kind::Dense, true, 256, false, false, kAMN, kBMN>::max_clusters()
+                         : PairLauncher<dg::Kind::Dense, false, 256, false, false, kAMN, kBMN>::max_clusters();
+    if (max_cl > 0) {
+      dg::Params pp{};
+      pp.M = M;
+      pp.N = N;
+      pp.K = K;
+      pp.G = 1;
+      pp.c = static_cast<const __nv_bfloat16*>(c);
+      pp.d = static_cast<__nv_bfloat16*>(d);
+      pp.status = ds->status;
+      pp.timeout_ns = wait_timeout_ns();
+      pp.fault = g_fault.load();
+      const long long pair_tiles = static_cast<long long>(ceil_div(M, 256)) * ceil_div(N, 256);
+      const int clusters = static_cast<int>(std::min<long long>(std::min(max_cl, sms / 2), pair_tiles));
+      if (c)
+        return run_pair<dg::Kind::Dense, true, 256, false, false, kAMN, kBMN>(*ds, a, sfa, b, sfb, d, pp, clusters,
+                                                                                stream);
+      return run_pair<dg::Kind::Dense, false, 256, false, false, kAMN, kBMN>(*ds, a, sfa, b, sfb, d, pp, clusters,
+                                                                               stream);
+    }
+  }
   int BN = 128;
   if (tiles128 >= sms) {
     BN = ceil_div(N, 256) * 256 <= ceil_div(N, 128) * 128 ? 256 : 128;   // the wider unless it wastes columns

@@ -178,7 +178,12 @@ struct PairScheduler {
 };
 
 // kOutF32: FP32 C / D (the dense weight-gradient form), else BF16. kBF4: B in FP4.
-template <Kind kKind, int kStages, int kBN, int kNumAccum, bool kHasC, bool kOutF32 = false, bool kBF4 = false>
+// kAMN / kBMN (dense form, 256-wide tiles): A given as [K, M] / B given as [K, N]. Each CTA's
+// 128 rows of A and 128 columns of B are then one MN-major atom: a TMA box of 128 K-rows x 128
+// M/N-bytes (128-byte swizzle), described with LBO = 16 KB, SBO = 1024 and advanced 4 KB per
+// 32-deep K step, with the instruction descriptor's transpose bits set.
+template <Kind kKind, int kStages, int kBN, int kNumAccum, bool kHasC, bool kOutF32 = false, bool kBF4 = false,
+          bool kAMN = false, bool kBMN = false>
 __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
@@ -189,6 +194,8 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
   static_assert(!kOutF32 || kKind == Kind::Dense || kKind == Kind::KGrouped, "FP32 output: dense and K-grouped");
   static_assert(kKind != Kind::KGrouped || (kOutF32 && !kBF4), "the K-grouped form: FP8 operands, FP32 output");
   static_assert(!kBF4 || !kOutF32, "FP4 B: BF16 output");
+  static_assert((!kAMN && !kBMN) || (kKind == Kind::Dense && kBN == 256 && !kBF4),
+                "MN-major operands: the dense form with 256-wide tiles");
   using C = PairConfig<kStages, kBN, kNumAccum, kBF4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -276,8 +283,14 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
           uint8_t* sa = smem + C::OFF_A + stage * C::A_BYTES;
           uint8_t* sb = smem + C::OFF_B + stage * C::B_BYTES;
           uint8_t* ssf = smem + C::OFF_SF + stage * C::SF_STRIDE;
-          tma_load_2d_pair(sa, &tm_a, fb, (seg.k_base + kb) * BLOCK_K, m_blk * BLOCK_M);
-          if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
+          if constexpr (kAMN) {
+            tma_load_2d_pair(sa, &tm_a, fb, m_blk * BLOCK_M, kb * BLOCK_K);
+          } else {
+            tma_load_2d_pair(sa, &tm_a, fb, (seg.k_base + kb) * BLOCK_K, m_blk * BLOCK_M);
+          }
+          if constexpr (kBMN) {
+            tma_load_2d_pair(sb, &tm_b, fb, n0 + static_cast<int>(rank) * (C::BN / 2), kb * BLOCK_K);
+          } else if constexpr (kKind == Kind::Dense || kKind == Kind::KGrouped) {
             tma_load_2d_pair(sb, &tm_b, fb, (seg.k_base + kb) * BLOCK_K, n0 + static_cast<int>(rank) * (C::BN / 2));
           } else {
             tma_load_3d_pair(sb, &tm_b, fb, kb * BLOCK_K, n0 + static_cast<int>(rank) * (C::BN / 2), seg.g);
@@ -312,9 +325,16 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
     // One thread of the leader runs the whole loop (no warp-wide synchronisation per K-group).
     if (leader && lane == 0) {
       // B format field [10,13): 0 = E4M3, 5 = E2M1
-      constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(2 * BLOCK_M, C::BN) | (kBF4 ? 5u << 10 : 0u);
-      const uint64_t a_desc0 = make_smem_desc(smem_addr(smem + C::OFF_A), 16, 1024, kLayoutSwizzle128B);
-      const uint64_t b_desc0 = make_smem_desc(smem_addr(smem + C::OFF_B), 16, 1024, kLayoutSwizzle128B);
+      constexpr uint32_t kIdesc = make_idesc_mxf8_e4m3(2 * BLOCK_M, C::BN) | (kBF4 ? 5u << 10 : 0u) |
+                                  (kAMN ? 1u << 15 : 0u) | (kBMN ? 1u << 16 : 0u);
+      const uint64_t a_desc0 =
+          make_smem_desc(smem_addr(smem + C::OFF_A), kAMN ? 128 * BLOCK_K : 16, 1024, kLayoutSwizzle128B);
+      const uint64_t b_desc0 =
+          make_smem_desc(smem_addr(smem + C::OFF_B), kBMN ? 128 * BLOCK_K : 16, 1024, kLayoutSwizzle128B);
+      // descriptor steps (address >> 4) per 32-deep K step: 32 bytes along a K-major row, or
+      // 32 rows of 128 bytes down an MN-major box
+      constexpr uint64_t kAStep = kAMN ? (32 * 128) >> 4 : 2;
+      constexpr uint64_t kBStep = kBMN ? (32 * 128) >> 4 : 2;
       uint32_t stage = 0, phase = 0, tile_iter = 0, sf_iter = 0;
       while (sched.next(p, seg)) {
         const uint32_t acc = tile_iter % kNumAccum;
@@ -347,7 +367,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
             for (int k = 0; k < BLOCK_K / 32; ++k) {
               // B's scale byte: the K-group's (FP8) or the k-th 32-wide block's (FP4)
               const uint32_t idesc = idesc_with_sf_id(kIdesc, kb % 4, kBF4 ? k : kb % 4);
-              mma_mxf8_block_scale_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_tmem, sfb_tmem,
+              mma_mxf8_block_scale_pair(d_tmem, adesc + kAStep * k, bdesc + kBStep * k, idesc, sfa_tmem, sfb_tmem,
                                         (kb | k) != 0);
             }
             tc_commit_pair(&empty_bar[stage]);

@@ -151,3 +151,37 @@ def test_tn_k_grouped_parity(lib, monkeypatch, ks, M, N, with_c):
     torch.cuda.synchronize()
     monkeypatch.delenv("DG_FORCE_BN")
     assert torch.equal(d_nt, d)
+
+
+# --------------------------------------------------------------------------------------
+# CTA-pair kernel (256-wide tiles) with MN-major operands; 8 SMs in use so that small
+# problems have enough tiles to take it
+# --------------------------------------------------------------------------------------
+
+@pytest.fixture
+def few_sms(lib):
+    lib.dg_set_num_sms(8)
+    yield
+    lib.dg_set_num_sms(0)
+
+
+@pytest.mark.parametrize("layout", ["nn", "tn", "tt"])
+@pytest.mark.parametrize("M,N,K,with_c", [
+    (512, 512, 640, True),
+    (304, 400, 1152, True),     # ragged M (an odd number of 128-row blocks) and N, K-groups not a multiple of 4
+    (1024, 768, 2048, False),   # several pair tiles per CTA pair
+])
+def test_layout_pair_parity(lib, few_sms, layout, M, N, K, with_c):
+    p = W.make_dense(M, N, K, seed=1500 + M + N + K, with_c=with_c)
+    d = _run(lib, layout, p)
+    assert_parity(bf16_f64(d), _oracle(layout, p), f"pair {layout} {M}x{N}x{K}")
+
+
+def test_layout_pair_bit_identical_to_nt(lib, few_sms, monkeypatch):
+    # the four layouts on the 256-wide pair kernel: the same MMAs, only the tiles' shared-
+    # memory layout differs
+    monkeypatch.setenv("DG_PAIR_BN", "256")
+    p = W.make_dense(1024, 1024, 768, seed=1600, with_c=True)
+    ref = bf16_bits(_run(lib, "nt", p))
+    for layout in ("nn", "tn", "tt"):
+        assert np.array_equal(bf16_bits(_run(lib, layout, p)), ref), layout
