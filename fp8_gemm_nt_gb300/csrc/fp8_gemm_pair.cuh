@@ -63,9 +63,12 @@ struct PairConfig {
   static constexpr int OFF_SF = OFF_B + kStages * B_BYTES;
   static constexpr int OFF_EPI = ((OFF_SF + kStages * SF_STRIDE + 1023) / 1024) * 1024;
   static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_BUF_BYTES;
+  // TMEM scale buffers (4 SFA + 8 SFB columns each): two, or with FP4 B (a copy every stage)
+  // four where the columns allow, so that copies can run further ahead of the MMAs
+  static constexpr int kSfBufs = (kBF4 && kNumAccum * BN + 12 * 4 <= 512) ? 4 : 2;
   // full / empty / ready per stage, tfull / tempty per accumulator, MMA drain, copy drain,
   // one "scale buffer free" barrier per TMEM scale buffer, one "C landed" per epilogue warp
-  static constexpr int NUM_BARS = 3 * kStages + 2 * kNumAccum + 4 + kEpiWarps;
+  static constexpr int NUM_BARS = 3 * kStages + 2 * kNumAccum + 2 + kSfBufs + kEpiWarps;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
@@ -74,13 +77,14 @@ struct PairConfig {
   // TMEM: kNumAccum BN-column accumulators and 2 x 4 SFA / 2 x 8 SFB columns, packed when
   // they fit; otherwise (two 240-column accumulators) the accumulators start at columns 0
   // and 256 and the scale columns sit in the 16 columns after each
-  static constexpr bool kPacked = kNumAccum * BN + 24 <= 512;
+  static constexpr bool kPacked = kNumAccum * BN + 12 * kSfBufs <= 512;
   static constexpr int ACC_STRIDE = kPacked ? BN : 256;
   static constexpr int SFA_COL = kPacked ? kNumAccum * BN : BN;
-  static constexpr int SFB_COL = kPacked ? SFA_COL + 8 : 256 + BN;
+  static constexpr int SFB_COL = kPacked ? SFA_COL + 4 * kSfBufs : 256 + BN;
   static constexpr int TMEM_COLS = 512;
   static_assert(kPacked || (kNumAccum == 2 && BN + 8 <= 256 && 256 + BN + 16 <= TMEM_COLS), "TMEM layout");
-  static_assert(!kPacked || SFB_COL + 16 <= TMEM_COLS, "TMEM columns exceeded");
+  static_assert(!kPacked || SFB_COL + 8 * kSfBufs <= TMEM_COLS, "TMEM columns exceeded");
+  static_assert(kPacked || kSfBufs == 2, "unpacked TMEM layout: two scale buffers");
 };
 
 // Walks the pair tiles of the sequence t = cluster, += clusters. A pair row is two
@@ -208,8 +212,8 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
   uint64_t* drain_bar = tempty_bar + kNumAccum;
   uint64_t* ready_bar = drain_bar + 1;          // [kStages] leader: stage handed to the MMA thread
   uint64_t* sf_drain_bar = ready_bar + kStages;
-  uint64_t* sf_free_bar = sf_drain_bar + 1;     // [2] leader: MMAs reading TMEM scale buffer b completed
-  uint64_t* c_bar = sf_free_bar + 2;            // [kEpiWarps] this CTA: a C box landed in warp w's staging
+  uint64_t* sf_free_bar = sf_drain_bar + 1;     // [kSfBufs] leader: MMAs reading TMEM scale buffer b completed
+  uint64_t* c_bar = sf_free_bar + C::kSfBufs;   // [kEpiWarps] this CTA: a C box landed in warp w's staging
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -232,8 +236,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
     mbar_init(drain_bar, 1);
     for (int s = 0; s < kStages; ++s) mbar_init(&ready_bar[s], 1);
     mbar_init(sf_drain_bar, 1);
-    mbar_init(&sf_free_bar[0], 1);
-    mbar_init(&sf_free_bar[1], 1);
+    for (int b = 0; b < C::kSfBufs; ++b) mbar_init(&sf_free_bar[b], 1);
     for (int w = 0; w < C::kEpiWarps; ++w) mbar_init(&c_bar[w], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -353,10 +356,10 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
             }
             tc_fence_after();
             if (kBF4 || kb % 4 == 0) {
-              // the scales of this K-quad (K-group, FP4 B) are in TMEM buffer (sf_iter & 1); the other
-              // buffer's readers are all issued: it may be refilled once they complete
-              if (sf_iter > 0) tc_commit_pair(&sf_free_bar[(sf_iter - 1) & 1]);
-              const uint32_t buf = sf_iter & 1;
+              // the scales of this K-quad (K-group, FP4 B) are in TMEM buffer sf_iter % kSfBufs; the
+              // previous buffer's readers are all issued: it may be refilled once they complete
+              if (sf_iter > 0) tc_commit_pair(&sf_free_bar[(sf_iter - 1) % C::kSfBufs]);
+              const uint32_t buf = sf_iter % C::kSfBufs;
               ++sf_iter;
               sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
               sfb_tmem = tmem_base + C::SFB_COL + 8 * buf;
@@ -388,8 +391,8 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
   } else if (warp == C::kReadyWarp) {
     // ================================ stage hand-off (leader) =======================
     // Walks the stages in the MMA thread's order. A TMEM scale buffer is refilled only
-    // after the MMAs reading its previous contents completed (use k waits for phase k - 1
-    // of its free barrier; phase k needs this very copy, so the parity cannot alias).
+    // after the MMAs reading its previous contents completed (its use k waits for phase
+    // k - 1 of its free barrier; phase k needs this very copy, so the parity cannot alias).
     if (leader && lane == 0) {
       const uint64_t sf_desc0 = make_smem_desc(smem_addr(smem + C::OFF_SF), 0, 128, kLayoutNone);
       uint32_t stage = 0, phase = 0, sf_iter = 0;
@@ -400,12 +403,13 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
             goto ready_done;
           }
           if (kBF4 || kb % 4 == 0) {
-            if (sf_iter >= 2 && !mbar_wait(&sf_free_bar[sf_iter & 1], ((sf_iter >> 1) - 1) & 1, p.timeout_ns)) {
+            if (sf_iter >= C::kSfBufs &&
+                !mbar_wait(&sf_free_bar[sf_iter % C::kSfBufs], ((sf_iter / C::kSfBufs) - 1) & 1, p.timeout_ns)) {
               on_timeout();
               goto ready_done;
             }
             tc_fence_after();
-            const uint32_t buf = sf_iter & 1;
+            const uint32_t buf = sf_iter % C::kSfBufs;
             ++sf_iter;
             const uint32_t sfa_tmem = tmem_base + C::SFA_COL + 4 * buf;
             const uint32_t sfb_tmem = tmem_base + C::SFB_COL + 8 * buf;
