@@ -47,7 +47,7 @@ extern "C" {
 typedef enum {
   DG_OK = 0,
   DG_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, K % 128 != 0, N % 16 != 0, G <= 0 */
-  DG_ERR_UNSUPPORTED = 2,   /* device is not sm_103 / not supported by this build */
+  DG_ERR_UNSUPPORTED = 2,   /* device is not sm_103, or a size past the library's limits */
   DG_ERR_MISALIGNED = 3,    /* a base pointer is not 16-byte aligned */
   DG_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (see dg_last_cuda_error) */
   DG_ERR_TIMEOUT = 5,       /* device: a pipeline wait exceeded its time limit; the kernel exited */
