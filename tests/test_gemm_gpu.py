@@ -274,3 +274,46 @@ def test_masked_graph_replay_reads_counts_on_the_device(lib):
         bits = bf16_bits(d)
         assert (bits[~valid] == SENTINEL).all(), counts
         assert_parity(bf16_f64(d)[valid], ref[valid], f"graph replay {counts.tolist()}")
+
+
+# --------------------------------------------------------------------------------------
+# inputs written by the kernel right before the GEMM (the dispatch step of a MoE layer)
+# --------------------------------------------------------------------------------------
+
+def test_masked_counts_written_by_the_previous_kernel(lib):
+    # the counts come from a device kernel launched just before each GEMM on the same stream:
+    # every launch must read the new values (the kernels read their inputs at L2 after the
+    # dependency wait)
+    p = W.make_masked(G=8, max_m=256, N=512, K=512, seed=91, masked_m=[0] * 8)
+    a, sfa, b, sfb = dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb)
+    mm = torch.zeros(8, dtype=torch.int32, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    for it in range(6):
+        d = sentinel_like((p.G, p.max_m, p.N))
+        mm.copy_(torch.randint(0, p.max_m + 1, (p.G,), device="cuda", generator=gen, dtype=torch.int32))
+        lib.dg_m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, d, mm)
+        torch.cuda.synchronize()
+        counts = mm.cpu().numpy()
+        ref, valid = O.m_grouped_fp8_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, counts, p.G, p.max_m, p.N, p.K)
+        bits = bf16_bits(d)
+        assert (bits[~valid] == SENTINEL).all(), f"launch {it}: rows past the counts were written"
+        assert not (bits[valid] == SENTINEL).any(), f"launch {it}: counted rows were not written"
+        assert_parity(bf16_f64(d)[valid], ref[valid], f"launch {it}")
+
+
+def test_contiguous_indices_written_by_the_previous_kernel(lib):
+    # the row -> expert map is rewritten on the device before each launch (experts permuted)
+    q = W.make_contiguous(G=3, tokens=600, N=256, K=512, seed=92, counts=[250, 100, 250])
+    a, sfa, b, sfb = dev(q.a), dev(q.sfa), dev(q.b), dev(q.sfb)
+    idx = dev(q.m_indices)
+    base = torch.from_numpy(q.m_indices).cuda()
+    for it, perm in enumerate(([0, 1, 2], [2, 0, 1], [1, 2, 0])):
+        table = torch.tensor(perm + [-1], dtype=torch.int32, device="cuda")
+        idx.copy_(table[base.long()])          # -1 maps to table[-1] = -1
+        d = sentinel_like((q.M_total, q.N))
+        lib.dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, idx)
+        torch.cuda.synchronize()
+        m_idx = idx.cpu().numpy()
+        ref, valid = O.m_grouped_fp8_gemm_nt_contiguous(q.a, q.sfa, q.b, q.sfb, m_idx, q.M_total, q.N, q.K, q.G)
+        assert (bf16_bits(d)[~valid] == SENTINEL).all()
+        assert_parity(bf16_f64(d)[valid], ref[valid], f"permutation {perm}")
