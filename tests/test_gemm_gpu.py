@@ -250,6 +250,21 @@ def test_pack_sf_matches_layout(lib):
     assert np.array_equal(out2.cpu().numpy(), W.pack_sf(e2))
 
 
+def test_pack_sf_gives_the_fp4_scale_layout(lib):
+    # FP4 B's scales (one per row per 32 K) are packed by the same utility: FP32 scales
+    # [N, K/32] -> int32 [K/128, ceil4(N)], and a GEMM with them matches the oracle
+    p = W.make_dense_fp4(64, 208, 512, seed=21)
+    eb = O.unpack_sf(p.sfb, p.N, p.K // 32)
+    f = np.ldexp(np.ones(eb.shape, np.float32), eb.astype(np.int32) - 127).astype(np.float32)
+    packed = lib.dg_pack_sf_ue8m0(dev(f))
+    torch.cuda.synchronize()
+    assert np.array_equal(packed.cpu().numpy(), p.sfb)
+    d = sentinel_like((p.M, p.N))
+    lib.dg_fp8_fp4_gemm_nt(dev(p.a), dev(p.sfa), dev(p.b), packed, None, d)
+    torch.cuda.synchronize()
+    assert_parity(bf16_f64(d), O.fp8_fp4_gemm_nt(p.a, p.sfa, p.b, p.sfb, None, p.M, p.N, p.K), "packed FP4 scales")
+
+
 def test_masked_graph_replay_reads_counts_on_the_device(lib):
     # the masked form is captured once into a CUDA graph; replays pick up new per-expert
     # counts written to device memory (the CPU never learns them), as the pages intend for
