@@ -87,6 +87,23 @@ unsigned long long wait_timeout_ns() {
   return t ? t : kWaitTimeoutNs;
 }
 
+// The parameter block every launch shares: the problem shape, C and D (BF16, or FP32 for the
+// weight-gradient forms, which the kernels reinterpret), the device status word, the wait
+// limit and the failure-injection switch.
+dg::Params base_params(const DeviceState& ds, int M, int N, int K, int G, const void* c, void* d) {
+  dg::Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.G = G;
+  p.c = static_cast<const __nv_bfloat16*>(c);
+  p.d = static_cast<__nv_bfloat16*>(d);
+  p.status = ds.status;
+  p.timeout_ns = wait_timeout_ns();
+  p.fault = g_fault.load();
+  return p;
+}
+
 // Workspace of at least `bytes` for `stream`, zeroed when (re)allocated. The stream-K
 // arrival counters at its start are left at zero by every completed launch.
 dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, void** out) {
@@ -849,16 +866,7 @@ dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, 
       !map_sf(&tsa, sfa, 0, M, KP, 128) || (!kBF4 && !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8)) ||
       !(kOutF32 ? map_out_f32(&td, d, M, N) : map_out(&td, d, 0, M, N)))
     return DG_ERR_CUDA;
-  dg::Params p{};
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.G = 1;
-  p.c = static_cast<const __nv_bfloat16*>(c);
-  p.d = static_cast<__nv_bfloat16*>(d);
-  p.status = ds->status;
-  p.timeout_ns = wait_timeout_ns();
-  p.fault = g_fault.load();
+  dg::Params p = base_params(*ds, M, N, K, 1, c, d);
   const long long tiles = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, BN);
   int grid = static_cast<int>(tiles < sms ? tiles : sms);
   // Fewer tiles than SMs: share the K-groups of all tiles among all SMs (stream-K) so that
@@ -935,16 +943,7 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   const int BN = tiles128 < sms ? sk_bn : pick_bn(dg::Kind::Dense, N);
   if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
     {
-      dg::Params pp{};
-      pp.M = M;
-      pp.N = N;
-      pp.K = K;
-      pp.G = 1;
-      pp.c = static_cast<const __nv_bfloat16*>(c);
-      pp.d = static_cast<__nv_bfloat16*>(d);
-      pp.status = ds->status;
-      pp.timeout_ns = wait_timeout_ns();
-      pp.fault = g_fault.load();
+      dg::Params pp = base_params(*ds, M, N, K, 1, c, d);
       bool launched = false;
       const dg_status s = try_pair<dg::Kind::Dense>(*ds, a, sfa, b, sfb, c, d, pp, ceil_div(M, 256), sms, stream,
                                                     &launched);
@@ -957,16 +956,7 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
           !map_sf(&tsa, sfa, 0, M, KP, 128) || !map_sf(&tsb, sfb, 0, ceil_div(N, 128), KP, 8) ||
           !map_out(&td, d, 0, M, N))
         return DG_ERR_CUDA;
-      dg::Params p{};
-      p.M = M;
-      p.N = N;
-      p.K = K;
-      p.G = 1;
-      p.c = static_cast<const __nv_bfloat16*>(c);
-      p.d = static_cast<__nv_bfloat16*>(d);
-      p.status = ds->status;
-      p.timeout_ns = wait_timeout_ns();
-      p.fault = g_fault.load();
+      dg::Params p = base_params(*ds, M, N, K, 1, c, d);
       const int grid = static_cast<int>(static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, sbn)) * kSplitWays;
       if (c) return launch_split<true>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
       return launch_split<false>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
@@ -999,16 +989,7 @@ dg_status dense_layout_entry(const void* a, const int32_t* sfa, const void* b, c
     const int max_cl = c ? PairLauncher<dg::Kind::Dense, true, 256, false, false, kAMN, kBMN>::max_clusters()
                          : PairLauncher<dg::Kind::Dense, false, 256, false, false, kAMN, kBMN>::max_clusters();
     if (max_cl > 0) {
-      dg::Params pp{};
-      pp.M = M;
-      pp.N = N;
-      pp.K = K;
-      pp.G = 1;
-      pp.c = static_cast<const __nv_bfloat16*>(c);
-      pp.d = static_cast<__nv_bfloat16*>(d);
-      pp.status = ds->status;
-      pp.timeout_ns = wait_timeout_ns();
-      pp.fault = g_fault.load();
+      dg::Params pp = base_params(*ds, M, N, K, 1, c, d);
       const long long pair_tiles = static_cast<long long>(ceil_div(M, 256)) * ceil_div(N, 256);
       const int clusters = static_cast<int>(std::min<long long>(std::min(max_cl, sms / 2), pair_tiles));
       if (c)
@@ -1060,16 +1041,7 @@ dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const
   const int sms = sms_to_use(*ds);
   const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
   if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
-    dg::Params pp{};
-    pp.M = M;
-    pp.N = N;
-    pp.K = K;
-    pp.G = 1;
-    pp.c = reinterpret_cast<const __nv_bfloat16*>(c);   // FP32 in this form (the kernel reinterprets)
-    pp.d = reinterpret_cast<__nv_bfloat16*>(d);
-    pp.status = ds->status;
-    pp.timeout_ns = wait_timeout_ns();
-    pp.fault = g_fault.load();
+    dg::Params pp = base_params(*ds, M, N, K, 1, c, d);
     bool launched = false;
     const dg_status s = try_pair<dg::Kind::Dense, true>(*ds, a, sfa, b, sfb, c, d, pp, ceil_div(M, 256), sms, stream,
                                                         &launched);
@@ -1112,18 +1084,9 @@ dg_status k_grouped_entry(const void* a, const int32_t* sfa, const void* b,
     // CTA pairs when the tiles fill the GPU (K-major operands only)
     const long long tiles128 = static_cast<long long>(G) * ceil_div(M, 128) * ceil_div(N, 128);
     if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
-      dg::Params pp{};
-      pp.M = M;
-      pp.N = N;
-      pp.K = K_total;
-      pp.G = G;
-      pp.c = reinterpret_cast<const __nv_bfloat16*>(c);   // FP32 in this form
-      pp.d = reinterpret_cast<__nv_bfloat16*>(d);
+      dg::Params pp = base_params(*ds, M, N, K_total, G, c, d);
       pp.ks = ks;
       pp.sf_k_rows = sf_k_rows;
-      pp.status = ds->status;
-      pp.timeout_ns = wait_timeout_ns();
-      pp.fault = g_fault.load();
       bool launched = false;
       const dg_status s = try_pair<dg::Kind::KGrouped, true>(*ds, a, sfa, b, sfb, c, d, pp,
                                                              static_cast<long long>(G) * ceil_div(M, 256), sms,
@@ -1144,18 +1107,9 @@ dg_status k_grouped_entry(const void* a, const int32_t* sfa, const void* b,
     ok = ok && make_map(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return DG_ERR_CUDA;
-  dg::Params p{};
-  p.M = M;
-  p.N = N;
-  p.K = K_total;
-  p.G = G;
-  p.c = reinterpret_cast<const __nv_bfloat16*>(c);   // FP32 in this form (the kernel reinterprets)
-  p.d = reinterpret_cast<__nv_bfloat16*>(d);
+  dg::Params p = base_params(*ds, M, N, K_total, G, c, d);
   p.ks = ks;
   p.sf_k_rows = sf_k_rows;
-  p.status = ds->status;
-  p.timeout_ns = wait_timeout_ns();
-  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(G) * ceil_div(M, 128) * ceil_div(N, BN);
   if (tiles > (1LL << 30)) return DG_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(std::min<long long>(tiles, sms));
@@ -1197,16 +1151,8 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   // tiles); DG_PAIR=0 or DG_FORCE_BN selects the single-CTA kernel.
   if (pair_enabled() && !std::getenv("DG_FORCE_BN")) {
     {
-      dg::Params pp{};
-      pp.M = M_total;
-      pp.N = N;
-      pp.K = K;
-      pp.G = G;
+      dg::Params pp = base_params(*ds, M_total, N, K, G, nullptr, d);
       pp.m_indices = m_indices;
-      pp.d = static_cast<__nv_bfloat16*>(d);
-      pp.status = ds->status;
-      pp.timeout_ns = wait_timeout_ns();
-      pp.fault = g_fault.load();
       // the number of pair rows depends on m_indices (device): bound it by the block count
       bool launched = false;
       const dg_status s = try_pair<dg::Kind::Contiguous>(*ds, a, sfa, b, sfb, nullptr, d, pp, ceil_div(M_total, 128),
@@ -1221,16 +1167,8 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
       !map_sf(&tsa, sfa, 0, M_total, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, 0, M_total, N))
     return DG_ERR_CUDA;
-  dg::Params p{};
-  p.M = M_total;
-  p.N = N;
-  p.K = K;
-  p.G = G;
+  dg::Params p = base_params(*ds, M_total, N, K, G, nullptr, d);
   p.m_indices = m_indices;
-  p.d = static_cast<__nv_bfloat16*>(d);
-  p.status = ds->status;
-  p.timeout_ns = wait_timeout_ns();
-  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
   return launch_bn<dg::Kind::Contiguous, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
@@ -1272,16 +1210,8 @@ dg_status dg_m_grouped_fp8_gemm_nn_contiguous(const void* a, const int32_t* sfa,
       !map_sf(&tsa, sfa, 0, M_total, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, 0, M_total, N))
     return DG_ERR_CUDA;
-  dg::Params p{};
-  p.M = M_total;
-  p.N = N;
-  p.K = K;
-  p.G = G;
+  dg::Params p = base_params(*ds, M_total, N, K, G, nullptr, d);
   p.m_indices = m_indices;
-  p.d = static_cast<__nv_bfloat16*>(d);
-  p.status = ds->status;
-  p.timeout_ns = wait_timeout_ns();
-  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
   return launch_bn<dg::Kind::Contiguous, false, false, false, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
@@ -1307,16 +1237,8 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
       !map_sf(&tsa, sfa, G, max_m, KP, 128) || !map_sf(&tsb, sfb, G, ceil_div(N, 128), KP, 8) ||
       !map_out(&td, d, G, max_m, N))
     return DG_ERR_CUDA;
-  dg::Params p{};
-  p.M = max_m;
-  p.N = N;
-  p.K = K;
-  p.G = G;
+  dg::Params p = base_params(*ds, max_m, N, K, G, nullptr, d);
   p.masked_m = masked_m;
-  p.d = static_cast<__nv_bfloat16*>(d);
-  p.status = ds->status;
-  p.timeout_ns = wait_timeout_ns();
-  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(G) * ceil_div(max_m, 128) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
   return launch_bn<dg::Kind::Masked, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
@@ -1459,16 +1381,7 @@ dg_status dg_fp8_fp4_gemm_nt(const void* a, const int32_t* sfa, const void* b, c
   const int sms = sms_to_use(*ds);
   const long long tiles128 = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 128);
   if (tiles128 >= sms && M > 128 && pair_enabled() && !std::getenv("DG_FORCE_BN")) {
-    dg::Params pp{};
-    pp.M = M;
-    pp.N = N;
-    pp.K = K;
-    pp.G = 1;
-    pp.c = static_cast<const __nv_bfloat16*>(c);
-    pp.d = static_cast<__nv_bfloat16*>(d);
-    pp.status = ds->status;
-    pp.timeout_ns = wait_timeout_ns();
-    pp.fault = g_fault.load();
+    dg::Params pp = base_params(*ds, M, N, K, 1, c, d);
     bool launched = false;
     const dg_status s = try_pair<dg::Kind::Dense, false, true>(*ds, a, sfa, b, sfb, c, d, pp, ceil_div(M, 256), sms,
                                                                stream, &launched);
@@ -1482,16 +1395,7 @@ dg_status dg_fp8_fp4_gemm_nt(const void* a, const int32_t* sfa, const void* b, c
           !map_sf(&tsa, sfa, 0, M, ceil_div(K / 128, 4), 128) || !map_sf_fp4(&tsb, sfb, 0, N, K / 128, sbn, 2) ||
           !map_out(&td, d, 0, M, N))
         return DG_ERR_CUDA;
-      dg::Params p{};
-      p.M = M;
-      p.N = N;
-      p.K = K;
-      p.G = 1;
-      p.c = static_cast<const __nv_bfloat16*>(c);
-      p.d = static_cast<__nv_bfloat16*>(d);
-      p.status = ds->status;
-      p.timeout_ns = wait_timeout_ns();
-      p.fault = g_fault.load();
+      dg::Params p = base_params(*ds, M, N, K, 1, c, d);
       const int grid = static_cast<int>(static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, sbn)) * kSplitWays;
       if (c) return launch_split<true, true>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
       return launch_split<false, true>(sbn, ta, tb, tsa, tsb, td, p, grid, stream);
@@ -1514,16 +1418,8 @@ dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void* a, const int32_t* 
   DeviceState* ds = nullptr;
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
   if (pair_enabled() && !std::getenv("DG_FORCE_BN")) {
-    dg::Params pp{};
-    pp.M = M_total;
-    pp.N = N;
-    pp.K = K;
-    pp.G = G;
+    dg::Params pp = base_params(*ds, M_total, N, K, G, nullptr, d);
     pp.m_indices = m_indices;
-    pp.d = static_cast<__nv_bfloat16*>(d);
-    pp.status = ds->status;
-    pp.timeout_ns = wait_timeout_ns();
-    pp.fault = g_fault.load();
     bool launched = false;
     const dg_status s = try_pair<dg::Kind::Contiguous, false, true>(*ds, a, sfa, b, sfb, nullptr, d, pp,
                                                                     ceil_div(M_total, 128), sms_to_use(*ds), stream,
@@ -1536,16 +1432,8 @@ dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void* a, const int32_t* 
       !map_sf(&tsa, sfa, 0, M_total, ceil_div(K / 128, 4), 128) || !map_sf_fp4(&tsb, sfb, G, N, K / 128, BN, 1) ||
       !map_out(&td, d, 0, M_total, N))
     return DG_ERR_CUDA;
-  dg::Params p{};
-  p.M = M_total;
-  p.N = N;
-  p.K = K;
-  p.G = G;
+  dg::Params p = base_params(*ds, M_total, N, K, G, nullptr, d);
   p.m_indices = m_indices;
-  p.d = static_cast<__nv_bfloat16*>(d);
-  p.status = ds->status;
-  p.timeout_ns = wait_timeout_ns();
-  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(ceil_div(M_total, 128)) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
   return launch_bn<dg::Kind::Contiguous, false, false, false, false, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
@@ -1568,16 +1456,8 @@ dg_status dg_m_grouped_fp8_fp4_gemm_nt_masked(const void* a, const int32_t* sfa,
       !map_sf(&tsa, sfa, G, max_m, ceil_div(K / 128, 4), 128) || !map_sf_fp4(&tsb, sfb, G, N, K / 128, BN, 1) ||
       !map_out(&td, d, G, max_m, N))
     return DG_ERR_CUDA;
-  dg::Params p{};
-  p.M = max_m;
-  p.N = N;
-  p.K = K;
-  p.G = G;
+  dg::Params p = base_params(*ds, max_m, N, K, G, nullptr, d);
   p.masked_m = masked_m;
-  p.d = static_cast<__nv_bfloat16*>(d);
-  p.status = ds->status;
-  p.timeout_ns = wait_timeout_ns();
-  p.fault = g_fault.load();
   const long long tiles = static_cast<long long>(G) * ceil_div(max_m, 128) * ceil_div(N, BN);
   const int grid = static_cast<int>(tiles < sms_to_use(*ds) ? tiles : sms_to_use(*ds));
   return launch_bn<dg::Kind::Masked, false, false, false, false, true>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
