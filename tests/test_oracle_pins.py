@@ -770,3 +770,28 @@ def test_pack_sf_layout():
     assert w.shape == (2, 8)
     assert np.array_equal(w, words_from_codes(e))
     assert np.array_equal(O.unpack_sf(w, 6, 5), e)
+
+
+def test_fp4_quantiser_roundtrip_ties_and_packing():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal((16, 256)) * 3).astype(np.float32)
+    x[0, :32] = 0.0
+    packed, e = W.quantize_fp4_rows(x)
+    assert packed.shape == (16, 128) and e.shape == (16, 8)
+    codes = np.stack([(packed >> 0) & 0xF, (packed >> 4) & 0xF], axis=-1).reshape(16, 256)   # even element low
+    vals = np.array([float(e2m1_value(int(c))) for c in codes.reshape(-1)]).reshape(16, 256)
+    scale = np.exp2(np.repeat(e.astype(np.float64) - 127, 32, axis=1))
+    deq = vals * scale
+    # E2M1 has one mantissa bit: within a quarter of the value's binade step, or half the
+    # smallest step (0.5 * scale) near zero
+    assert (np.abs(deq - x) <= np.maximum(0.25 * np.abs(x), 0.25 * scale) + 1e-12).all()
+    assert e[0, 0] == 127 and (codes[0, :32] == 0).all()
+    amax = np.abs(x.reshape(16, 8, 32)).max(2)
+    ok = amax > 0
+    assert (amax[ok] / np.exp2(e[ok].astype(np.float64) - 127) <= 6).all()      # fits E2M1
+    assert (amax[ok] / np.exp2(e[ok].astype(np.float64) - 128) > 6).all()       # the least such exponent
+    # ties go to the even code: 0.25 -> 0, 0.75 -> 1.0, 1.25 -> 1.0, 1.75 -> 2.0, 2.5 -> 2, 3.5 -> 4, 5 -> 4
+    t = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -5.0], np.float32)
+    got = [float(e2m1_value(int(c))) for c in W._to_e2m1_codes(t)]
+    assert got == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, -4.0]
+    assert W.pack_fp4(np.array([[1, 2, 3, 4]], np.uint8)).tolist() == [[0x21, 0x43]]
