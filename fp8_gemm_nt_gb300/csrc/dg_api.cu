@@ -29,6 +29,7 @@ constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
 constexpr int kMinKGroupsPerCta = 4;                            // stream-K: smallest share per CTA
 constexpr size_t kSkCounterInts = 4096;                         // stream-K arrival counters per workspace
+constexpr size_t kMaxWorkspaces = 16;                           // streams with a cached workspace, per device
 
 // Stream-K workspace owned by the library: one per (device, stream), grown on demand.
 struct Workspace {
@@ -112,6 +113,16 @@ dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, v
   for (auto& x : ds.workspaces)
     if (x.stream == stream) w = &x;
   if (!w) {
+    if (ds.workspaces.size() >= kMaxWorkspaces) {
+      // Many streams have come and gone (a workspace is never tied to a stream's lifetime):
+      // wait for the device, so that every workspace is idle, and release them all; the
+      // streams still in use get new ones on their next call.
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e);
+      for (auto& x : ds.workspaces)
+        if (x.ptr && (e = cudaFree(x.ptr)) != cudaSuccess) return cuda_fail(e);
+      ds.workspaces.clear();
+    }
     ds.workspaces.push_back(Workspace{stream, nullptr, 0});
     w = &ds.workspaces.back();
   }

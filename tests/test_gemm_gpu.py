@@ -332,3 +332,22 @@ def test_contiguous_indices_written_by_the_previous_kernel(lib):
         ref, valid = O.m_grouped_fp8_gemm_nt_contiguous(q.a, q.sfa, q.b, q.sfb, m_idx, q.M_total, q.N, q.K, q.G)
         assert (bf16_bits(d)[~valid] == SENTINEL).all()
         assert_parity(bf16_f64(d)[valid], ref[valid], f"permutation {perm}")
+
+
+def test_workspaces_for_many_streams(lib):
+    # more streams than the library keeps workspaces for (16): the cache is released and
+    # rebuilt; the stream-K shape below uses the workspace on every call, and every stream
+    # computes the same bits (stream-K sums its partials in a fixed order)
+    p = W.make_dense(256, 384, 1152, seed=55)
+    a, sfa, b, sfb = dev(p.a), dev(p.sfa), dev(p.b), dev(p.sfb)
+    outs = []
+    for s in [torch.cuda.Stream() for _ in range(24)]:
+        d = sentinel_like((p.M, p.N))
+        with torch.cuda.stream(s):
+            lib.dg_fp8_gemm_nt(a, sfa, b, sfb, None, d)
+        outs.append(d)
+    torch.cuda.synchronize()
+    first = bf16_bits(outs[0])
+    for i, d in enumerate(outs[1:]):
+        assert np.array_equal(bf16_bits(d), first), f"stream {i + 1}"
+    assert_parity(bf16_f64(outs[0]), O.fp8_gemm_nt(p.a, p.sfa, p.b, p.sfb, None, p.M, p.N, p.K), "many streams")
