@@ -2,18 +2,18 @@
  * dg.h -- C ABI of the GB300 (sm_103a) fine-grained-scaled FP8 GEMM library (libdg.so).
  *
  * Operation (DeepGEMM README, as reproduced on the page "Weight gradient kernels for
- * dense and MoE models #95", section "Interfaces / Notices"): the library follows the
- * naming convention D = C + A @ B with the NT layout, so fp8_gemm_nt computes
+ * dense and MoE models #95", section "Interfaces / Notices"): every GEMM is named after
+ * D = C + A @ B and the suffix gives the storage of A and B; NT keeps A as is and reads B
+ * transposed, so fp8_gemm_nt computes
  *
  *     D[m, n] = C[m, n] + sum_g sA[m, g] * sB[n / 128, g] * sum_{k = 128 g}^{128 g + 127} A[m, k] * B[n, k]
  *
  * with A and B in FP8 E4M3 (OCP "E4M3FN"), FP32 accumulation and a BF16 result.
  * Scale granularity: A has one scale per row per 128-wide K-group ("1x128"), B one
- * scale per 128x128 block. Scales are UE8M0 (code e means 2^(e-127)), packed four per
- * int32 ("SM100 requires scaling factors in packed UE8M0 format, which packs 4 UE8M0
- * into a single torch.int", same section): K-group 4q+j is byte j (least significant
- * first) of word q. The LHS scales are "TMA-aligned and transposed": MN-major, with
- * the MN extent padded to a multiple of 4 words (16 bytes).
+ * scale per 128x128 block. Scales are UE8M0 (code e means 2^(e-127)); on SM100 the same
+ * section has them packed four to a 32-bit integer: K-group 4q+j is byte j (least
+ * significant first) of word q. The section also asks for the LHS scales transposed and
+ * padded for TMA: MN-major, with the MN extent padded to a multiple of 4 words (16 bytes).
  *
  * Notation used below: KG = K / 128, KP = ceil(KG / 4), NB = ceil(N / 128),
  * ceil4(x) = 4 * ceil(x / 4).
@@ -105,8 +105,8 @@ dg_status dg_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* sfa, const
 /*
  * K-grouped weight-gradient GEMM for MoE experts, FP32 output (page "Weight gradient kernels
  * for dense and MoE models #95": k_grouped_wgrad_gemm_fp8_fp8_fp32_nt; README "Grouped GEMMs":
- * the K-axis-grouped API, M and N fixed). Expert g owns the K-slice [off_g, off_g + ks[g]) of
- * A and B, off_g = ks[0] + ... + ks[g-1], and D[g] = C[g] + A[:, slice_g] @ B[:, slice_g].T.
+ * grouping along K, with M and N the same for every group). Expert g owns the K-slice
+ * [off_g, off_g + ks[g]) of A and B, off_g = ks[0] + ... + ks[g-1], and D[g] = C[g] + A[:, slice_g] @ B[:, slice_g].T.
  *   a   : e4m3 [M, K_total] row-major (the experts' token columns concatenated along K).
  *   sfa : int32 [sf_k_rows][ceil4(M)] UE8M0 words packed per expert: expert g's K-groups
  *         j = 0, 1, ... in byte j % 4 of word row R_g + j / 4, R_g = sum over h < g of
@@ -128,8 +128,9 @@ dg_status dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(const void* a, const int32_t* 
                                                 cudaStream_t stream);
 
 /*
- * K-grouped GEMM in the TN layout (README "Grouped GEMMs (contiguous layout)": the K-axis-
- * grouped API for MoE weight backward, k_grouped_fp8_gemm_tn_contiguous). The same operation
+ * K-grouped GEMM in the TN layout (README "Grouped GEMMs (contiguous layout)": the API that
+ * groups K instead of M, meant for the weight gradient of MoE layers,
+ * k_grouped_fp8_gemm_tn_contiguous). The same operation
  * and arguments as dg_k_grouped_wgrad_gemm_fp8_fp8_fp32_nt, with A and B stored token-major:
  *   a : E4M3 [K_total, M] row-major (M contiguous; M a multiple of 16),
  *   b : E4M3 [K_total, N] row-major (N contiguous),
@@ -195,8 +196,8 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa,
 /*
  * FP8 x FP4 GEMMs: D = C + A @ B.T with A in E4M3 and B in FP4 (DeepGEMM news entry of
  * 2026.04.16, "FP8xFP4 GEMM"; the Mega MoE section of the same README runs its linear layers
- * as "FP8xFP4" on weights given as "FP4 with UE8M0 SF"). The pages say no more; the readings
- * taken here:
+ * as FP8 x FP4 products, on FP4 weights that carry UE8M0 scales). The pages say no more; the
+ * readings taken here:
  *   - B is OCP MX FP4 (E2M1: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}), two codes per byte, element 2j
  *     of a row in the low nibble of byte j: b is uint8 [N, K/2] row-major.
  *   - B has one UE8M0 scale per row per 32 consecutive K-elements (the MX block), packed four

@@ -10,9 +10,10 @@ gradient kernels for dense and MoE models #95" (gitblind.noratr.app, DeepGEMM pu
 95), by README section, plus the Hindi summary page "DeepGEMM: ... FP8 GEMM kernel"
 (hi.news.hada.io topic 19459) where it restates the same section:
 
-* "Interfaces / Notices": the naming convention D = C + A @ B, the NT layout
-  (fp8_gemm_nt computes D = C + A @ B.T), and the SM100 scale format "packed UE8M0,
-  four UE8M0 in one int", LHS scales "TMA-aligned and transposed".
+* "Interfaces / Notices": GEMMs are named after D = C + A @ B, the NT layout
+  (fp8_gemm_nt computes D = C + A @ B.T), and the SM100 scale format (UE8M0 codes,
+  four of them packed into one 32-bit integer; the LHS scales transposed and padded
+  for TMA).
 * "Grouped GEMMs (contiguous layout)": only M is grouped; N and K are fixed; each
   expert's token rows are concatenated and every segment is aligned to the M block.
 * "Grouped GEMMs (masked layout)": a mask tensor gives each group's valid rows and
@@ -100,9 +101,9 @@ def decode_bf16(bits: np.ndarray) -> np.ndarray:
 def unpack_sf(words: np.ndarray, mn: int, kgroups: int) -> np.ndarray:
     """Packed UE8M0 words [ceil(kgroups/4), >=mn] (MN-major) -> codes [mn, kgroups].
 
-    "SM100 requires scaling factors in packed UE8M0 format, which packs 4 UE8M0
-    into a single torch.int" and the LHS factor is "transposed" (README "Interfaces /
-    Notices"). Reading: K-group g is byte g % 4 of word g // 4 of its row.
+    On SM100 the scales are UE8M0 codes packed four to a 32-bit integer, and the LHS
+    scales are stored transposed (README "Interfaces / Notices"). Reading: K-group g is
+    byte g % 4 of word g // 4 of its row.
     """
     w = np.asarray(words).view(np.uint32)
     out = np.empty((mn, kgroups), np.uint8)
@@ -240,8 +241,8 @@ def k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, c: Optional[np.ndarray], ks
                                      groups: Optional[Sequence[int]] = None,
                                      rows: Optional[Sequence[int]] = None) -> np.ndarray:
     """The K-grouped GEMM with A stored [K_total, M] and B stored [K_total, N] (README
-    "Grouped GEMMs (contiguous layout)": k_grouped_fp8_gemm_tn_contiguous, the K-axis-grouped
-    API for MoE weight backward). Storage only: the same D[g] = C[g] + A_g @ B_g.T as
+    "Grouped GEMMs (contiguous layout)": k_grouped_fp8_gemm_tn_contiguous, the API that groups
+    K instead of M for the weight gradient of MoE layers). Storage only: the same D[g] = C[g] + A_g @ B_g.T as
     k_grouped_wgrad_gemm_fp8_fp8_fp32_nt over the logical [M, K_total] and [N, K_total]."""
     return k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(np.ascontiguousarray(np.asarray(a).T), sfa,
                                                 np.ascontiguousarray(np.asarray(b).T), sfb, c, ks, M, N,
@@ -307,7 +308,8 @@ def m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, masked_m, G: int, max_m: int, N
 # FP8 x FP4: E4M3 activations against E2M1 weights
 # --------------------------------------------------------------------------------------
 # The pages name the GEMM only (the DeepGEMM news entry of 2026.04.16, "FP8xFP4 GEMM", and
-# the Mega MoE section, whose linear layers are "FP8xFP4" with weights "FP4 with UE8M0 SF").
+# the Mega MoE section, whose linear layers multiply FP8 activations by FP4 weights that carry
+# UE8M0 scales).
 # Readings, each the plainest one the pages allow:
 # * the FP4 operand is OCP MX FP4 (E2M1: sign, 2 exponent bits with bias 1, 1 mantissa
 #   bit; +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}; no infinities or NaN), two codes per byte, element

@@ -10,13 +10,13 @@ as quoted on the pages, "Interfaces / Notices"): A and B are E4M3 bytes, both
 K-major ("NT": A is [M, K] row-major, B is [N, K] row-major). Scale factors are
 UE8M0 exponents packed four to one int32 (K-group 4q+j in byte j of word q,
 little-endian), stored MN-major with the MN extent padded to a multiple of four
-words ("TMA-aligned and transposed"). A has one scale per row per 128-wide
+words (the transposed, TMA-padded layout). A has one scale per row per 128-wide
 K-group; B has one scale per 128x128 block. The pages leave the packing byte
 order and the B-scale layout open; these are the plain readings adopted here.
 
-Every generator is deterministic in its seed (numpy PCG64). Quantisation is the
-user's job on the pages ("FP8 casting must be handled separately by the user");
-the recipe used here is a per-group power-of-two scale that maps the group's
+Every generator is deterministic in its seed (numpy PCG64). On the pages the caller
+quantises its own inputs (the library does no FP8 casting for them); the recipe
+used here is a per-group power-of-two scale that maps the group's
 absolute maximum into the E4M3 range, then round-to-nearest-even to E4M3.
 """
 from __future__ import annotations
