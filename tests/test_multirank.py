@@ -36,7 +36,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks_agree_on_the_slowest_time():
     world, port = 2, _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:     # no fork of a multi-threaded process
         out = mgr.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         results = dict(out)

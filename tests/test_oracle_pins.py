@@ -496,11 +496,24 @@ def pin_fp4_grouped_equals_dense(O_):
     assert np.isnan(Dm[1]).all() and np.isnan(Dm[0, 2:]).all()
 
 
+def pin_golden(O_):
+    # the hand-worked examples under tests/golden/ (each shows its arithmetic in the file)
+    from golden_util import all_fixtures, check_oracle, load
+    for name in all_fixtures():
+        g = load(name)
+        if g.form == "pack_sf":
+            mn, kg = g.sf.shape
+            codes = O_.unpack_sf(g.words.view(np.int32), mn, kg)
+            assert np.array_equal(W.pack_sf(codes).view(np.uint32), g.words), name
+        else:
+            check_oracle(O_, g)
+
+
 PINS = [pin_e4m3_table, pin_ue8m0_table, pin_bf16, pin_unpack, pin_brute_force, pin_identity,
         pin_one_hot, pin_pow2_invariance, pin_c_only, pin_dequantised_route,
         pin_contiguous_equals_dense, pin_masked_equals_dense, pin_wgrad_brute_force, pin_wgrad_c_only,
         pin_k_grouped_equals_per_expert, pin_layouts, pin_grouped_layouts, pin_e2m1_table, pin_fp4_brute_force,
-        pin_fp4_one_hot, pin_fp4_matches_fp8_route, pin_fp4_grouped_equals_dense]
+        pin_fp4_one_hot, pin_fp4_matches_fp8_route, pin_fp4_grouped_equals_dense, pin_golden]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
