@@ -16,6 +16,7 @@
 #include "dg.h"
 #include "fp8_gemm.cuh"
 #include "fp8_gemm_pair.cuh"
+#include "workspace_cache.h"
 
 namespace {
 
@@ -29,13 +30,22 @@ constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
 constexpr int kMinKGroupsPerCta = 4;                            // stream-K: smallest share per CTA
 constexpr size_t kSkCounterInts = 4096;                         // stream-K arrival counters per workspace
-constexpr size_t kMaxWorkspaces = 16;                           // streams with a cached workspace, per device
+constexpr size_t kMaxWorkspaces = 16;                           // freeable cached workspaces, per device
 
-// Stream-K workspace owned by the library: one per (device, stream), grown on demand.
-struct Workspace {
-  cudaStream_t stream = nullptr;
-  void* ptr = nullptr;
-  size_t bytes = 0;
+// The CUDA runtime calls the workspace cache policy (workspace_cache.h) is written against.
+struct CudaApi {
+  using Stream = cudaStream_t;
+  static int is_capturing(Stream s, bool* capturing) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &st);
+    *capturing = st != cudaStreamCaptureStatusNone;
+    return static_cast<int>(e);
+  }
+  static int device_synchronize() { return static_cast<int>(cudaDeviceSynchronize()); }
+  static int stream_synchronize(Stream s) { return static_cast<int>(cudaStreamSynchronize(s)); }
+  static int malloc(void** p, size_t n) { return static_cast<int>(cudaMalloc(p, n)); }
+  static int free(void* p) { return static_cast<int>(cudaFree(p)); }
+  static int memset_async(void* p, size_t n, Stream s) { return static_cast<int>(cudaMemsetAsync(p, 0, n, s)); }
 };
 
 struct DeviceState {
@@ -43,7 +53,7 @@ struct DeviceState {
   bool supported = false;
   int num_sms = 0;
   uint32_t* status = nullptr;
-  std::vector<Workspace> workspaces;
+  dg::WorkspaceCache<cudaStream_t> workspaces;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mutex;
@@ -105,41 +115,26 @@ dg::Params base_params(const DeviceState& ds, int M, int N, int K, int G, const 
   return p;
 }
 
-// Workspace of at least `bytes` for `stream`, zeroed when (re)allocated. The stream-K
-// arrival counters at its start are left at zero by every completed launch.
-dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, void** out) {
-  std::lock_guard<std::mutex> lock(g_mutex);
-  Workspace* w = nullptr;
-  for (auto& x : ds.workspaces)
-    if (x.stream == stream) w = &x;
-  if (!w) {
-    if (ds.workspaces.size() >= kMaxWorkspaces) {
-      // Many streams have come and gone (a workspace is never tied to a stream's lifetime):
-      // wait for the device, so that every workspace is idle, and release them all; the
-      // streams still in use get new ones on their next call.
-      cudaError_t e = cudaDeviceSynchronize();
-      if (e != cudaSuccess) return cuda_fail(e);
-      for (auto& x : ds.workspaces)
-        if (x.ptr && (e = cudaFree(x.ptr)) != cudaSuccess) return cuda_fail(e);
-      ds.workspaces.clear();
-    }
-    ds.workspaces.push_back(Workspace{stream, nullptr, 0});
-    w = &ds.workspaces.back();
-  }
-  if (w->bytes < bytes) {
-    cudaError_t e;
-    if (w->ptr) {
-      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e);
-      if ((e = cudaFree(w->ptr)) != cudaSuccess) return cuda_fail(e);
-      w->ptr = nullptr;
-      w->bytes = 0;
-    }
-    const size_t alloc = bytes + bytes / 2;
-    if ((e = cudaMalloc(&w->ptr, alloc)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMemsetAsync(w->ptr, 0, alloc, stream)) != cudaSuccess) return cuda_fail(e);
-    w->bytes = alloc;
-  }
-  *out = w->ptr;
+// A workspace pointer and the lock that keeps it valid. Workspaces are freed only under
+// g_mutex, after a synchronisation (the device's, for a 17th stream; the stream's, to grow
+// one), and that synchronisation waits only for work already enqueued. A caller therefore
+// holds the lease until its kernels are launched: another host thread cannot free the
+// memory between the lookup and the launch.
+struct WorkspaceLease {
+  void* ptr = nullptr;
+  std::unique_lock<std::mutex> lock;
+};
+
+// Workspace of at least `bytes` for `stream` (policy in workspace_cache.h). The stream-K
+// arrival counters at its start are zero when allocated and left at zero by every completed
+// launch.
+dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, WorkspaceLease* out) {
+  std::unique_lock<std::mutex> lock(g_mutex);
+  void* ptr = nullptr;
+  if (const int e = dg::acquire<CudaApi, kMaxWorkspaces>(ds.workspaces, stream, bytes, &ptr))
+    return cuda_fail(static_cast<cudaError_t>(e));
+  out->ptr = ptr;
+  out->lock = std::move(lock);
   return DG_OK;
 }
 
@@ -655,11 +650,11 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
     return DG_ERR_UNSUPPORTED;
   // contiguous form: the pair-row list (3 ints per pair row, at most one per block) and its length
   const size_t list_words = kKind == dg::Kind::Contiguous ? 4 + 4 * static_cast<size_t>(ceil_div(3 * num_mb, 4)) : 0;
-  void* ws = nullptr;
+  WorkspaceLease ws;   // held until both kernels below are launched
   if (dg_status s = stream_workspace(ds, stream, kSkCounterInts * 4 + (sfa_words + sfb_words + list_words) * 4, &ws);
       s != DG_OK)
     return s;
-  int32_t* sfa_t = static_cast<int32_t*>(ws) + kSkCounterInts;
+  int32_t* sfa_t = static_cast<int32_t*>(ws.ptr) + kSkCounterInts;
   int32_t* sfb_t = sfa_t + sfa_words;
   int32_t* list = sfb_t + sfb_words;
   {
@@ -892,6 +887,7 @@ dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, 
   const int num_kc = ceil_div(K / 128, kg);                 // stream-K units per tile
   const long long units = tiles * num_kc;
   const long long sk = std::min<long long>(sms, units * kg / kMinKGroupsPerCta);
+  WorkspaceLease ws;   // stream-K only; held until the launch at the end
   if (tiles < sms && sk > tiles) {
     int slots = 1;
     for (long long t = 0; t < tiles; ++t) {
@@ -903,12 +899,11 @@ dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, 
     // problem shape: completed launches leave it all-zero for the next one), then partials.
     const size_t ws_floats = static_cast<size_t>(tiles) * slots * 128 * BN;
     if (static_cast<size_t>(tiles) * kEpilogueWarps > kSkCounterInts) return DG_ERR_UNSUPPORTED;
-    void* ws = nullptr;
     if (dg_status s = stream_workspace(*ds, stream, kSkCounterInts * 4 + ws_floats * 4, &ws); s != DG_OK) return s;
     p.sk_ctas = static_cast<int>(sk);
     p.sk_slots = slots;
-    p.sk_counters = static_cast<int*>(ws);
-    p.sk_ws = reinterpret_cast<float*>(static_cast<int*>(ws) + kSkCounterInts);
+    p.sk_counters = static_cast<int*>(ws.ptr);
+    p.sk_ws = reinterpret_cast<float*>(static_cast<int*>(ws.ptr) + kSkCounterInts);
     grid = static_cast<int>(sk);
   } else {
     kg = 1;   // tile mode: whole tiles, one K-group per stage
@@ -1319,8 +1314,9 @@ dg_status dg_get_device_status(cudaStream_t stream) {
   if (v & dg::kStatusTimeoutBit) {
     // an aborted stream-K launch may leave its arrival counters non-zero: clear them
     std::lock_guard<std::mutex> lock(g_mutex);
-    for (auto& w : ds->workspaces)
-      if (w.ptr && (e = cudaMemset(w.ptr, 0, w.bytes)) != cudaSuccess) return cuda_fail(e);
+    for (const auto* list : {&ds->workspaces.live, &ds->workspaces.retained})
+      for (const auto& w : *list)
+        if (w.ptr && (e = cudaMemset(w.ptr, 0, w.bytes)) != cudaSuccess) return cuda_fail(e);
     return DG_ERR_TIMEOUT;
   }
   return DG_ERR_BAD_INDEX;

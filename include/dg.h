@@ -33,6 +33,15 @@
  *     Rows past M are never read or written.
  *   - Not thread-safe against concurrent dg_set_num_sms(); GEMM calls themselves may
  *     be issued from several host threads.
+ *   - Library-owned device memory: a 4-byte status word per device, and a workspace per
+ *     (device, stream) for the paths that need one (stream-K partials, the CTA-pair kernel's
+ *     scale chunks), grown on demand. At most 16 workspaces are cached per device; a call
+ *     on a further stream synchronises the device and releases them.
+ *   - CUDA graphs: a captured call uses the workspace its stream already has, so make one
+ *     uncaptured call of at least the same size on the capturing stream first (allocating
+ *     inside a capture works only in cudaStreamCaptureModeRelaxed). Nothing is synchronised
+ *     or freed during a capture, and a workspace used in one is kept until the process exits,
+ *     so replays stay valid however many streams come later.
  */
 #ifndef DG_H_
 #define DG_H_
@@ -254,7 +263,7 @@ dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgrou
  * For callers that cannot allocate when they run the GEMM: code being captured into a
  * CUDA graph, servers that fix their device-memory footprint at start-up, or a custom
  * allocator that owns all device memory. dg_fp8_gemm_nt allocates on first use (a status
- * word, and a per-stream workspace for problems with fewer 128x128 tiles than SMs); this
+ * word, and a per-stream workspace for stream-K and the CTA-pair kernel); this
  * entry point uses instead a fixed 16 MiB scratch array that the library holds in device
  * memory from the first call on each GPU until the process exits.
  *
