@@ -200,8 +200,8 @@ def k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(a, sfa, b, sfb, c: Optional[np.ndarray]
                                          groups: Optional[Sequence[int]] = None,
                                          rows: Optional[Sequence[int]] = None) -> np.ndarray:
     """K-grouped weight-gradient GEMM for MoE (page "Weight gradient kernels for dense and MoE
-    models #95": k_grouped_wgrad_gemm_fp8_fp8_fp32_nt; README "Grouped GEMMs": the K-axis-
-    grouped API with M and N fixed). Expert g owns the K-slice [off_g, off_g + ks[g]) of A
+    models #95": k_grouped_wgrad_gemm_fp8_fp8_fp32_nt; README "Grouped GEMMs": grouping along
+    K, with M and N the same for every group). Expert g owns the K-slice [off_g, off_g + ks[g]) of A
     [M, K_total] and B [N, K_total] (off_g = ks[0] + ... + ks[g-1]) and gets its own FP32
     output: D[g] = C[g] + A[:, slice_g] @ B[:, slice_g].T.
 
