@@ -102,21 +102,33 @@ def _need(cond: bool, msg: str) -> None:
         raise ValueError(msg)
 
 
+def _here(t: torch.Tensor, name: str) -> None:
+    # the library works on the current device (and its stream): memory of another GPU would be
+    # read through the wrong device's mappings
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.device.index == torch.cuda.current_device(),
+          f"{name} is on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
+
+
 def _fp8(t: torch.Tensor, name: str) -> None:
-    _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _here(t, name)
+    _need(t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
     _need(t.dtype in (torch.float8_e4m3fn, torch.uint8), f"{name} must be float8_e4m3fn (or its uint8 bytes)")
 
 
 def _i32(t: torch.Tensor, name: str) -> None:
-    _need(t.is_cuda and t.is_contiguous() and t.dtype == torch.int32, f"{name} must be a contiguous CUDA int32 tensor")
+    _here(t, name)
+    _need(t.is_contiguous() and t.dtype == torch.int32, f"{name} must be a contiguous CUDA int32 tensor")
 
 
 def _bf16(t: torch.Tensor, name: str) -> None:
-    _need(t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16, f"{name} must be a contiguous CUDA bf16 tensor")
+    _here(t, name)
+    _need(t.is_contiguous() and t.dtype == torch.bfloat16, f"{name} must be a contiguous CUDA bf16 tensor")
 
 
 def _f32(t: torch.Tensor, name: str) -> None:
-    _need(t.is_cuda and t.is_contiguous() and t.dtype == torch.float32, f"{name} must be a contiguous CUDA float32 tensor")
+    _here(t, name)
+    _need(t.is_contiguous() and t.dtype == torch.float32, f"{name} must be a contiguous CUDA float32 tensor")
 
 
 def sf_shape(mn: int, k: int, groups: Optional[int] = None):
@@ -295,7 +307,8 @@ _FP4_DTYPES = (torch.uint8,) + ((torch.float4_e2m1fn_x2,) if hasattr(torch, "flo
 
 
 def _fp4(t: torch.Tensor, name: str) -> None:
-    _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _here(t, name)
+    _need(t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
     _need(t.dtype in _FP4_DTYPES, f"{name} must hold packed E2M1 bytes (uint8 or float4_e2m1fn_x2)")
 
 
@@ -357,7 +370,8 @@ def dg_m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, d, masked_m, stream=None
 def dg_pack_sf_ue8m0(sf: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """FP32 scales [mn, kgroups] -> packed UE8M0 int32 [ceil(kgroups/4), ceil4(mn)] (MN-major)."""
     lib = load_library()
-    _need(sf.is_cuda and sf.is_contiguous() and sf.dtype == torch.float32 and sf.dim() == 2,
+    _here(sf, "sf")
+    _need(sf.is_contiguous() and sf.dtype == torch.float32 and sf.dim() == 2,
           "sf must be a contiguous 2-D CUDA float32 tensor")
     mn, kg = sf.shape
     shape = (-(-kg // 4), 4 * (-(-mn // 4)))
@@ -433,7 +447,8 @@ def dg_fp8_gemm_nt_no_alloc(a, sfa, b, sfb, c, d, status, stream=None) -> torch.
     the GPU race on that scratch."""
     lib = load_library()
     _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _bf16(d, "d")
-    _need(status.is_cuda and status.numel() == 1 and status.element_size() == 4, "status must be one 4-byte CUDA word")
+    _here(status, "status")
+    _need(status.numel() == 1 and status.element_size() == 4, "status must be one 4-byte CUDA word")
     M, K = a.shape
     N = b.shape[0]
     _need(b.shape[1] == K and tuple(d.shape) == (M, N), "shape mismatch")

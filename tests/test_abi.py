@@ -129,3 +129,24 @@ def test_fp8_fp4_forms_reject_bad_arguments(lib):
     # empty problems launch nothing and accept null pointers
     assert lib.dg_fp8_fp4_gemm_nt(None, None, None, None, None, None, 0, 128, 128, None) == 0
     assert lib.dg_m_grouped_fp8_fp4_gemm_nt_masked(None, None, None, None, None, None, 2, 0, 128, 128, None) == 0
+
+
+def test_binding_rejects_tensors_outside_the_current_device(lib):
+    # host tensors never reach the library: the binding raises before any call
+    import torch
+    import fp8_gemm_nt_gb300 as L
+    M = N = K = 128
+    a = torch.zeros((M, K), dtype=torch.uint8)
+    sf = torch.zeros(L.sf_shape(M, K), dtype=torch.int32)
+    sfb = torch.zeros(L.sf_shape(1, K), dtype=torch.int32)
+    d = torch.zeros((M, N), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.dg_fp8_gemm_nt(a, sf, a, sfb, None, d)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.dg_wgrad_gemm_fp8_fp8_fp32_nt(a, sf, a, sfb, None, d.float())
+    with pytest.raises(ValueError, match="CUDA"):
+        L.dg_fp8_fp4_gemm_nt(a, sf, a[:, :K // 2].contiguous(), torch.zeros((1, N), dtype=torch.int32), None, d)
+    with pytest.raises(ValueError, match="CUDA"):
+        L.dg_pack_sf_ue8m0(torch.ones((4, 4), dtype=torch.float32))
+    with pytest.raises(ValueError, match="CUDA"):
+        L.dg_fp8_gemm_nt_no_alloc(a, sf, a, sfb, None, d, torch.zeros(1, dtype=torch.int32))
