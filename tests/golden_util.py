@@ -7,8 +7,9 @@ value, then lists one item per line:
           k_grouped_fp32 | pack_sf
   shape   dense, wgrad: M N K;  masked: G max_m N K;  contiguous: G M_total N K;
           k_grouped: M N (with "ks");  pack_sf: mn kgroups
-  layout  nt | nn | tn | tt   (dense_e4m3 only; default nt). The rows below always give the
-          logical A' [M, K] and B [N, K]; the layout says how the library receives them.
+  layout  nt | nn | tn | tt (dense_e4m3), nt | nn (contiguous_e4m3), nt | tn (k_grouped_fp32);
+          default nt. The rows below always give the logical A' [M, K] and B [N, K]; the
+          layout says how the library receives them.
   ks      K of each expert (k_grouped)
   a  IDX RUNS     one row of A: IDX is "r" ("g,r" for masked); codes fill from k = 0, zeros after
   b  IDX RUNS     one row of B: IDX is "n" ("g,n" for the grouped forms); E2M1 codes are nibbles
@@ -96,7 +97,8 @@ def load(name: str) -> Golden:
     form = items["form"][0][0]
     shape = [int(x) for x in items["shape"][0]]
     layout = items["layout"][0][0] if "layout" in items else "nt"
-    assert layout == "nt" or form == "dense_e4m3"
+    assert layout == "nt" or form == "dense_e4m3" or (form, layout) in (("contiguous_e4m3", "nn"),
+                                                                         ("k_grouped_fp32", "tn"))
 
     if form == "pack_sf":
         mn, kg = shape
@@ -200,10 +202,16 @@ def all_fixtures() -> List[str]:
 
 
 def stored(g: Golden):
-    """A and B as the library receives them in the fixture's layout (dense forms)."""
+    """A and B as the library receives them in the fixture's layout. A transposed A is
+    [K, M]; a transposed B is [K, N], or [G, K, N] for the grouped weights."""
     p = g.problem
     a = p.a if g.layout[0] == "n" else np.ascontiguousarray(p.a.T)
-    b = np.ascontiguousarray(p.b.T) if g.layout[1] == "n" else p.b
+    if g.layout[1] == "t":
+        b = p.b
+    elif p.b.ndim == 3:
+        b = np.ascontiguousarray(p.b.transpose(0, 2, 1))
+    else:
+        b = np.ascontiguousarray(p.b.T)
     return a, b
 
 
@@ -217,10 +225,16 @@ def oracle_result(O_, g: Golden):
         return O_.fp8_fp4_gemm_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K), None
     if g.form == "wgrad_fp32":
         return O_.wgrad_gemm_fp8_fp8_fp32_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.M, p.N, p.K), None
+    if g.form == "k_grouped_fp32" and g.layout == "tn":
+        a, b = stored(g)
+        return O_.k_grouped_fp8_gemm_tn_contiguous(a, p.sfa, b, p.sfb, p.c, p.ks, p.M, p.N), None
     if g.form == "k_grouped_fp32":
         return O_.k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.ks, p.M, p.N), None
     if g.form == "masked_e4m3":
         return O_.m_grouped_fp8_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, p.masked_m, p.G, p.max_m, p.N, p.K)
+    if g.form == "contiguous_e4m3" and g.layout == "nn":
+        _, b = stored(g)
+        return O_.m_grouped_fp8_gemm_nn_contiguous(p.a, p.sfa, b, p.sfb, p.m_indices, p.M_total, p.N, p.K, p.G)
     if g.form == "contiguous_e4m3":
         return O_.m_grouped_fp8_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K,
                                                    p.G)

@@ -26,7 +26,9 @@ FORMS = {"dense_e4m3", "dense_e2m1", "masked_e4m3", "contiguous_e4m3", "wgrad_fp
 
 def test_fixtures_cover_every_form():
     assert {load(n).form for n in GEMM_FIXTURES} == FORMS and PACK_FIXTURES
-    assert "tn" in {load(n).layout for n in GEMM_FIXTURES}
+    layouts = {(load(n).form, load(n).layout) for n in GEMM_FIXTURES}
+    assert {("dense_e4m3", x) for x in ("nt", "nn", "tn", "tt")} <= layouts
+    assert {("contiguous_e4m3", "nn"), ("k_grouped_fp32", "tn")} <= layouts
     for name in GEMM_FIXTURES:
         assert (load(name).out != 0).any(), name
 
@@ -81,6 +83,20 @@ def lib():
 def _run_library(lib, g):
     from gpu_util import dev, run_contiguous, run_dense, run_k_grouped, run_masked, run_wgrad, sentinel_like
     p = g.problem
+    if g.form == "contiguous_e4m3" and g.layout == "nn":
+        _, b = stored(g)
+        d = sentinel_like((p.M_total, p.N))
+        lib.dg_m_grouped_fp8_gemm_nn_contiguous(dev(p.a), dev(p.sfa), dev(b), dev(p.sfb), d, dev(p.m_indices))
+        torch.cuda.synchronize()
+        return d
+    if g.form == "k_grouped_fp32" and g.layout == "tn":
+        a, b = stored(g)
+        c = dev(p.c) if p.c is not None else None
+        d = torch.full((p.G, p.M, p.N), float("nan"), dtype=torch.float32, device="cuda")
+        lib.dg_k_grouped_fp8_gemm_tn_contiguous(dev(a), dev(p.sfa), dev(b), dev(p.sfb), c, d,
+                                                dev(np.asarray(p.ks, np.int32)))
+        torch.cuda.synchronize()
+        return d
     if g.form == "dense_e4m3" and g.layout != "nt":
         a, b = stored(g)
         c = dev(p.c.view(np.int16), torch.bfloat16) if p.c is not None else None
