@@ -670,6 +670,28 @@ def _tn_forgets_to_transpose_a(old):
     return f
 
 
+def _tt_forgets_to_transpose_a(old):
+    def f(a, sfa, b, sfb, c, M, N, K):
+        return O.fp8_gemm_nt(np.asarray(a).reshape(M, K), sfa, b, sfb, c, M, N, K)
+    return f
+
+
+def _nn_contiguous_reads_b_as_n_major(old):
+    def f(a, sfa, b, sfb, m_indices, M_total, N, K, G, rows=None):
+        return O.m_grouped_fp8_gemm_nt_contiguous(a, sfa, np.asarray(b).reshape(G, N, K), sfb, m_indices,
+                                                  M_total, N, K, G, rows=rows)
+    return f
+
+
+def _tn_k_grouped_reads_b_as_k_major(old):
+    def f(a, sfa, b, sfb, c, ks, M, N, groups=None, rows=None):
+        K_total = int(np.sum(ks))
+        return O.k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(np.ascontiguousarray(np.asarray(a).T), sfa,
+                                                      np.asarray(b).reshape(N, K_total), sfb, c, ks, M, N,
+                                                      groups=groups, rows=rows)
+    return f
+
+
 def _mut_e2m1(table_fn):
     @contextlib.contextmanager
     def ctx():
@@ -732,6 +754,11 @@ MUTANTS = {
     "wgrad_c_dropped": _mut_attr("wgrad_gemm_fp8_fp8_fp32_nt", _wgrad_c_dropped),
     "k_grouped_scales_packed_globally": _mut_attr("k_grouped_wgrad_gemm_fp8_fp8_fp32_nt", _k_grouped_global_packing),
     "tn_reads_a_as_k_major": _mut_attr("fp8_gemm_tn", _tn_forgets_to_transpose_a),
+    "tt_reads_a_as_k_major": _mut_attr("fp8_gemm_tt", _tt_forgets_to_transpose_a),
+    "nn_contiguous_reads_b_as_n_major": _mut_attr("m_grouped_fp8_gemm_nn_contiguous",
+                                                  _nn_contiguous_reads_b_as_n_major),
+    "tn_k_grouped_reads_b_as_k_major": _mut_attr("k_grouped_fp8_gemm_tn_contiguous",
+                                                 _tn_k_grouped_reads_b_as_k_major),
     "fp4_subnormal_as_normal": _mut_e2m1(_e2m1_subnormal_as_normal),
     "fp4_sign_ignored": _mut_e2m1(lambda t: np.abs(t)),
     "fp4_high_nibble_first": _mut_attr("unpack_e2m1", _fp4_high_nibble_first),
