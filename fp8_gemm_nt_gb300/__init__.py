@@ -42,7 +42,7 @@ SIGNATURES = [
     ("dg_fp8_fp4_gemm_nt", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_fp4_gemm_nt_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("dg_m_grouped_fp8_fp4_gemm_nt_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
-    ("dg_pack_sf_ue8m0", _I, [_P, _P, _I, _I, _P]),
+    ("dg_pack_sf_ue8m0", _I, [_P, _P, _I, _I, _I, _P]),
     ("dg_get_mk_alignment_for_contiguous_layout", _I, []),
     ("dg_set_mk_alignment_for_contiguous_layout", _I, [_I]),
     ("dg_get_theoretical_mk_alignment_for_contiguous_layout", _I, []),
@@ -367,19 +367,21 @@ def dg_m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, d, masked_m, stream=None
     return d
 
 
-def dg_pack_sf_ue8m0(sf: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """FP32 scales [mn, kgroups] -> packed UE8M0 int32 [ceil(kgroups/4), ceil4(mn)] (MN-major)."""
+def dg_pack_sf_ue8m0(sf: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None,
+                     mn_major: bool = False) -> torch.Tensor:
+    """FP32 scales [mn, kgroups] (or [kgroups, mn] with mn_major) -> packed UE8M0 int32
+    [ceil(kgroups/4), ceil4(mn)] (MN-major)."""
     lib = load_library()
     _here(sf, "sf")
     _need(sf.is_contiguous() and sf.dtype == torch.float32 and sf.dim() == 2,
           "sf must be a contiguous 2-D CUDA float32 tensor")
-    mn, kg = sf.shape
+    mn, kg = (sf.shape[1], sf.shape[0]) if mn_major else (sf.shape[0], sf.shape[1])
     shape = (-(-kg // 4), 4 * (-(-mn // 4)))
     if out is None:
         out = torch.empty(shape, dtype=torch.int32, device=sf.device)
     _i32(out, "out")
     _need(tuple(out.shape) == shape, "out shape mismatch")
-    _check("dg_pack_sf_ue8m0", lib.dg_pack_sf_ue8m0(_ptr(sf), _ptr(out), mn, kg, _stream(stream)))
+    _check("dg_pack_sf_ue8m0", lib.dg_pack_sf_ue8m0(_ptr(sf), _ptr(out), mn, kg, int(mn_major), _stream(stream)))
     return out
 
 

@@ -842,8 +842,9 @@ __device__ __forceinline__ uint32_t ue8m0_ceil(float f, uint32_t* status) {
   return code > 254u ? 254u : code;
 }
 
+// sf is [mn, kgroups] (K-group contiguous), or [kgroups, mn] with mn_major_in.
 __global__ void pack_sf_kernel(const float* __restrict__ sf, int32_t* __restrict__ out, int mn, int kgroups,
-                               int mn_pad, int kp, uint32_t* status) {
+                               int mn_major_in, int mn_pad, int kp, uint32_t* status) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(mn_pad) * kp) return;
   const int q = static_cast<int>(idx / mn_pad);
@@ -853,7 +854,10 @@ __global__ void pack_sf_kernel(const float* __restrict__ sf, int32_t* __restrict
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int g = 4 * q + j;
-      if (g < kgroups) w |= ue8m0_ceil(sf[static_cast<long long>(i) * kgroups + g], status) << (8 * j);
+      if (g < kgroups) {
+        const long long at = mn_major_in ? static_cast<long long>(g) * mn + i : static_cast<long long>(i) * kgroups + g;
+        w |= ue8m0_ceil(sf[at], status) << (8 * j);
+      }
     }
   }
   out[idx] = static_cast<int32_t>(w);
@@ -1250,8 +1254,9 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   return launch_bn<dg::Kind::Masked, false>(BN, ta, tb, tsa, tsb, td, p, grid, stream);
 }
 
-dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgroups, cudaStream_t stream) {
-  if (!sf_fp32 || !out || mn < 0 || kgroups <= 0) return DG_ERR_INVALID_ARG;
+dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgroups, int mn_major_in,
+                           cudaStream_t stream) {
+  if (!sf_fp32 || !out || mn < 0 || kgroups <= 0 || (mn_major_in != 0 && mn_major_in != 1)) return DG_ERR_INVALID_ARG;
   if (!aligned16(out) || (reinterpret_cast<uintptr_t>(sf_fp32) & 3u)) return DG_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
   if (dg_status s = device_state(&ds); s != DG_OK) return s;
@@ -1262,8 +1267,8 @@ dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgrou
   const int threads = 256;
   const long long blocks = (n + threads - 1) / threads;
   if (blocks > 0x7FFFFFFFll) return DG_ERR_INVALID_ARG;
-  pack_sf_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(sf_fp32, out, mn, kgroups, mn_pad, kp,
-                                                                        ds->status);
+  pack_sf_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(sf_fp32, out, mn, kgroups, mn_major_in,
+                                                                        mn_pad, kp, ds->status);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DG_OK : cuda_fail(e);
 }

@@ -245,15 +245,17 @@ dg_status dg_m_grouped_fp8_fp4_gemm_nt_masked(const void* a, const int32_t* sfa,
  * Scale-factor packing ("Utilities": get_mn_major_tma_aligned_packed_ue8m0_tensor /
  * transform_sf_into_required_layout). Converts FP32 scales into the packed, MN-major,
  * TMA-aligned UE8M0 words the GEMMs consume.
- *   sf_fp32 : FP32 [mn, kgroups] row-major device array (one scale per row/block and
- *             K-group). Each value must be a positive finite number; it is rounded UP to
+ *   sf_fp32 : FP32 device array of one scale per row/block and K-group: [mn, kgroups]
+ *             row-major (K-groups contiguous) when mn_major_in is 0, [kgroups, mn]
+ *             row-major (rows contiguous) when it is 1; any other value of mn_major_in is
+ *             DG_ERR_INVALID_ARG. Each value must be a positive finite number; it is rounded UP to
  *             the next power of two (exact powers of two are kept), then clamped to the
  *             UE8M0 range [2^-127, 2^127]. Non-positive or non-finite values encode 127
  *             (scale 1.0) and set DG_ERR_BAD_INDEX on the device.
  *   out     : int32 [ceil(kgroups/4), ceil4(mn)] device array, fully written (padding
  *             bytes and padding rows are 0).
  */
-dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgroups,
+dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgroups, int mn_major_in,
                            cudaStream_t stream);
 
 /*

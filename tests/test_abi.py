@@ -79,7 +79,8 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert lib.dg_m_grouped_fp8_gemm_nt_masked(x, x, x, x, x, x, 0, 128, 128, 128, None) == INVALID
     assert lib.dg_m_grouped_fp8_gemm_nt_masked(x, x, x, x, x, x, 4, -1, 128, 128, None) == INVALID
     assert lib.dg_m_grouped_fp8_gemm_nt_contiguous(x, x, x, x, x, P(0x10002), 128, 128, 128, 2, None) == MISALIGNED
-    assert lib.dg_pack_sf_ue8m0(None, x, 4, 4, None) == INVALID
+    assert lib.dg_pack_sf_ue8m0(None, x, 4, 4, 0, None) == INVALID
+    assert lib.dg_pack_sf_ue8m0(x, x, 4, 4, 2, None) == INVALID          # orientation flag is 0 or 1
 
 
 def test_mk_alignment_setter(lib):

@@ -241,6 +241,9 @@ def test_pack_sf_matches_layout(lib):
     out = lib.dg_pack_sf_ue8m0(dev(f))
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), W.pack_sf(e))
+    out_t = lib.dg_pack_sf_ue8m0(dev(np.ascontiguousarray(f.T)), mn_major=True)   # [kgroups, mn] input
+    torch.cuda.synchronize()
+    assert np.array_equal(out_t.cpu().numpy(), W.pack_sf(e))
     # non-powers of two round up to the next power of two
     g = f * np.float32(1.5)
     g[e >= 254] = f[e >= 254]

@@ -134,3 +134,7 @@ def test_library_packs_hand_worked_scales(lib, name):
     out = lib.dg_pack_sf_ue8m0(dev(g.sf)).cpu().numpy()
     assert lib.dg_get_device_status() == 0
     assert np.array_equal(out.view(np.uint32), g.words)
+    # the same scales given MN-major ([kgroups, mn]) pack to the same words
+    out_t = lib.dg_pack_sf_ue8m0(dev(np.ascontiguousarray(g.sf.T)), mn_major=True).cpu().numpy()
+    assert lib.dg_get_device_status() == 0
+    assert np.array_equal(out_t.view(np.uint32), g.words)
