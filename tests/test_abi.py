@@ -151,3 +151,27 @@ def test_binding_rejects_tensors_outside_the_current_device(lib):
         L.dg_pack_sf_ue8m0(torch.ones((4, 4), dtype=torch.float32))
     with pytest.raises(ValueError, match="CUDA"):
         L.dg_fp8_gemm_nt_no_alloc(a, sf, a, sfb, None, d, torch.zeros(1, dtype=torch.int32))
+
+
+def declared_prototypes():
+    """name -> parameter count of every dg_ function declared in include/*.h."""
+    protos = {}
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if not f.endswith(".h"):
+            continue
+        src = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+        for name, params in re.findall(r"\b(dg_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
+            params = params.strip()
+            protos[name] = 0 if params in ("", "void") else len(params.split(","))
+    return protos
+
+
+def test_binding_argument_counts_match_the_header():
+    # ctypes passes whatever it is told: a parameter added to the header but not to the
+    # binding (or the reverse) would shift every later argument
+    from fp8_gemm_nt_gb300 import SIGNATURES
+    protos = declared_prototypes()
+    assert set(protos) == {name for name, _, _ in SIGNATURES}
+    for name, _, args in SIGNATURES:
+        assert len(args) == protos[name], f"{name}: header has {protos[name]} parameters, binding {len(args)}"
