@@ -153,8 +153,17 @@ def test_binding_rejects_tensors_outside_the_current_device(lib):
         L.dg_fp8_gemm_nt_no_alloc(a, sf, a, sfb, None, d, torch.zeros(1, dtype=torch.int32))
 
 
+def _param_kind(param: str) -> str:
+    if "*" in param or "cudaStream_t" in param:
+        return "pointer"
+    if "unsigned long long" in param:
+        return "u64"
+    assert re.match(r"^(const\s+)?(int|dg_status)\s+\w+$", param.strip()), param
+    return "int"
+
+
 def declared_prototypes():
-    """name -> parameter count of every dg_ function declared in include/*.h."""
+    """name -> parameter kinds ("pointer", "int", "u64") of every dg_ function in include/*.h."""
     protos = {}
     inc = os.path.join(ROOT, "include")
     for f in os.listdir(inc):
@@ -163,15 +172,24 @@ def declared_prototypes():
         src = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
         for name, params in re.findall(r"\b(dg_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
             params = params.strip()
-            protos[name] = 0 if params in ("", "void") else len(params.split(","))
+            protos[name] = [] if params in ("", "void") else [_param_kind(x) for x in params.split(",")]
     return protos
 
 
-def test_binding_argument_counts_match_the_header():
+def _ctypes_kind(t) -> str:
+    if t is ctypes.c_void_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "pointer"
+    if t is ctypes.c_ulonglong:
+        return "u64"
+    assert t is ctypes.c_int, t
+    return "int"
+
+
+def test_binding_arguments_match_the_header():
     # ctypes passes whatever it is told: a parameter added to the header but not to the
-    # binding (or the reverse) would shift every later argument
+    # binding (or the reverse), or an int where a pointer is expected, would corrupt the call
     from fp8_gemm_nt_gb300 import SIGNATURES
     protos = declared_prototypes()
     assert set(protos) == {name for name, _, _ in SIGNATURES}
     for name, _, args in SIGNATURES:
-        assert len(args) == protos[name], f"{name}: header has {protos[name]} parameters, binding {len(args)}"
+        assert [_ctypes_kind(t) for t in args] == protos[name], name
