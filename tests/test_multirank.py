@@ -59,3 +59,21 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     args = argparse.Namespace(steps=1, warmup=0)
     bench.run_reference(args, rank=1, world=2)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the CPU oracle arm as the benchmark launches it: one JSON line with the keys and units
+    # of the library's own line, warm-up raised to the minimum of three steps
+    import json
+    import subprocess
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOPS" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["n_gpus"] == 1 and line["steps"] == 1 and line["warmup"] >= 3
+    assert line["config"]["workload"] == "dense_decode_128x7168x16384_c"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
