@@ -311,23 +311,34 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), util=float(parts[4]),
-                                 flags=dict(zip(REASON_FIELDS, [x.lower() == "active" for x in parts[6:10]]))))
-            except ValueError:
-                continue
-        if not rows:
-            return None
-        busy = [r for r in rows if r["util"] >= 50] or rows
-        reasons = sorted({k for r in busy for k, v in r["flags"].items() if v})
-        return dict(sm_mhz=statistics.median(r["sm"] for r in busy), sm_max_mhz=max(r["max"] for r in rows),
-                    reasons=reasons, samples=len(rows), samples_under_load=len([r for r in rows if r["util"] >= 50]),
-                    window="every timed region of this run")
+        with open(self.path) as f:
+            return summarize_clocks(f)
+
+
+def summarize_clocks(lines):
+    """nvidia-smi samples (index, sm MHz, max sm MHz, power, utilisation %, active reasons,
+    then the four reason flags) -> median SM clock over the samples under load (utilisation
+    >= 50 %, or all samples if none is), the highest max clock, every throttle reason active
+    in any sample of the window (and, apart, those active under load). None without a
+    parseable sample."""
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            rows.append(dict(sm=float(parts[1]), max=float(parts[2]), util=float(parts[4]),
+                             flags=dict(zip(REASON_FIELDS, [x.lower() == "active" for x in parts[6:10]]))))
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    busy = [r for r in rows if r["util"] >= 50] or rows
+    reasons = sorted({k for r in rows for k, v in r["flags"].items() if v})
+    under_load = sorted({k for r in busy for k, v in r["flags"].items() if v})
+    return dict(sm_mhz=statistics.median(r["sm"] for r in busy), sm_max_mhz=max(r["max"] for r in rows),
+                reasons=reasons, reasons_under_load=under_load, samples=len(rows),
+                samples_under_load=len([r for r in rows if r["util"] >= 50]), window="every timed region of this run")
 
 
 # --------------------------------------------------------------------------------------
