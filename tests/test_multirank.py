@@ -78,25 +78,3 @@ def test_reference_arm_prints_the_contract_line():
     assert line["e2e"] == {"value": line["value"], "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
 
-
-def test_clock_summary_uses_samples_under_load():
-    sys.path.insert(0, ROOT)
-    import bench
-    lines = [
-        "0, 1980, 2070, 300.0, 0, 0x0, Not Active, Not Active, Not Active, Not Active",     # idle
-        "0, 2070, 2070, 1350.5, 100, 0x4, Not Active, Not Active, Not Active, Active",     # power cap
-        "0, 1995, 2070, 1390.0, 98, 0x4, Not Active, Not Active, Not Active, Active",
-        "0, 2040, 2070, 1200.0, 97, 0x0, Not Active, Not Active, Not Active, Not Active",
-        "garbage line",
-        "0, [N/A], 2070, 0, 0, 0x0, Not Active, Not Active, Not Active, Not Active",        # unparseable
-    ]
-    c = bench.summarize_clocks(lines)
-    assert c["sm_mhz"] == 2040 and c["sm_max_mhz"] == 2070
-    assert c["reasons"] == ["sw_power_cap"]
-    assert c["samples"] == 4 and c["samples_under_load"] == 3
-    # a slowdown in any sample of the window is reported, even one taken at low utilisation
-    idle_slow = ["0, 900, 2070, 100, 0, 0x8, Active, Not Active, Not Active, Not Active"] + lines[1:4]
-    c = bench.summarize_clocks(idle_slow)
-    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"] and c["reasons_under_load"] == ["sw_power_cap"]
-    assert c["sm_mhz"] == 2040
-    assert bench.summarize_clocks(["header only"]) is None
