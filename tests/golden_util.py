@@ -3,8 +3,8 @@
 A fixture names its source in '#' lines, shows the arithmetic that gives each expected
 value, then lists one item per line:
 
-  form    dense_e4m3 | dense_e2m1 | masked_e4m3 | contiguous_e4m3 | wgrad_fp32 |
-          k_grouped_fp32 | pack_sf
+  form    dense_e4m3 | dense_e2m1 | masked_e4m3 | masked_e2m1 | contiguous_e4m3 |
+          contiguous_e2m1 | wgrad_fp32 | k_grouped_fp32 | pack_sf   (e2m1: B in FP4)
   shape   dense, wgrad: M N K;  masked: G max_m N K;  contiguous: G M_total N K;
           k_grouped: M N (with "ks");  pack_sf: mn kgroups
   layout  nt | nn | tn | tt (dense_e4m3), nt | nn (contiguous_e4m3), nt | tn (k_grouped_fp32);
@@ -16,7 +16,8 @@ value, then lists one item per line:
   sfa IDX E...    UE8M0 codes of one row of A, one per 128-wide K-group, from the first
                   (codes and rows not listed: 127)
   sfb IDX E...    E4M3 B: one 128-row block of B ("j" or "g,j"), one code per K-group;
-                  E2M1 B: one row of B ("n"), one code per 32-wide K-block (not listed: 127)
+                  E2M1 B: one row of B ("n" or "g,n"), one code per 32-wide K-block
+                  (not listed: 127)
   c  IDX N VALUE  one entry of C (IDX "r", or "g,r" for k_grouped); entries not listed are 0
   masked_m COUNTS / m_indices VALUE*COUNT ...
   d  IDX N EXACT OUT   one entry of D (IDX "r" or "g,r"): its exact value, and that value
@@ -111,12 +112,12 @@ def load(name: str) -> Golden:
             words[int(q), int(i)] = int(h, 16)
         return Golden(name, form, None, sf=sf, words=words)
 
-    fp4 = form == "dense_e2m1"
+    fp4 = form.endswith("_e2m1")
     ks = None
     if form in ("dense_e4m3", "dense_e2m1", "wgrad_fp32"):
         M, N, K = shape
         G, rows = 1, M
-    elif form in ("masked_e4m3", "contiguous_e4m3"):
+    elif form.startswith(("masked_", "contiguous_")):
         G, rows, N, K = shape
     elif form == "k_grouped_fp32":
         rows, N = shape
@@ -125,8 +126,8 @@ def load(name: str) -> Golden:
     else:
         raise ValueError(form)
     KG, NB = K // 128, -(-N // 128)
-    grouped_a = form == "masked_e4m3"
-    grouped_b = form in ("masked_e4m3", "contiguous_e4m3")
+    grouped_a = form.startswith("masked_")
+    grouped_b = form.startswith(("masked_", "contiguous_"))
     a = np.zeros((G, rows, K) if grouped_a else (rows, K), np.uint8)
     b = np.zeros((G, N, K) if grouped_b else (N, K), np.uint8)
     ea = np.full((G, rows, KG) if grouped_a else (rows, KG), 127, np.uint8)
@@ -144,20 +145,21 @@ def load(name: str) -> Golden:
         assert (b < 16).all(), "E2M1 codes are nibbles"
 
     f32_out = form in ("wgrad_fp32", "k_grouped_fp32")
-    dshape = (G, rows, N) if form in ("masked_e4m3", "k_grouped_fp32") else (rows, N)
+    dshape = (G, rows, N) if grouped_a or form == "k_grouped_fp32" else (rows, N)
     cv = None
     if "c" in items:
         cv = np.zeros(dshape, np.float32)
         for tok, n, v in items["c"]:
             cv[_idx(tok) + (int(n),)] = _f32(number(v))
     valid = None
-    if form == "masked_e4m3":
+    b_dev, b_format = (W.pack_fp4(b), "e2m1") if fp4 else (b, "e4m3")
+    if grouped_a:
         counts = np.array([int(v) for v in items["masked_m"][0]], np.int32)
         valid = np.zeros((G, rows), bool)
         for g in range(G):
             valid[g, :min(max(int(counts[g]), 0), rows)] = True
-        p = W.Masked(a, _pack_grouped(ea), b, _pack_grouped(eb), counts, G, rows, N, K)
-    elif form == "contiguous_e4m3":
+        p = W.Masked(a, _pack_grouped(ea), b_dev, _pack_grouped(eb), counts, G, rows, N, K, b_format=b_format)
+    elif form.startswith("contiguous_"):
         idx: List[int] = []
         for t in items["m_indices"][0]:
             v, _, n = t.partition("*")
@@ -165,7 +167,7 @@ def load(name: str) -> Golden:
         assert len(idx) == rows
         m_indices = np.array(idx, np.int32)
         valid = m_indices >= 0
-        p = W.Contiguous(a, W.pack_sf(ea), b, _pack_grouped(eb), m_indices, rows, N, K, G)
+        p = W.Contiguous(a, W.pack_sf(ea), b_dev, _pack_grouped(eb), m_indices, rows, N, K, G, b_format=b_format)
     elif form == "wgrad_fp32":
         p = W.Wgrad(a, W.pack_sf(ea), b, W.pack_sf(eb), cv, rows, N, K)
     elif form == "k_grouped_fp32":
@@ -230,6 +232,11 @@ def oracle_result(O_, g: Golden):
         return O_.k_grouped_fp8_gemm_tn_contiguous(a, p.sfa, b, p.sfb, p.c, p.ks, p.M, p.N), None
     if g.form == "k_grouped_fp32":
         return O_.k_grouped_wgrad_gemm_fp8_fp8_fp32_nt(p.a, p.sfa, p.b, p.sfb, p.c, p.ks, p.M, p.N), None
+    if g.form == "masked_e2m1":
+        return O_.m_grouped_fp8_fp4_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, p.masked_m, p.G, p.max_m, p.N, p.K)
+    if g.form == "contiguous_e2m1":
+        return O_.m_grouped_fp8_fp4_gemm_nt_contiguous(p.a, p.sfa, p.b, p.sfb, p.m_indices, p.M_total, p.N, p.K,
+                                                       p.G)
     if g.form == "masked_e4m3":
         return O_.m_grouped_fp8_gemm_nt_masked(p.a, p.sfa, p.b, p.sfb, p.masked_m, p.G, p.max_m, p.N, p.K)
     if g.form == "contiguous_e4m3" and g.layout == "nn":

@@ -21,7 +21,8 @@ from golden_util import all_fixtures, check_oracle, load, stored
 
 GEMM_FIXTURES = [n for n in all_fixtures() if not n.startswith("pack_sf")]
 PACK_FIXTURES = [n for n in all_fixtures() if n.startswith("pack_sf")]
-FORMS = {"dense_e4m3", "dense_e2m1", "masked_e4m3", "contiguous_e4m3", "wgrad_fp32", "k_grouped_fp32"}
+FORMS = {"dense_e4m3", "dense_e2m1", "masked_e4m3", "masked_e2m1", "contiguous_e4m3", "contiguous_e2m1",
+         "wgrad_fp32", "k_grouped_fp32"}
 
 
 def test_fixtures_cover_every_form():
@@ -104,8 +105,9 @@ def _run_library(lib, g):
         getattr(lib, f"dg_fp8_gemm_{g.layout}")(dev(a), dev(p.sfa), dev(b), dev(p.sfb), c, d)
         torch.cuda.synchronize()
         return d
-    run = {"dense_e4m3": run_dense, "dense_e2m1": run_dense, "masked_e4m3": run_masked,
-           "contiguous_e4m3": run_contiguous, "wgrad_fp32": run_wgrad, "k_grouped_fp32": run_k_grouped}
+    run = {"dense_e4m3": run_dense, "dense_e2m1": run_dense, "masked_e4m3": run_masked, "masked_e2m1": run_masked,
+           "contiguous_e4m3": run_contiguous, "contiguous_e2m1": run_contiguous, "wgrad_fp32": run_wgrad,
+           "k_grouped_fp32": run_k_grouped}
     return run[g.form](lib, p)
 
 
