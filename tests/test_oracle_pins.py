@@ -509,11 +509,62 @@ def pin_golden(O_):
             check_oracle(O_, g)
 
 
+def pin_parity_report(O_):
+    """The comparator every GPU parity check goes through, on hand-worked cases: each
+    expected verdict follows from the bound |d - ref| <= rel*|ref| + abs_rms*rms(ref) (rms
+    over ref) and the strict cosine-style bar, computed here by hand."""
+    pr = O_.parity_report
+    # ref = [1, 7]: rms = sqrt((1 + 49) / 2) = 5, so element 0's bound is 0.01 + 0.05 = 0.06
+    r = pr(np.array([1.0595, 7.0]), np.array([1.0, 7.0]))
+    assert r["ok"] and r["n_bad"] == 0 and r["n"] == 2 and r["rms"] == 5.0, r
+    r = pr(np.array([1.0605, 7.0]), np.array([1.0, 7.0]))
+    assert not r["ok"] and r["n_bad"] == 1, r
+    # the relative part uses |ref|: for ref = -1 the bound is still 0.06
+    r = pr(np.array([-1.0595, 7.0]), np.array([-1.0, 7.0]))
+    assert r["ok"] and r["n_bad"] == 0, r
+    # rms is over ref, not d. ref = [100, 0]: rms = 70.7107, element 1's bound 0.707107.
+    # d = [101.7, 0.71] fails there (rms(d) would be 71.91, a bound of 0.719, and pass);
+    # d = [98.3, 0.7] passes both elements (1.7 <= 1.70711, 0.7 <= 0.70711; rms(d) = 69.51
+    # would fail element 1); both cosine-style differences are ~1.7e-4
+    r = pr(np.array([101.7, 0.71]), np.array([100.0, 0.0]))
+    assert not r["ok"] and r["n_bad"] == 1, r
+    r = pr(np.array([98.3, 0.7]), np.array([100.0, 0.0]))
+    assert r["ok"] and r["n_bad"] == 0, r
+    # rel multiplies |ref|, abs_rms multiplies rms: with rel = 0.02, abs_rms = 0.005 and
+    # ref = [1, 7] the bounds are 0.045 and 0.165 (swapped roles would give 0.105, 0.135)
+    r = pr(np.array([1.08, 7.0]), np.array([1.0, 7.0]), rel=0.02, abs_rms=0.005)
+    assert not r["ok"] and r["n_bad"] == 1, r
+    r = pr(np.array([1.0, 7.15]), np.array([1.0, 7.0]), rel=0.02, abs_rms=0.005)
+    assert r["ok"] and r["n_bad"] == 0, r
+    # an element exactly at its bound passes: rel = abs_rms = 2^-7 gives the exact bounds
+    # 6 * 2^-7 and 12 * 2^-7 for ref = [1, 7]
+    r = pr(np.array([1.0 + 6 / 128, 7.0 - 12 / 128]), np.array([1.0, 7.0]), rel=2.0 ** -7, abs_rms=2.0 ** -7)
+    assert r["n_bad"] == 0 and r["ok"], r
+    # cosine-style difference: d = 1 + (e, -e, e, -e) against ref = 1 gives exactly
+    # e^2 / (2 + e^2); rel = 0, abs_rms = 1 keeps every element inside its bound (1)
+    ones = np.ones(4)
+    for e, ok in ((0.0447, True), (0.0448, False)):
+        r = pr(ones + e * np.array([1.0, -1.0, 1.0, -1.0]), ones, rel=0.0, abs_rms=1.0)
+        assert abs(r["diff"] - e * e / (2 + e * e)) < 1e-15 and r["ok"] == ok and r["n_bad"] == 0, (e, r)
+    # the bar is strict: d = (1, 1, 1, 1), ref = (1, 1, 1, -1) give 2*2/8 = 0.5, difference 0.5
+    r = pr(np.ones(4), np.array([1.0, 1.0, 1.0, -1.0]), rel=0.0, abs_rms=10.0, cos_max=0.5)
+    assert r["diff"] == 0.5 and r["n_bad"] == 0 and not r["ok"], r
+    r = pr(np.ones(4), np.array([1.0, 1.0, 1.0, -1.0]), rel=0.0, abs_rms=10.0, cos_max=0.5 + 2.0 ** -20)
+    assert r["ok"], r
+    # a NaN in d fails its element (and the difference)
+    r = pr(np.array([np.nan, 7.0]), np.array([1.0, 7.0]))
+    assert not r["ok"] and r["n_bad"] == 1, r
+    # nothing to compare: reported ok with n = 0
+    r = pr(np.zeros(0), np.zeros(0))
+    assert r["ok"] and r["n"] == 0 and r["n_bad"] == 0, r
+
+
 PINS = [pin_e4m3_table, pin_ue8m0_table, pin_bf16, pin_unpack, pin_brute_force, pin_identity,
         pin_one_hot, pin_pow2_invariance, pin_c_only, pin_dequantised_route,
         pin_contiguous_equals_dense, pin_masked_equals_dense, pin_wgrad_brute_force, pin_wgrad_c_only,
         pin_k_grouped_equals_per_expert, pin_layouts, pin_grouped_layouts, pin_e2m1_table, pin_fp4_brute_force,
-        pin_fp4_one_hot, pin_fp4_matches_fp8_route, pin_fp4_grouped_equals_dense, pin_golden]
+        pin_fp4_one_hot, pin_fp4_matches_fp8_route, pin_fp4_grouped_equals_dense, pin_golden,
+        pin_parity_report]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -738,6 +789,38 @@ def _make_scaled_fp4(mode):
     return factory
 
 
+def _make_parity(mode):
+    """Copies of the comparator with one planted mistake each."""
+    def factory(old):
+        def f(d, ref, rel=1e-2, abs_rms=1e-2, cos_max=1e-3):
+            d = np.asarray(d, np.float64)
+            ref = np.asarray(ref, np.float64)
+            over = d if mode == "rms_over_d" else ref
+            rms = float(np.sqrt(np.mean(over * over))) if ref.size else 0.0
+            err = np.abs(d - ref)
+            if mode == "rel_abs_swapped":
+                bound = abs_rms * np.abs(ref) + rel * rms
+            elif mode == "signed_ref":
+                bound = rel * ref + abs_rms * rms
+            else:
+                bound = rel * np.abs(ref) + abs_rms * rms
+            if mode == "nan_passes":
+                bad = err > bound
+            elif mode == "strict_bound":
+                bad = ~(err < bound)
+            else:
+                bad = ~(err <= bound)
+            denom = float((d * d).sum() + (ref * ref).sum())
+            diff = 0.0 if denom == 0.0 else 1.0 - 2.0 * float((d * ref).sum()) / denom
+            if mode == "diff_sign_flipped":
+                diff = -diff
+            ok_cos = diff <= cos_max if mode == "cos_not_strict" else diff < cos_max
+            return dict(n=int(ref.size), n_bad=int(bad.sum()), max_err=float(err.max()) if ref.size else 0.0,
+                        rms=rms, diff=diff, ok=bool(not bad.any() and ok_cos))
+        return f
+    return factory
+
+
 MUTANTS = {
     "subnormal_implicit_one": _mut_table(_subnormal_with_implicit_one),
     "sign_ignored": _mut_table(lambda t: np.abs(t)),
@@ -764,6 +847,13 @@ MUTANTS = {
     "fp4_high_nibble_first": _mut_attr("unpack_e2m1", _fp4_high_nibble_first),
     "fp4_b_scale_per_128": _mut_attr("_scaled_gemm_fp4", _make_scaled_fp4("b_scale_per_128")),
     "fp4_a_scale_per_32": _mut_attr("_scaled_gemm_fp4", _make_scaled_fp4("a_scale_per_32")),
+    "parity_rms_over_d": _mut_attr("parity_report", _make_parity("rms_over_d")),
+    "parity_rel_abs_swapped": _mut_attr("parity_report", _make_parity("rel_abs_swapped")),
+    "parity_signed_ref": _mut_attr("parity_report", _make_parity("signed_ref")),
+    "parity_nan_passes": _mut_attr("parity_report", _make_parity("nan_passes")),
+    "parity_strict_bound": _mut_attr("parity_report", _make_parity("strict_bound")),
+    "parity_diff_sign_flipped": _mut_attr("parity_report", _make_parity("diff_sign_flipped")),
+    "parity_cos_not_strict": _mut_attr("parity_report", _make_parity("cos_not_strict")),
 }
 
 
