@@ -48,6 +48,8 @@ SIGNATURES = [
     ("dg_get_theoretical_mk_alignment_for_contiguous_layout", _I, []),
     ("dg_get_tma_aligned_size", _I, [_I, _I]),
     ("dg_set_num_sms", _I, [_I]),
+    ("dg_set_pdl", _I, [_I]),
+    ("dg_get_pdl", _I, []),
     ("dg_get_num_sms", _I, []),
     ("dg_get_device_status", _I, [_P]),
     ("dg_status_string", ctypes.c_char_p, [_I]),
@@ -409,6 +411,15 @@ def dg_set_num_sms(n: int) -> None:
 
 def dg_get_num_sms() -> int:
     return load_library().dg_get_num_sms()
+
+
+def dg_set_pdl(enable: bool) -> None:
+    """Programmatic dependent launch on (True) or off (False) for later launches."""
+    _check("dg_set_pdl", load_library().dg_set_pdl(1 if enable else 0))
+
+
+def dg_get_pdl() -> bool:
+    return bool(load_library().dg_get_pdl())
 
 
 def dg_get_device_status(stream=None) -> int:

@@ -13,6 +13,7 @@
 #include <mutex>
 #include <vector>
 
+#include "debug_state.h"
 #include "dg.h"
 #include "fp8_gemm.cuh"
 #include "fp8_gemm_pair.cuh"
@@ -141,12 +142,21 @@ dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, W
 // ------------------------------------------------------------------------------------
 // TMA descriptors
 // ------------------------------------------------------------------------------------
-// Programmatic dependent launch (DG_PDL=0 disables): a GEMM may start its prologue while the
-// previous kernel in the stream finishes; the kernels wait for that grid before touching
-// global memory.
+// Programmatic dependent launch: a GEMM may start its prologue while the previous kernel in
+// the stream finishes; the kernels wait for that grid before touching global memory. On by
+// default (the environment variable DG_PDL=0 makes the default off); dg_set_pdl changes it.
+// -1: not yet initialised from the environment.
+std::atomic<int> g_pdl{-1};
+
 bool pdl_enabled() {
-  const char* f = std::getenv("DG_PDL");
-  return !(f && f[0] == '0');
+  int v = g_pdl.load();
+  if (v < 0) {
+    const char* f = std::getenv("DG_PDL");
+    int expected = -1;
+    g_pdl.compare_exchange_strong(expected, (f && f[0] == '0') ? 0 : 1);
+    v = g_pdl.load();
+  }
+  return v != 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -922,6 +932,11 @@ dg_status run_dense_single(DeviceState& dsr, const void* a, const int32_t* sfa, 
 
 }  // namespace
 
+namespace dg {
+int debug_fault_mode() { return g_fault.load(); }
+unsigned long long pipeline_wait_timeout_ns() { return wait_timeout_ns(); }
+}  // namespace dg
+
 // ======================================================================================
 // C ABI
 // ======================================================================================
@@ -1341,6 +1356,14 @@ const char* dg_status_string(dg_status s) {
 }
 
 int dg_last_cuda_error(void) { return g_last_cuda_error; }
+
+dg_status dg_set_pdl(int enable) {
+  if (enable != 0 && enable != 1) return DG_ERR_INVALID_ARG;
+  g_pdl.store(enable);
+  return DG_OK;
+}
+
+int dg_get_pdl(void) { return pdl_enabled() ? 1 : 0; }
 
 dg_status dg_set_debug(int fault_mode, unsigned long long wait_timeout_ns) {
   if (fault_mode < 0 || fault_mode > dg::kFaultProducerSilent) return DG_ERR_INVALID_ARG;

@@ -262,29 +262,33 @@ dg_status dg_pack_sf_ue8m0(const float* sf_fp32, int32_t* out, int mn, int kgrou
  * Dense GEMM that allocates no device memory (the pages have no counterpart: this is an
  * extra entry point of this library).
  *
- * For callers that cannot allocate when they run the GEMM: code being captured into a
- * CUDA graph, servers that fix their device-memory footprint at start-up, or a custom
- * allocator that owns all device memory. dg_fp8_gemm_nt allocates on first use (a status
- * word, and a per-stream workspace for stream-K and the CTA-pair kernel); this
- * entry point uses instead a fixed 16 MiB scratch array that the library holds in device
- * memory from the first call on each GPU until the process exits.
+ * For callers that cannot allocate when they run the GEMM: servers that fix their
+ * device-memory footprint at start-up and forbid later allocations, custom allocators that
+ * own all of the device's memory, code under a memory budget where a lazy allocation could
+ * fail in the middle of a step, or latency-critical loops that cannot afford the implicit
+ * device synchronisation of cudaMalloc / cudaFree. dg_fp8_gemm_nt allocates on first use (a
+ * status word, and for some shapes a per-stream workspace); this entry point uses instead a
+ * fixed 16 MiB scratch array that the library holds in device memory from the first call on
+ * each GPU until the process exits.
  *
  * Computes the same D = C + A @ B.T as dg_fp8_gemm_nt, with the same argument meanings and
- * layouts, through the same kernel in its stream-K mode (the K-groups of all 128x128 tiles
- * shared among the SMs), so results match dg_fp8_gemm_nt within the parity tolerance.
+ * layouts, on the library's single-CTA kernel in stream-K mode (128 x 128 tiles, one K-group
+ * per pipeline stage, the K-groups of all tiles split among every SM of the device;
+ * dg_set_num_sms does not apply), so results match dg_fp8_gemm_nt within the parity
+ * tolerance. dg_set_debug's fault mode and wait limit apply to it as to every GEMM.
  *   status : caller-owned DEVICE uint32 word (4-byte aligned); device-side errors are OR-ed
  *            into it as bit (1 << DG_ERR_TIMEOUT). It is not cleared by the call.
  * Limits: the problem must fit the scratch: 16 KiB of counters (at most 1024 tiles of
- * 128x128) plus tiles x contributors-per-tile x 64 KiB of FP32 partials (the 128x7168
- * decode shape uses about 14.7 MiB). Larger problems return DG_ERR_INVALID_ARG with nothing
- * launched; use dg_fp8_gemm_nt for them.
- * The first call on a device looks up the scratch array's device address (once per device,
- * with that device current); make that first call before any stream capture. Every call
- * shares the one array and it keeps the previous call's contents: each call clears the
- * counters it needs (an asynchronous memset on `stream`) before its kernel. Calls whose work
- * overlaps on the GPU (different streams, or several host threads) race on the array: keep
- * them ordered on one stream.
- * Calls no cudaMalloc / cudaFree and no allocating library routine.
+ * 128x128) plus tiles x (largest contributor count of any tile) x 64 KiB of FP32 partials,
+ * a conservative bound (the 128x7168x16384 decode shape needs 14.0 MiB of partials). Larger
+ * problems return DG_ERR_INVALID_ARG with nothing launched; use dg_fp8_gemm_nt for them.
+ * The first call on a device does its set-up: it looks up the scratch array's device
+ * address and sets the kernels' shared-memory limit (once per device, with that device
+ * current); make that first call before any stream capture. Every call shares the one array
+ * and it keeps the previous call's contents: each call clears the counters it needs (an
+ * asynchronous memset on `stream`) before its kernel. Calls whose work overlaps on the GPU
+ * (different streams, or several host threads) race on the array: keep them ordered on one
+ * stream. Calls no cudaMalloc / cudaFree and no allocating library routine.
  */
 dg_status dg_fp8_gemm_nt_no_alloc(const void* a, const int32_t* sfa,
                                   const void* b, const int32_t* sfb,
@@ -311,6 +315,19 @@ int dg_get_tma_aligned_size(int mn, int elem_bytes);
  * exceeds the device's SM count. */
 dg_status dg_set_num_sms(int n);
 int dg_get_num_sms(void);
+
+/* Programmatic dependent launch ("Utilities": set_pdl / get_pdl). When on, every GEMM
+ * launch of the library (and the CTA-pair path's scale-preparation kernel) may begin its
+ * prologue (barrier set-up, TMEM allocation, descriptor prefetch, an L2 prefetch of its first
+ * operand boxes) while the preceding kernel in the stream is still running; each kernel
+ * waits for that kernel's completion (griddepcontrol.wait) before it reads or writes any
+ * global memory the preceding kernel may touch, so results do not depend on the setting.
+ * On by default; the environment variable DG_PDL=0 makes the default off. dg_set_pdl takes
+ * 1 (on) or 0 (off) and returns DG_ERR_INVALID_ARG for anything else; process-wide, for
+ * launches made after the call. dg_get_pdl returns the current setting (1 or 0).
+ * dg_fp8_gemm_nt_no_alloc launches without it. Host-only: no device is touched. */
+dg_status dg_set_pdl(int enable);
+int dg_get_pdl(void);
 
 /* Synchronises `stream`, then returns (and clears) the first error recorded on the
  * current device by any earlier call: DG_ERR_TIMEOUT, DG_ERR_BAD_INDEX, or DG_OK. */

@@ -96,6 +96,19 @@ def test_mk_alignment_setter(lib):
     assert lib.dg_get_mk_alignment_for_contiguous_layout() == 128
 
 
+def test_pdl_setter(lib):
+    # host-only: the setting is process-wide and touches no device
+    before = lib.dg_get_pdl()
+    try:
+        assert lib.dg_set_pdl(0) == 0 and lib.dg_get_pdl() == 0
+        assert lib.dg_set_pdl(1) == 0 and lib.dg_get_pdl() == 1
+        for bad in (-1, 2, 7):
+            assert lib.dg_set_pdl(bad) == 1        # DG_ERR_INVALID_ARG, setting unchanged
+            assert lib.dg_get_pdl() == 1
+    finally:
+        lib.dg_set_pdl(before)
+
+
 def test_weight_gradient_forms_reject_bad_arguments(lib):
     P = ctypes.c_void_p
     x = P(0x10000)
