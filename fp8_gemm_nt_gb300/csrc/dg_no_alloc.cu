@@ -1,18 +1,20 @@
 // dg_fp8_gemm_nt_no_alloc: the dense GEMM for callers that must not allocate device memory.
 //
-// Some callers cannot call cudaMalloc at the moment they need a GEMM: a region that is
-// being captured into a CUDA graph (allocation there is not permitted or not replayable),
-// an inference server that fixes its memory footprint at start-up and forbids later
-// allocations, a custom allocator that owns all device memory, or code running under a
-// memory budget where a lazy allocation could fail mid-flight. The regular entry point
-// dg_fp8_gemm_nt allocates on first use (its status word and the stream-K workspace).
-// This entry point allocates nothing: the stream-K scratch (arrival counters and FP32
-// partial tiles) lives in the file-scope device array below, and device-side errors go to
-// a status word the caller passes.
+// Some callers cannot call cudaMalloc at the moment they need a GEMM: an inference server
+// that fixes its device-memory footprint at start-up and forbids later allocations, a
+// custom allocator that owns all of the device's memory, code running under a memory budget
+// where a lazy allocation could fail in the middle of a step, or a latency-critical loop
+// that cannot afford the implicit device synchronisation a cudaMalloc / cudaFree may bring.
+// The regular entry point dg_fp8_gemm_nt allocates on first use (its status word and, for
+// some shapes, a per-stream workspace). This entry point allocates nothing: the stream-K
+// scratch (arrival counters and FP32 partial tiles) lives in the file-scope device array
+// below, and device-side errors go to a status word the caller passes.
 //
-// It runs the same kernel as dg_fp8_gemm_nt's stream-K mode (128 x 128 tiles whose
-// K-groups are shared among the SMs, partial tiles summed in a fixed order by the last
-// contributor), so its results match dg_fp8_gemm_nt within the parity tolerance.
+// It runs the single-CTA kernel of this library in stream-K mode with one K-group per
+// pipeline stage and 128 x 128 tiles, on every SM of the device (dg_set_num_sms does not
+// apply): the K-groups of all tiles are split evenly among the CTAs, and a tile split
+// between CTAs is summed in a fixed order by its last contributor. Its results therefore
+// match dg_fp8_gemm_nt within the parity tolerance (the summation order may differ).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -21,6 +23,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "debug_state.h"
 #include "dg.h"
 #include "fp8_gemm.cuh"
 
@@ -33,9 +36,15 @@ constexpr size_t kCounterInts = 4096;                 // first 16 KiB: arrival c
 constexpr int kBN = 128;                              // tile width of the stream-K kernel
 constexpr int kEpiWarps = 4;
 constexpr int kMaxDevices = 64;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[kScratchBytes];
+
+// The kernel this entry point launches (stream-K, 128-wide tiles, 5 stages, two accumulators).
+using Cfg = dg::Config<kBN, 5, 2, kEpiWarps, 2>;
+template <bool kHasC>
+constexpr auto kernel() {
+  return dg::fp8_gemm_kernel<dg::Kind::Dense, kBN, 5, 2, kEpiWarps, 2, kHasC>;
+}
 
 struct DeviceSetup {
   bool done = false;
@@ -65,6 +74,12 @@ dg_status setup_device(DeviceSetup** out) {
       void* ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_no_alloc_scratch) != cudaSuccess || ptr == nullptr) return DG_ERR_CUDA;
       s.scratch = static_cast<unsigned char*>(ptr);
+      // the kernels' dynamic shared-memory limit, once per device (not on every call)
+      if (cudaFuncSetAttribute(kernel<true>(), cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(kernel<false>(), cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+              cudaSuccess)
+        return DG_ERR_CUDA;
     }
     s.done = true;
   }
@@ -101,14 +116,11 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t i
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// (the shared-memory attribute was set by setup_device for this device)
 template <bool kHasC>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                    const CUtensorMap& td, const dg::Params& p, int grid, cudaStream_t stream) {
-  using Cfg = dg::Config<kBN, 5, 2, kEpiWarps, 2>;
-  auto kern = dg::fp8_gemm_kernel<dg::Kind::Dense, kBN, 5, 2, kEpiWarps, 2, kHasC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, td, p);
+  kernel<kHasC>()<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, td, p);
   return cudaGetLastError();
 }
 
@@ -127,7 +139,9 @@ extern "C" dg_status dg_fp8_gemm_nt_no_alloc(const void* a, const int32_t* sfa, 
   if (dg_status s = setup_device(&ds); s != DG_OK) return s;
 
   // Partition of the K-groups of all 128 x 128 tiles among the SMs (stream-K), and the
-  // scratch it needs: counters for every tile, one FP32 partial tile per contributor.
+  // scratch it needs: counters for every tile, and room for one FP32 partial tile per
+  // contributor slot of every tile (the largest contributor count of any tile, for all
+  // tiles: a conservative bound, as a tile that one CTA computes whole writes no partial).
   const int num_kb = K / 128;
   const long long tiles = static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, kBN);
   const long long kgroups = tiles * num_kb;
@@ -166,7 +180,8 @@ extern "C" dg_status dg_fp8_gemm_nt_no_alloc(const void* a, const int32_t* sfa, 
   p.c = static_cast<const __nv_bfloat16*>(c);
   p.d = static_cast<__nv_bfloat16*>(d);
   p.status = status;
-  p.timeout_ns = kTimeoutNs;
+  p.timeout_ns = dg::pipeline_wait_timeout_ns();
+  p.fault = dg::debug_fault_mode();
   p.sk_ctas = static_cast<int>(ctas);
   p.sk_slots = slots;
   p.sk_counters = counters;
