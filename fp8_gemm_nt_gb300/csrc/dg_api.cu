@@ -436,17 +436,20 @@ dg_status launch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const 
 }
 constexpr int kEpilogueWarps = 4;
 
-// CTA-pair configurations: 256 x BN tiles over two SMs, 5-stage ring per CTA; BN = 256
-// with one accumulator, BN = 240 or 192 with two.
-constexpr int kPairStages = 5;
+// CTA-pair configurations: 256 x BN tiles over two SMs; BN = 256 with one accumulator, BN = 240
+// or 192 with two. Ring: 6 stages per CTA for BF16 output without C (32-column epilogue pieces
+// leave the shared memory for it), 5 otherwise.
+template <bool kHasC, bool kOutF32>
+constexpr int pair_stages() { return (!kHasC && !kOutF32) ? 6 : 5; }
 
 template <dg::Kind kKind, bool kHasC, int kBN, bool kOutF32 = false, bool kBF4 = false, bool kAMN = false,
           bool kBMN = false>
 struct PairLauncher {
   static constexpr int kNumAccum = kBN == 256 ? 1 : 2;
-  using Cfg = dg::PairConfig<kPairStages, kBN, kNumAccum, kBF4>;
+  static constexpr int kStages = pair_stages<kHasC, kOutF32>();
+  using Cfg = dg::PairConfig<kStages, kBN, kNumAccum, kBF4, !kHasC && !kOutF32>;
   static constexpr auto kernel() {
-    return dg::fp8_gemm_pair_kernel<kKind, kPairStages, kBN, kNumAccum, kHasC, kOutF32, kBF4, kAMN, kBMN>;
+    return dg::fp8_gemm_pair_kernel<kKind, kStages, kBN, kNumAccum, kHasC, kOutF32, kBF4, kAMN, kBMN>;
   }
 
   // Largest number of co-resident CTA pairs (0 if the device cannot run the kernel).
@@ -500,7 +503,7 @@ struct PairLauncher {
     if (e != cudaSuccess) return cuda_fail(e);
     if (std::getenv("DG_PRINT_CONFIGS"))
       std::fprintf(stderr, "[dg] kind=%d M=%d N=%d K=%d G=%d pair 256x%d accum=%d stages=%d clusters=%d smem=%d fp4=%d\n",
-                   static_cast<int>(kKind), p.M, p.N, p.K, p.G, kBN, kNumAccum, kPairStages, clusters,
+                   static_cast<int>(kKind), p.M, p.N, p.K, p.G, kBN, kNumAccum, kStages, clusters,
                    Cfg::SMEM_BYTES, kBF4 ? 1 : 0);
     return DG_OK;
   }
@@ -579,6 +582,15 @@ bool map_out(CUtensorMap* m, void* base, int G, int rows, int N) {
   const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(N) * 2 * rows};
   const uint32_t box[3] = {64, 32, 1};
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output D (BF16) in 32-row x 32-column pieces (64-byte rows, 64-byte swizzle): the CTA-pair
+// kernel's epilogue for BF16 output without C.
+bool map_out_pieces(CUtensorMap* m, void* base, int rows, int N) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(N) * 2};
+  const uint32_t box[2] = {32, 32};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // MN-major operand ("t" A given as [K, M], "n" B given as [K, N]): boxes of 128 K-rows x 128
@@ -712,9 +724,12 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
   }
 
   CUtensorMap ta, tb, tsa, tsb, td, td_tail, tc;
+  // BF16 output without C: 32-column pieces (see PairConfig::kSmallEpi)
+  constexpr bool kSmallEpi = !kHasC && !kOutF32;
   bool ok = (kAMN ? map_operand_mn(&ta, a, p.M, p.K) : map_operand_2d(&ta, a, p.M, p.K, 128)) &&
             (kKG ? map_out_f32_3d(&td, d, p.G, p.M, p.N)
-                 : kOutF32 ? map_out_f32(&td, d, p.M, p.N) : map_out(&td, d, 0, p.M, p.N));
+                 : kOutF32 ? map_out_f32(&td, d, p.M, p.N)
+                           : kSmallEpi ? map_out_pieces(&td, d, p.M, p.N) : map_out(&td, d, 0, p.M, p.N));
   // C is read by TMA in boxes of the output's geometry (the map of D over C's memory)
   void* c_mem = const_cast<void*>(static_cast<const void*>(p.c));
   if (kHasC)
@@ -722,12 +737,13 @@ dg_status run_pair(DeviceState& ds, const void* a, const int32_t* sfa, const voi
                     : kOutF32 ? map_out_f32(&tc, c_mem, p.M, p.N) : map_out(&tc, c_mem, 0, p.M, p.N));
   else
     tc = td;
-  if constexpr (kBN % 64 != 0) {
+  if constexpr (kSmallEpi ? kBN % 32 != 0 : kBN % 64 != 0) {
     // the narrower end of each tile, 32 rows high, no swizzle: BF16 its last kBN % 64
-    // columns; FP32 its last (kBN % 64) % 32 columns (the rest goes out as 32-column boxes)
+    // columns (kBN % 32 with 32-column pieces); FP32 its last (kBN % 64) % 32 columns (the
+    // rest goes out as 32-column boxes)
     const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(p.N) * (kOutF32 ? 4 : 2)};
-    const uint32_t box[2] = {static_cast<uint32_t>(kOutF32 ? (kBN % 64) % 32 : kBN % 64), 32};
+    const uint32_t box[2] = {static_cast<uint32_t>(kOutF32 ? (kBN % 64) % 32 : kSmallEpi ? kBN % 32 : kBN % 64), 32};
     static_assert(!kOutF32 || (kBN % 64) % 32 != 0, "an FP32 narrow box needs a remainder");
     ok = ok && make_map(&td_tail, kOutF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d,
                         dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);

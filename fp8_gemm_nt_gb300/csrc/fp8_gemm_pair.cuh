@@ -41,8 +41,14 @@ namespace dg {
 // kBF4: B is FP4 (E2M1 with one UE8M0 per row per 32 K), loaded through 16U4_ALIGN16B maps into
 // the same shared-memory shape as E4M3 (the barrier counts half the bytes); every stage then
 // carries scale chunks (A's K-quad chunk and this K-group's B chunks).
-template <int kStages, int kBN, int kNumAccum, bool kBF4 = false>
+// kSmallEpi (BF16 output without C): each epilogue warp stages 32-column pieces in 2 KB
+// (64-byte rows) instead of 64-column chunks in 4 KB, which leaves room for a sixth stage.
+// Measured on GB300, the CTA-pair kernel is bound by the depth of its ring (a stage is
+// refilled only after the MMAs that read it complete and its TMA loads land again): 3 / 4 / 5
+// stages gave 2500 / 2915 / 3200 TFLOPS on the contiguous G=8 workload.
+template <int kStages, int kBN, int kNumAccum, bool kBF4 = false, bool kSmallEpi_ = false>
 struct PairConfig {
+  static constexpr bool kSmallEpi = kSmallEpi_;
   static constexpr int BN = kBN;                 // tile width of the pair; each CTA loads BN/2 B rows
   static_assert(BN % 16 == 0 && BN >= 128 && BN <= 256, "tile width: a multiple of 16 in [128, 256]");
   static constexpr int kChunks = ceil_div_c(BN, 64);   // epilogue chunks of 64 columns (last may be narrower)
@@ -56,8 +62,8 @@ struct PairConfig {
   static constexpr int B_BYTES = (BN / 2) * BLOCK_K;
   static constexpr int SFA_BYTES = 512;          // one tcgen05.cp chunk: this CTA's 128 rows
   static constexpr int SFB_BYTES = 1024;         // two chunks: the 256 columns of the pair tile
-  static constexpr int SF_STRIDE = 2048;
-  static constexpr int EPI_BUF_BYTES = 32 * 128;
+  static constexpr int SF_STRIDE = SFA_BYTES + SFB_BYTES;   // a multiple of 128 (TMA destinations)
+  static constexpr int EPI_BUF_BYTES = kSmallEpi ? 32 * 64 : 32 * 128;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + kStages * A_BYTES;
   static constexpr int OFF_SF = OFF_B + kStages * B_BYTES;
@@ -188,7 +194,7 @@ struct PairScheduler {
 // 32-deep K step, with the instruction descriptor's transpose bits set.
 template <Kind kKind, int kStages, int kBN, int kNumAccum, bool kHasC, bool kOutF32 = false, bool kBF4 = false,
           bool kAMN = false, bool kBMN = false>
-__global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kThreads, 1)
+__global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4, !kHasC && !kOutF32>::kThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                          const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_d_tail,
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
   static_assert(!kBF4 || !kOutF32, "FP4 B: BF16 output");
   static_assert((!kAMN && !kBMN) || (kKind == Kind::Dense && kBN == 256 && !kBF4),
                 "MN-major operands: the dense form with 256-wide tiles");
-  using C = PairConfig<kStages, kBN, kNumAccum, kBF4>;
+  using C = PairConfig<kStages, kBN, kNumAccum, kBF4, !kHasC && !kOutF32>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -594,6 +600,61 @@ __global__ void __launch_bounds__(PairConfig<kStages, kBN, kNumAccum, kBF4>::kTh
                 tma_store_2d(narrow ? &tm_d_tail : &tm_d, sbuf, n0 + hcol, m_blk * BLOCK_M + quad * 32);
               }
               bulk_commit_group();
+            }
+          }
+          continue;
+        }
+        if constexpr (C::kSmallEpi) {
+          // 32-column pieces through the 2 KB staging buffer: 64-byte rows in the 64-byte
+          // swizzle of tm_d (16-byte unit u of row r at r * 64 + (u ^ ((r >> 1) & 3)) * 16);
+          // the 16-column end of a 240-wide tile as plain 32-byte rows (tm_d_tail)
+          const int width = tail ? C::kTail : 64;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int pw = width - 32 * h < 32 ? width - 32 * h : 32;   // columns of this piece
+            if (pw <= 0) break;
+            const int pcol = col + 32 * h;
+            if (lane == 0) bulk_wait_group_read<0>();   // the previous piece's store has read sbuf
+            __syncwarp();
+            const bool narrow = pw < 32;
+            const uint32_t srow = smem_addr(sbuf) + lane * (narrow ? 32 : 64);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (8 * u < pw) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const __nv_bfloat162 b2 =
+                      __floats2bfloat162_rn(f[32 * h + 8 * u + 2 * e], f[32 * h + 8 * u + 2 * e + 1]);
+                  w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                st_shared_v4(srow + (narrow ? u * 16 : (u ^ ((lane >> 1) & 3u)) * 16), w[0], w[1], w[2], w[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (kKind == Kind::Dense || ok_mask == 0xffffffffu) {
+              if (lane == 0) {
+                tma_store_2d(narrow ? &tm_d_tail : &tm_d, sbuf, n0 + pcol, m_blk * BLOCK_M + quad * 32);
+                bulk_commit_group();
+              }
+            } else if (ok_mask != 0) {
+              // only the expert's rows: two rows per pass, 16 lanes x 4 bytes per row
+              const int l = static_cast<int>(lane & 15u);
+              const int gcol = n0 + pcol + 2 * l;
+#pragma unroll 1
+              for (int r0 = 0; r0 < 32; r0 += 2) {
+                const int r = r0 + static_cast<int>(lane >> 4);
+                const long long drow = __shfl_sync(0xffffffffu, d_row, r);
+                if (((ok_mask >> r) & 1u) && 2 * l < pw && gcol < p.N) {
+                  const uint32_t off = narrow ? r * 32 + l * 4
+                                              : r * 64 + ((static_cast<uint32_t>(l) / 4) ^ ((r >> 1) & 3u)) * 16 +
+                                                    (l % 4) * 4;
+                  const uint32_t val = ld_shared_u32(smem_addr(sbuf) + off);
+                  *reinterpret_cast<uint32_t*>(p.d + drow * p.N + gcol) = val;
+                }
+              }
+              __syncwarp();
             }
           }
           continue;
