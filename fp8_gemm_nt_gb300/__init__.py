@@ -48,6 +48,9 @@ SIGNATURES = [
     ("dg_get_theoretical_mk_alignment_for_contiguous_layout", _I, []),
     ("dg_get_tma_aligned_size", _I, [_I, _I]),
     ("dg_set_num_sms", _I, [_I]),
+    ("dg_reserve_workspace", _I, [_P, ctypes.c_size_t]),
+    ("dg_release_workspace", _I, [_P]),
+    ("dg_get_workspace_size", ctypes.c_size_t, [_P]),
     ("dg_set_pdl", _I, [_I]),
     ("dg_get_pdl", _I, []),
     ("dg_get_num_sms", _I, []),
@@ -411,6 +414,19 @@ def dg_set_num_sms(n: int) -> None:
 
 def dg_get_num_sms() -> int:
     return load_library().dg_get_num_sms()
+
+
+def dg_reserve_workspace(nbytes: int, stream=None) -> None:
+    """Reserve (at least nbytes of) the library's workspace for the stream (current by default)."""
+    _check("dg_reserve_workspace", load_library().dg_reserve_workspace(_stream(stream), nbytes))
+
+
+def dg_release_workspace(stream=None) -> None:
+    _check("dg_release_workspace", load_library().dg_release_workspace(_stream(stream)))
+
+
+def dg_get_workspace_size(stream=None) -> int:
+    return int(load_library().dg_get_workspace_size(_stream(stream)))
 
 
 def dg_set_pdl(enable: bool) -> None:

@@ -36,17 +36,21 @@ constexpr size_t kMaxWorkspaces = 16;                           // freeable cach
 // The CUDA runtime calls the workspace cache policy (workspace_cache.h) is written against.
 struct CudaApi {
   using Stream = cudaStream_t;
+  using Event = cudaEvent_t;
   static int is_capturing(Stream s, bool* capturing) {
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
     const cudaError_t e = cudaStreamIsCapturing(s, &st);
     *capturing = st != cudaStreamCaptureStatusNone;
     return static_cast<int>(e);
   }
-  static int device_synchronize() { return static_cast<int>(cudaDeviceSynchronize()); }
-  static int stream_synchronize(Stream s) { return static_cast<int>(cudaStreamSynchronize(s)); }
   static int malloc(void** p, size_t n) { return static_cast<int>(cudaMalloc(p, n)); }
-  static int free(void* p) { return static_cast<int>(cudaFree(p)); }
+  static int malloc_async(void** p, size_t n, Stream s) { return static_cast<int>(cudaMallocAsync(p, n, s)); }
+  static int free_async(void* p, Stream s) { return static_cast<int>(cudaFreeAsync(p, s)); }
   static int memset_async(void* p, size_t n, Stream s) { return static_cast<int>(cudaMemsetAsync(p, 0, n, s)); }
+  static int event_create(Event* e) { return static_cast<int>(cudaEventCreateWithFlags(e, cudaEventDisableTiming)); }
+  static int event_destroy(Event e) { return static_cast<int>(cudaEventDestroy(e)); }
+  static int event_record(Event e, Stream s) { return static_cast<int>(cudaEventRecord(e, s)); }
+  static int stream_wait_event(Stream s, Event e) { return static_cast<int>(cudaStreamWaitEvent(s, e, 0)); }
 };
 
 struct DeviceState {
@@ -54,7 +58,7 @@ struct DeviceState {
   bool supported = false;
   int num_sms = 0;
   uint32_t* status = nullptr;
-  dg::WorkspaceCache<cudaStream_t> workspaces;
+  dg::WorkspaceCache<cudaStream_t, cudaEvent_t> workspaces;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mutex;
@@ -117,24 +121,40 @@ dg::Params base_params(const DeviceState& ds, int M, int N, int K, int G, const 
 }
 
 // A workspace pointer and the lock that keeps it valid. Workspaces are freed only under
-// g_mutex, after a synchronisation (the device's, for a 17th stream; the stream's, to grow
-// one), and that synchronisation waits only for work already enqueued. A caller therefore
-// holds the lease until its kernels are launched: another host thread cannot free the
-// memory between the lookup and the launch.
+// g_mutex, in stream order after their last use (an event recorded once the kernels that use
+// them are enqueued). A caller therefore holds the lease until its kernels are launched and
+// done() has recorded that point: another host thread cannot evict the memory in between.
 struct WorkspaceLease {
   void* ptr = nullptr;
+  DeviceState* ds = nullptr;
+  size_t index = 0;
+  cudaStream_t stream = nullptr;
   std::unique_lock<std::mutex> lock;
+
+  // After the launches that use the workspace are enqueued (also on a failed launch).
+  void done() {
+    if (ds && lock.owns_lock()) {
+      dg::release<CudaApi>(ds->workspaces, index, stream);
+      lock.unlock();
+    }
+  }
+  ~WorkspaceLease() { done(); }
 };
 
-// Workspace of at least `bytes` for `stream` (policy in workspace_cache.h). The stream-K
-// arrival counters at its start are zero when allocated and left at zero by every completed
-// launch.
+// Workspace of at least `bytes` for `stream` (policy in workspace_cache.h): allocated in
+// stream order on the first call that needs it (or by dg_reserve_workspace), never with a
+// device or stream synchronisation. The stream-K arrival counters at its start are zero when
+// allocated and left at zero by every completed launch.
 dg_status stream_workspace(DeviceState& ds, cudaStream_t stream, size_t bytes, WorkspaceLease* out) {
   std::unique_lock<std::mutex> lock(g_mutex);
   void* ptr = nullptr;
-  if (const int e = dg::acquire<CudaApi, kMaxWorkspaces>(ds.workspaces, stream, bytes, &ptr))
+  size_t index = 0;
+  if (const int e = dg::acquire<CudaApi, kMaxWorkspaces>(ds.workspaces, stream, bytes, &ptr, &index))
     return cuda_fail(static_cast<cudaError_t>(e));
   out->ptr = ptr;
+  out->ds = &ds;
+  out->index = index;
+  out->stream = stream;
   out->lock = std::move(lock);
   return DG_OK;
 }
@@ -1372,6 +1392,31 @@ const char* dg_status_string(dg_status s) {
 }
 
 int dg_last_cuda_error(void) { return g_last_cuda_error; }
+
+dg_status dg_reserve_workspace(cudaStream_t stream, size_t bytes) {
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  const int e = dg::reserve<CudaApi, kMaxWorkspaces>(ds->workspaces, stream, bytes);
+  if (e < 0) return DG_ERR_INVALID_ARG;   // the stream is being captured
+  return e ? cuda_fail(static_cast<cudaError_t>(e)) : DG_OK;
+}
+
+dg_status dg_release_workspace(cudaStream_t stream) {
+  DeviceState* ds = nullptr;
+  if (dg_status s = device_state(&ds); s != DG_OK) return s;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  const int e = dg::reserve_release<CudaApi>(ds->workspaces, stream);
+  if (e < 0) return DG_ERR_INVALID_ARG;
+  return e ? cuda_fail(static_cast<cudaError_t>(e)) : DG_OK;
+}
+
+size_t dg_get_workspace_size(cudaStream_t stream) {
+  DeviceState* ds = nullptr;
+  if (device_state(&ds) != DG_OK) return 0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  return dg::workspace_bytes(ds->workspaces, stream);
+}
 
 dg_status dg_set_pdl(int enable) {
   if (enable != 0 && enable != 1) return DG_ERR_INVALID_ARG;

@@ -35,13 +35,13 @@
  *     be issued from several host threads.
  *   - Library-owned device memory: a 4-byte status word per device, and a workspace per
  *     (device, stream) for the paths that need one (stream-K partials, the CTA-pair kernel's
- *     scale chunks), grown on demand. At most 16 workspaces are cached per device; a call
- *     on a further stream synchronises the device and releases them.
+ *     scale chunks), allocated in stream order on demand or reserved up front with
+ *     dg_reserve_workspace (see there). No GEMM call synchronises the device or a stream.
  *   - CUDA graphs: a captured call uses the workspace its stream already has, so make one
  *     uncaptured call of at least the same size on the capturing stream first (allocating
- *     inside a capture works only in cudaStreamCaptureModeRelaxed). Nothing is synchronised
- *     or freed during a capture, and a workspace used in one is kept until the process exits,
- *     so replays stay valid however many streams come later.
+ *     inside a capture works only in cudaStreamCaptureModeRelaxed). Nothing is freed during a
+ *     capture, and a workspace used in one is kept until the process exits, so replays stay
+ *     valid however many streams come later.
  */
 #ifndef DG_H_
 #define DG_H_
@@ -315,6 +315,29 @@ int dg_get_tma_aligned_size(int mn, int elem_bytes);
  * exceeds the device's SM count. */
 dg_status dg_set_num_sms(int n);
 int dg_get_num_sms(void);
+
+/* Per-stream workspaces (no counterpart on the pages: memory management of this library).
+ * Some paths need device scratch beyond the caller's buffers: stream-K (partial tiles and
+ * arrival counters) and the CTA-pair kernel (scale chunks in the tensor-core copy layout, the
+ * contiguous form's pair-row list). The library keeps one workspace per (device, stream),
+ * allocated and freed in stream order (cudaMallocAsync / cudaFreeAsync): no GEMM call ever
+ * synchronises the device or a stream.
+ *   dg_reserve_workspace : makes the current device's workspace for `stream` at least `bytes`
+ *     now (allocating in stream order) and keeps it until dg_release_workspace. Afterwards a
+ *     GEMM call on that stream whose needs fit allocates, frees and synchronises nothing; a
+ *     call that needs more grows it (in stream order). bytes = 0 keeps what the stream has, so
+ *     one warm-up call followed by dg_reserve_workspace(stream, 0) pins that call's footprint.
+ *     Returns DG_ERR_INVALID_ARG while `stream` is being captured into a graph.
+ *   dg_release_workspace : frees it in `stream`'s order (call it before destroying a stream
+ *     that had one reserved). A workspace a captured graph refers to is kept until exit.
+ *   dg_get_workspace_size : its current size in bytes (0 if the stream has none).
+ * Workspaces that are not reserved are created by the first call that needs one; at most 16
+ * of them are kept per device, and a call on a further stream evicts the least recently used
+ * one after its last use (an event, not a synchronisation). A workspace used inside a graph
+ * capture is kept until the process exits. */
+dg_status dg_reserve_workspace(cudaStream_t stream, size_t bytes);
+dg_status dg_release_workspace(cudaStream_t stream);
+size_t dg_get_workspace_size(cudaStream_t stream);
 
 /* Programmatic dependent launch ("Utilities": set_pdl / get_pdl). When on, every GEMM
  * launch of the library (and the CTA-pair path's scale-preparation kernel) may begin its

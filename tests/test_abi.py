@@ -169,7 +169,7 @@ def test_binding_rejects_tensors_outside_the_current_device(lib):
 def _param_kind(param: str) -> str:
     if "*" in param or "cudaStream_t" in param:
         return "pointer"
-    if "unsigned long long" in param:
+    if "unsigned long long" in param or re.match(r"^\s*size_t\s+\w+$", param):
         return "u64"
     assert re.match(r"^(const\s+)?(int|dg_status)\s+\w+$", param.strip()), param
     return "int"
@@ -192,7 +192,7 @@ def declared_prototypes():
 def _ctypes_kind(t) -> str:
     if t is ctypes.c_void_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
         return "pointer"
-    if t is ctypes.c_ulonglong:
+    if t in (ctypes.c_ulonglong, ctypes.c_size_t):
         return "u64"
     assert t is ctypes.c_int, t
     return "int"

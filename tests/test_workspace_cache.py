@@ -1,9 +1,11 @@
 """The per-stream workspace cache policy (csrc/workspace_cache.h), checked on the host.
 
 tests/workspace_cache_check.cpp instantiates the policy with fake CUDA calls and walks
-through the situations that must stay safe: streams that come and go, a captured graph
-whose workspace must outlive any later eviction or growth, and captures during which
-nothing may be synchronised. No GPU is needed.
+through the situations that must stay safe: streams that come and go (evictions ordered after
+the evicted block's last use), reserved workspaces (no allocation, free or event on a call that
+fits), a captured graph whose workspace must outlive any later eviction, growth or release,
+and captures during which nothing may be freed. The fake API has no synchronisation call, so
+the policy cannot synchronise. No GPU is needed.
 """
 from __future__ import annotations
 

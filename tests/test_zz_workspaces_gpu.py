@@ -94,3 +94,57 @@ def test_host_threads_share_the_workspace_cache(lib):
         for i, bits in enumerate(outs):
             assert np.array_equal(bits, want), f"thread {t}, call {i}"
     assert lib.dg_get_device_status() == 0
+
+
+def test_reserved_workspace_calls_allocate_nothing(lib):
+    # a warm-up call sizes the stream's workspace, dg_reserve_workspace(0) pins it; later calls on
+    # that stream (while other streams come and go) leave the device's free memory unchanged
+    p, (a, sfa, b, sfb) = _operands(59)
+    s = torch.cuda.Stream()
+    d = sentinel_like((p.M, p.N))
+    with torch.cuda.stream(s):
+        lib.dg_fp8_gemm_nt(a, sfa, b, sfb, None, d)
+        lib.dg_reserve_workspace(0, stream=s)
+    torch.cuda.synchronize()
+    size = lib.dg_get_workspace_size(stream=s)
+    assert size > 0
+    want = bf16_bits(d)
+    outs = [sentinel_like((p.M, p.N)) for _ in range(8)]
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    with torch.cuda.stream(s):
+        for e in outs:
+            lib.dg_fp8_gemm_nt(a, sfa, b, sfb, None, e)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    for e in outs:
+        assert np.array_equal(bf16_bits(e), want)
+    # other streams churn through the cache; the reserved workspace is never evicted
+    for t in [torch.cuda.Stream() for _ in range(20)]:
+        with torch.cuda.stream(t):
+            lib.dg_fp8_gemm_nt(a, sfa, b, sfb, None, sentinel_like((p.M, p.N)))
+    torch.cuda.synchronize()
+    assert lib.dg_get_workspace_size(stream=s) == size
+    lib.dg_release_workspace(stream=s)
+    assert lib.dg_get_workspace_size(stream=s) == 0
+    assert lib.dg_get_device_status() == 0
+
+
+def test_reserve_up_front_then_first_call_allocates_nothing(lib):
+    p, (a, sfa, b, sfb) = _operands(60)
+    s = torch.cuda.Stream()
+    lib.dg_reserve_workspace(64 << 20, stream=s)        # well above what this shape needs
+    assert lib.dg_get_workspace_size(stream=s) >= 64 << 20
+    d = sentinel_like((p.M, p.N))
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    with torch.cuda.stream(s):
+        lib.dg_fp8_gemm_nt(a, sfa, b, sfb, None, d)      # the stream's first GEMM call
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    ref = sentinel_like((p.M, p.N))
+    lib.dg_fp8_gemm_nt(a, sfa, b, sfb, None, ref)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(d), bf16_bits(ref))
+    lib.dg_release_workspace(stream=s)
+    assert lib.dg_get_device_status() == 0
