@@ -63,3 +63,20 @@ def test_clock_summary():
     assert c["reasons"] == ["hw_slowdown", "sw_power_cap"] and c["reasons_under_load"] == ["sw_power_cap"]
     assert c["sm_mhz"] == 2040
     assert bench.summarize_clocks(["header only"]) is None
+
+
+def test_oracle_sample_rows_are_one_experts_valid_rows():
+    G, K, N = 3, 128, 16
+    m_idx = np.array([0] * 100 + [-1] * 28 + [1] * 40 + [-1] * 88 + [2] * 128, np.int32)
+    c = W.Contiguous(np.zeros((384, K), np.uint8), np.zeros((1, 384), np.int32), np.zeros((G, N, K), np.uint8),
+                     np.zeros((G, 1, 4), np.int32), m_idx, 384, N, K, G)
+    for call in range(7):
+        rows = bench.oracle_sample_rows(c, call, 32)
+        assert len(rows) == 32 and len(set(rows.tolist())) == 32
+        assert (m_idx[rows] == call % G).all()                 # valid rows of one expert, never padding
+
+
+def test_headline_is_the_largest_configuration():
+    # the contiguous G=8 workload: the most FLOPs of the five configurations
+    assert bench.HEADLINE == "contiguous_g8_t32768_n4096_k7168"
+    assert bench.HEADLINE_TRAFFIC["kernel"].startswith("pair 256x")

@@ -72,7 +72,11 @@ def test_reference_arm_prints_the_contract_line():
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "TFLOPS" and line["higher_is_better"] is True
     assert line["value"] > 0 and line["n_gpus"] == 1 and line["steps"] == 1 and line["warmup"] >= 3
-    assert line["config"]["workload"] == "dense_decode_128x7168x16384_c"
+    assert line["config"]["workload"] == "contiguous_g8_t32768_n4096_k7168"
+    # the same config block as the library's own arm (so the two lines describe one workload)
+    import bench
+    import workloads as W
+    assert line["config"] == bench.headline_config(W.make_workload(bench.HEADLINE), 1)
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "TFLOPS", "h2d_bytes_per_step": 0,
