@@ -277,6 +277,62 @@ def time_steps(torch, prob, steps, warmup, barrier=None, sustain_ms=0.0):
 # end to end through the C ABI with host buffers
 # --------------------------------------------------------------------------------------
 
+def library_context(torch, lib, reps=20):
+    """cuBLAS FP8 GEMMs (torch._scaled_mm) and this library's dense GEMM on one dense shape with
+    the headline's padded rows, N and K (33152 x 4096 x 7168; random E4M3 on the device, unit
+    scales): context for the headline, not on its path. Per-tensor-scaled FP8 does no block
+    scaling; MXFP8 scales every 32 K (finer than this library's 1 x 128 / 128 x 128). Each:
+    TFLOPS over `reps` back-to-back calls after 3 warm-up calls, CUDA events."""
+    t = torch
+    M, N, K = 33152, 4096, 7168
+    flops = 2.0 * M * N * K
+    out = {"shape": f"{M}x{N}x{K}"}
+    try:
+        a = t.randn(M, K, device="cuda").to(t.float8_e4m3fn)
+        b = t.randn(N, K, device="cuda").to(t.float8_e4m3fn)
+    except Exception as e:  # reported, never fatal
+        return dict(out, error=str(e)[:200])
+
+    def timed(fn):
+        s = t.cuda.Stream()
+        with t.cuda.stream(s):
+            for _ in range(3):
+                fn()
+            e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(reps):
+                fn()
+            e1.record(s)
+        t.cuda.synchronize()
+        return flops * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+
+    one = t.ones((), device="cuda")
+    try:
+        out["cublas_fp8_per_tensor_tflops"] = timed(
+            lambda: t._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=t.bfloat16))
+    except Exception as e:
+        out["cublas_fp8_per_tensor_tflops"] = f"failed: {str(e)[:120]}"
+    try:
+        kq = -(-(K // 32) // 4) * 4
+        sa = t.full((-(-M // 128) * 128 * kq,), 127, dtype=t.uint8, device="cuda").view(t.float8_e8m0fnu)
+        sb = t.full((-(-N // 128) * 128 * kq,), 127, dtype=t.uint8, device="cuda").view(t.float8_e8m0fnu)
+        out["cublas_mxfp8_tflops"] = timed(lambda: t._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=t.bfloat16))
+    except Exception as e:
+        out["cublas_mxfp8_tflops"] = f"failed: {str(e)[:120]}"
+    try:
+        kp = -(-(K // 128) // 4)
+        sfa = t.full((kp, -(-M // 4) * 4), 0x7F7F7F7F, dtype=t.int32, device="cuda")
+        nb = -(-N // 128)
+        sfb = t.full((kp, -(-nb // 4) * 4), 0x7F7F7F7F, dtype=t.int32, device="cuda")
+        d = t.empty(M, N, dtype=t.bfloat16, device="cuda")
+        out["this_library_dense_tflops"] = timed(lambda: lib.dg_fp8_gemm_nt(a, sfa, b, sfb, None, d))
+    except Exception as e:
+        out["this_library_dense_tflops"] = f"failed: {str(e)[:120]}"
+    del a, b
+    t.cuda.empty_cache()
+    return out
+
+
 def e2e_headline(torch, lib, p, steps, warmup):
     """The headline GEMM as a serving loop runs it from host memory, through the public API:
     every step copies the step's inputs (A, its scales, the experts' B and scales, the
@@ -551,6 +607,7 @@ def main():
             torch.cuda.empty_cache()
         if L.dg_get_device_status() != 0:
             raise RuntimeError("device status reported an error during the benchmark")
+    context = None if args.headline_only else library_context(torch, L)
     clocks = sampler.stop()
 
     e2e = e2e_headline(torch, L, p, max(3, min(args.steps, 20)), 2)
@@ -611,6 +668,7 @@ def main():
         "harness_check": {"copy_gbs": copy_gbs, "hbm_peak_gbs": peaks["hbm_gbs"],
                           "how": "1 GiB device-to-device copy (torch), 10 reps, CUDA events on the launching "
                                  "stream, read + write bytes: the timing method against a known-size transfer"},
+        "library_context": context,
         "workloads_how": ("each workload: about 0.2 s of back-to-back launches in one graph replay; tflops = "
                           "algorithmic FLOPs / time; us per launch; f_ceil = tflops / the measured FP8 ceiling; "
                           "f_hbm = algorithmic bytes / time / measured HBM copy bandwidth"),
