@@ -511,7 +511,7 @@ def pin_golden(O_):
 
 def pin_parity_report(O_):
     """The comparator every GPU parity check goes through, on hand-worked cases: each
-    expected verdict follows from the bound |d - ref| <= rel*|ref| + abs_rms*rms(ref) (rms
+    expected outcome follows from the bound |d - ref| <= rel*|ref| + abs_rms*rms(ref) (rms
     over ref) and the strict cosine-style bar, computed here by hand."""
     pr = O_.parity_report
     # ref = [1, 7]: rms = sqrt((1 + 49) / 2) = 5, so element 0's bound is 0.01 + 0.05 = 0.06
